@@ -1,0 +1,367 @@
+#!/usr/bin/env python
+"""Benchmark of one fused DSA decode step on GB300.
+
+Workload (default): batch 32 requests, 131072-token context each, indexer
+64 heads x 128 dims in fp8 e4m3 with per-row scales, top-k 2048, sparse MLA
+with 64 heads over 576-wide bf16 latent rows (Dv 512).  Synthetic, seeded
+inputs.  One step = index score -> top-k -> sparse MLA (-> split combine) for
+all 32 requests, through the C ABI entry point dsa_decode.
+
+Timing: W warm-up steps, then K steps each bracketed by CUDA events on the
+launching stream; between timed steps a 256 MiB buffer is written to flush
+the L2 (the flush is outside the events).  Multi-GPU runs (torchrun) are
+independent replicas: the path does not shard across GPUs.
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead (the
+reference arm), on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA decode/prefill µs per step (score+topk+attn); % of GB300 HBM roofline"
+UNIT = "us/step"
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def workload_config(B, N, k):
+    return {"workload": "decode_b%d_n%d" % (B, N), "batch": B, "context": N, "topk": k,
+            "heads": 64, "index_heads": 64, "index_dim": 128, "index_dtype": "fp8_e4m3",
+            "kv_format": "bf16 latent 576 (Dv 512)",
+            "l2": "flushed between timed steps (256 MiB write); index-k sweep 553 MB > L2",
+            "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world):
+    import torch
+    from deepseek_sparse_attention_index_gb300 import build as B
+    from deepseek_sparse_attention_index_gb300 import inputs as I
+    from deepseek_sparse_attention_index_gb300 import ops
+
+    if rank == 0 or not os.path.exists(B.LIB):
+        B.build()
+    if world > 1:
+        torch.distributed.barrier()
+    ops.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    Bsz, N, k = args.batch, args.context, 2048
+    case = I.decode_sweep(Bsz, N, device=dev, seed=rank)
+    ind = case.indexer
+    H, Dv = case.H, case.Dv
+    ws = ops.workspace(ops.dsa_decode_workspace_size(Bsz, N, k, H, Dv), dev)
+    idx_out = torch.empty((Bsz, k), dtype=torch.int32, device=dev)
+    out = torch.empty((Bsz, H, Dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Bsz, H), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ops.decode_case(case, ws=ws, idx_out=idx_out, out=out, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K fused steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    us_per_step = total_ms * 1000.0 / args.steps
+
+    # ---- staged pass: the three stages as separate entry points, events around each
+    rs = case.slot_base
+    re = (case.slot_base + case.seq_lens).contiguous()
+    ld = (N + 3) // 4 * 4
+    scores = torch.empty((Bsz, ld), dtype=torch.float32, device=dev)
+    tws = ops.workspace(ops.dsa_topk_workspace_size(Bsz, N, k), dev)
+    mws = ops.workspace(ops.dsa_sparse_mla_workspace_size(Bsz, H, Dv, k, 0), dev)
+    stage_ms = {"index_score": [], "topk": [], "sparse_mla": []}
+    for i in range(max(3, min(args.steps, 10))):
+        flush.fill_(i & 0xff)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        ops.dsa_index_score(ind["q_idx"], ind["idx_dtype"], ind["q_scale"], ind["k_idx"],
+                            ind["k_scale"], ind["w"], rs, re, N, scores=scores)
+        e[1].record(stream)
+        ops.dsa_topk(scores, case.seq_lens, k, N, index_base=case.slot_base, idx=idx_out, ws=tws)
+        e[2].record(stream)
+        ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, idx_out, out=out, lse=lse,
+                               ws=mws)
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        stage_ms["index_score"].append(e[0].elapsed_time(e[1]))
+        stage_ms["topk"].append(e[1].elapsed_time(e[2]))
+        stage_ms["sparse_mla"].append(e[2].elapsed_time(e[3]))
+    stage_us = {s: 1000.0 * statistics.median(v) for s, v in stage_ms.items()}
+
+    # algorithmic bytes (per launch) of the dominant kernel, the index score:
+    # per key 128 B fp8 + 4 B scale read, 4 B score written
+    hbm_gbs, _, peak_kind = measured_peaks()
+    idx_bytes = Bsz * N * (128 + 4 + 4) + Bsz * 64 * (128 + 8)
+    idx_gbs = idx_bytes / (stage_us["index_score"] * 1e-6) / 1e9
+    # whole-step algorithmic bytes: keys + scores + gathered KV rows + q/out/lse
+    rows = Bsz * min(N, k)
+    step_bytes = idx_bytes + rows * 1152 + Bsz * H * (576 * 2 + Dv * 2 + 4)
+    step_gbs = step_bytes / (us_per_step * 1e-6) / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "index_score_traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            traffic = json.load(f).get("bytes_per_launch_full_size")
+
+    # ---- e2e: host buffers, per-step inputs copied in and results copied out
+    pin = lambda t: t.detach().cpu().pin_memory()
+    h_in = {"q_idx": pin(ind["q_idx"]), "q_scale": pin(ind["q_scale"]), "w": pin(ind["w"]),
+            "q": pin(case.q), "seq_lens": pin(case.seq_lens), "slot_base": pin(case.slot_base)}
+    d_in = {n: torch.empty_like(t, device=dev) for n, t in h_in.items()}
+    h_out = {"idx": torch.empty_like(idx_out, device="cpu").pin_memory(),
+             "out": torch.empty_like(out, device="cpu").pin_memory(),
+             "lse": torch.empty_like(lse, device="cpu").pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        for n in h_in:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        ops.dsa_decode(d_in["q_idx"], ind["idx_dtype"], d_in["q_scale"], ind["k_idx"],
+                       ind["k_scale"], d_in["w"], d_in["seq_lens"], d_in["slot_base"], N, k,
+                       d_in["q"], case.softmax_scale, case.kv, idx_out=idx_out, out=out, lse=lse,
+                       ws=ws)
+        h_out["idx"].copy_(idx_out, non_blocking=True)
+        h_out["out"].copy_(out, non_blocking=True)
+        h_out["lse"].copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms.append((time.perf_counter() - t0) * 1000.0)
+    e2e_us = 1000.0 * statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_us], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_us = float(t.item())
+
+    splits = 1 if ops.dsa_sparse_mla_workspace_size(Bsz, H, Dv, k, 0) == 0 else 2
+    launches_per_step = 1 + 1 + 1 + 1 + (1 if splits > 1 else 0)
+
+    res = {
+        "metric": METRIC, "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_per_step / 1000, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 indexer + bf16 attention (fp32 accumulate)", "data": "synthetic",
+        "config": workload_config(Bsz, N, k),
+        "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": round(idx_gbs, 1),
+                     "peak": hbm_gbs, "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
+                     "unit": "GB/s", "frac": round(idx_gbs / hbm_gbs, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": idx_bytes,
+                     "launch_us": round(stage_us["index_score"], 2)},
+        "step_roofline": {"achieved_gbs": round(step_gbs, 1), "frac": round(step_gbs / hbm_gbs, 4),
+                          "algorithmic_bytes_per_step": step_bytes},
+        "stages_us": {s: round(v, 2) for s, v in stage_us.items()},
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "note": "per-step inputs from pinned host memory, results back to host; the "
+                        "index-k cache and KV pool stay resident in HBM as model state"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    return res
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+
+def oracle_sample(B, N, n_req, seed=1):
+    """Time the CPU oracle on n_req requests of a (B, N) decode; returns
+    (seconds per request, sample description)."""
+    import numpy as np
+    import torch
+    import oracle.dsa_oracle as O
+    from deepseek_sparse_attention_index_gb300 import inputs as I
+    from tests.helpers import decode_case_np
+    case = I.decode_sweep(n_req, N, device="cpu", seed=seed)
+    c = decode_case_np(case)
+    t0 = time.perf_counter()
+    for b in range(n_req):
+        O.decode_request(b, c)
+    dt = (time.perf_counter() - t0) / n_req
+    return dt, "%d of the %d requests (context %d, full index sweep, sort and attention each)" % (
+        n_req, B, N)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    Bsz, N = args.batch, args.context
+    n_req = 2
+    per_req, sample = oracle_sample(Bsz, N, n_req)
+    # steps: each step times a bounded sample (one request) and scales to the batch
+    for _ in range(args.warmup):
+        pass
+    per = []
+    import oracle.dsa_oracle as O
+    from deepseek_sparse_attention_index_gb300 import inputs as I
+    from tests.helpers import decode_case_np
+    case = decode_case_np(I.decode_sweep(1, N, device="cpu", seed=2))
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        O.decode_request(0, case)
+        per.append(time.perf_counter() - t0)
+    us = statistics.mean(per) * Bsz * 1e6
+    res = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1000, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(Bsz, N, 2048),
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cpu_cores(),
+                         "kind": "oracle",
+                         "sample": "each step: 1 of the %d requests (context %d), scaled x%d"
+                                   % (Bsz, N, Bsz)},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=32)
+    ap.add_argument("--context", type=int, default=131072)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            per_req, sample = oracle_sample(args.batch, args.context, 2)
+            us = per_req * args.batch * 1e6
+            res["cpu_baseline"] = {"value": round(us, 1), "unit": UNIT, "cores": cpu_cores(),
+                                   "kind": "oracle", "sample": sample + ", scaled to the batch"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,96 @@
+// Shared device helpers for the DSA kernels (sm_103a).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+#define DSA_DEVINLINE __device__ __forceinline__
+
+namespace dsa {
+
+// ---------------------------------------------------------------- errors
+
+DSA_DEVINLINE void raise_flag(int32_t *err_flag, int32_t bits) {
+  if (err_flag) atomicOr(err_flag, bits);
+}
+
+// ---------------------------------------------------------------- numbers
+
+DSA_DEVINLINE float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Two OCP e4m3 bytes (low byte first) -> two floats, exact.
+DSA_DEVINLINE float2 e4m3x2_to_float2(uint16_t two) {
+  __nv_fp8x2_storage_t s = two;
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(s, __NV_E4M3);
+  return __half22float2(*reinterpret_cast<__half2 *>(&h));
+}
+
+DSA_DEVINLINE float e4m3_to_float(uint8_t b) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw(b, __NV_E4M3);
+  return __half2float(*reinterpret_cast<__half *>(&h));
+}
+
+// UE8M0 exponent byte -> 2^(e - 127).  e = 0 gives 2^-127 (an fp32 subnormal);
+// e = 255 (NaN in the MX encoding) is not produced by the formats here.
+DSA_DEVINLINE float ue8m0_to_float(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+// Order-preserving map fp32 -> uint32: a > b (as floats) iff key(a) > key(b).
+// -0.0 is first turned into +0.0 so the two tie.
+DSA_DEVINLINE uint32_t score_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u << 1) == 0) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+DSA_DEVINLINE unsigned lane_id() { return threadIdx.x & 31; }
+
+// Pack two floats to a bf16x2 word (round to nearest even), low half = a.
+DSA_DEVINLINE uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+}  // namespace dsa
+
+// ---------------------------------------------------------------- host side
+namespace dsa {
+
+// Round x up to a multiple of a (a power of two).
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) & ~(a - 1); }
+
+// Carves aligned sub-buffers out of a caller workspace.
+struct WsCarver {
+  char *base;
+  size_t off = 0;
+  explicit WsCarver(void *p) : base(static_cast<char *>(p)) {}
+  template <typename T>
+  T *take(size_t count) {
+    off = align_up(off, 256);
+    T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+  size_t bytes() const { return align_up(off, 256); }
+};
+
+inline int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+  }
+  return n;
+}
+
+}  // namespace dsa

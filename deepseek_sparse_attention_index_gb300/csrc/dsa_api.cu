@@ -1,0 +1,254 @@
+// C ABI of the DSA forward hot path (declarations and contracts: include/dsa.h).
+// Host side only: argument checks, workspace carving and stream-ordered
+// launches of the kernels in index_score.cu, topk.cu and sparse_mla.cu.
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace dsa;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_kv(const dsa_kv_pool *kv, int D) {
+  if (!kv || !kv->data || kv->rows < 0) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(kv->data)) return DSA_ERR_INVALID_ARG;
+  if (kv->d_nope + kv->d_rope != D || kv->d_rope != 64) return DSA_ERR_UNSUPPORTED;
+  switch (kv->format) {
+    case DSA_KV_BF16:
+      if (D != 576) return DSA_ERR_UNSUPPORTED;
+      return DSA_OK;
+    case DSA_KV_FP8_UNIFORM:
+      if (D != 512) return DSA_ERR_UNSUPPORTED;
+      if (!kv->scales) return DSA_ERR_INVALID_ARG;
+      return DSA_OK;
+    case DSA_KV_FP8_DS_MLA:
+      if (D != 512 || kv->d_nope != 448) return DSA_ERR_UNSUPPORTED;
+      if (kv->block <= 0 || (kv->block & 1)) return DSA_ERR_UNSUPPORTED;
+      if (kv->rows % kv->block) return DSA_ERR_INVALID_ARG;
+      return DSA_OK;
+    default:
+      return DSA_ERR_UNSUPPORTED;
+  }
+}
+
+PoolDev to_dev(const dsa_kv_pool *kv) {
+  PoolDev p{};
+  if (!kv) return p;
+  p.data = static_cast<const uint8_t *>(kv->data);
+  p.scales = kv->scales;
+  p.rows = kv->rows;
+  p.format = kv->format;
+  p.block = kv->block > 0 ? kv->block : 1;
+  return p;
+}
+
+int check_indexer(const void *q_idx, int idx_dtype, const float *q_scale, const void *k_idx,
+                  const float *k_scale, int64_t k_rows, const float *w, int T, int H_I, int d) {
+  if (T < 0 || k_rows < 0) return DSA_ERR_INVALID_ARG;
+  if (T > 0 && (!q_idx || !k_idx || !w)) return DSA_ERR_INVALID_ARG;
+  if (H_I < 1 || H_I > DSA_MAX_INDEX_HEADS || (H_I % 8)) return DSA_ERR_UNSUPPORTED;
+  if (idx_dtype == DSA_IDX_FP8_E4M3) {
+    if (d != 128) return DSA_ERR_UNSUPPORTED;
+    if (T > 0 && (!q_scale || !k_scale)) return DSA_ERR_INVALID_ARG;
+  } else if (idx_dtype == DSA_IDX_BF16) {
+    if (d != 64 && d != 128) return DSA_ERR_UNSUPPORTED;
+  } else {
+    return DSA_ERR_UNSUPPORTED;
+  }
+  if (!aligned16(k_idx) || !aligned16(q_idx)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+int check_mla_shape(const void *q, int T, int H, int D, int Dv, const dsa_kv_pool *kv,
+                    const int32_t *idx, int k, const dsa_kv_pool *kv2, const int32_t *idx2,
+                    int k2, const void *out, const float *lse, bool need_idx = true) {
+  if (T < 0 || k < 0 || k2 < 0) return DSA_ERR_INVALID_ARG;
+  if (H < 1 || H > DSA_MAX_HEADS) return DSA_ERR_UNSUPPORTED;
+  if (!((D == 576 && Dv == 512) || (D == 512 && Dv == 448))) return DSA_ERR_UNSUPPORTED;
+  if (k + k2 < 1) return DSA_ERR_INVALID_ARG;
+  if (T > 0 && (!q || !out || !lse)) return DSA_ERR_INVALID_ARG;
+  if (need_idx && k > 0 && T > 0 && !idx) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+  int st = check_kv(kv, D);
+  if (st != DSA_OK) return st;
+  if (k2 > 0) {
+    if (!idx2) return DSA_ERR_INVALID_ARG;
+    st = check_kv(kv2, D);
+    if (st != DSA_OK) return st;
+  }
+  return DSA_OK;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+int64_t scores_ld(int64_t max_len) { return (max_len + 3) & ~int64_t(3); }
+
+struct DecodeLayout {
+  float *scores;
+  TopkWs topk;
+  int32_t *idx;
+  float *part_o, *part_lse;
+  size_t bytes;
+};
+
+DecodeLayout decode_layout(int B, int64_t max_seq_len, int k, int H, int Dv, int k_swa,
+                           void *ws) {
+  DecodeLayout L{};
+  WsCarver c(ws);
+  L.scores = c.take<float>((size_t)B * scores_ld(max_seq_len));
+  size_t tb = topk_ws_layout(B, k, nullptr, nullptr);
+  char *tp = c.take<char>(tb);
+  topk_ws_layout(B, k, tp, &L.topk);
+  L.idx = c.take<int32_t>((size_t)B * k);
+  size_t mb = mla_ws_bytes(B, H, Dv, k + k_swa);
+  char *mp = c.take<char>(mb);
+  if (ws) mla_ws_layout(B, H, Dv, k + k_swa, mp, &L.part_o, &L.part_lse);
+  L.bytes = c.bytes();
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case DSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case DSA_ERR_CUDA: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+int dsa_abi_version(void) { return 1; }
+
+int dsa_index_score(const void *q_idx, int idx_dtype, const float *q_scale, const void *k_idx,
+                    const float *k_scale, int64_t k_rows, const float *w,
+                    const int32_t *row_start, const int32_t *row_end, int T, int H_I, int d,
+                    int64_t max_len, float *scores, int64_t ld_scores, int32_t *err_flag,
+                    dsa_stream_t stream) {
+  int st = check_indexer(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, T, H_I, d);
+  if (st != DSA_OK) return st;
+  if (max_len < 0 || ld_scores < max_len) return DSA_ERR_INVALID_ARG;
+  if (T > 0 && (!row_start || !row_end || !scores)) return DSA_ERR_INVALID_ARG;
+  IndexScoreArgs a{};
+  a.q_idx = q_idx; a.idx_dtype = idx_dtype; a.q_scale = q_scale;
+  a.k_idx = k_idx; a.k_scale = k_scale; a.k_rows = k_rows; a.w = w;
+  a.row_start = row_start; a.row_end = row_end;
+  a.T = T; a.H_I = H_I; a.d = d; a.max_len = max_len;
+  a.scores = scores; a.ld_scores = ld_scores; a.err_flag = err_flag;
+  return status_of(index_score_launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t dsa_topk_workspace_size(int T, int64_t max_len, int k) {
+  (void)max_len;
+  if (T <= 0 || k <= 0) return 0;
+  return topk_ws_layout(T, k, nullptr, nullptr);
+}
+
+int dsa_topk(const float *scores, int64_t ld_scores, const int32_t *row_len, int T,
+             int64_t max_len, int k, const int32_t *index_base, int32_t *idx, int32_t *lens,
+             void *ws, size_t ws_bytes, int32_t *err_flag, dsa_stream_t stream) {
+  if (T < 0 || max_len < 0 || ld_scores < max_len) return DSA_ERR_INVALID_ARG;
+  if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!scores || !row_len || !idx) return DSA_ERR_INVALID_ARG;
+  const size_t need = dsa_topk_workspace_size(T, max_len, k);
+  if (ws_bytes < need || (need && !ws)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  TopkWs w;
+  topk_ws_layout(T, k, ws, &w);
+  cudaError_t e = topk_clear(w, T, s);
+  if (e == cudaSuccess) e = topk_hist(scores, ld_scores, row_len, T, max_len, k, w, s);
+  if (e == cudaSuccess)
+    e = topk_select(scores, ld_scores, row_len, T, max_len, k, index_base, idx, lens, w,
+                    err_flag, s);
+  return status_of(e);
+}
+
+size_t dsa_sparse_mla_workspace_size(int T, int H, int Dv, int k, int k2) {
+  if (T <= 0 || H <= 0 || k + k2 <= 0) return 0;
+  return mla_ws_bytes(T, H, Dv, k + k2);
+}
+
+int dsa_sparse_mla_fwd(const void *q, int T, int H, int D, int Dv, float softmax_scale,
+                       const dsa_kv_pool *kv, const int32_t *idx, int k,
+                       const dsa_kv_pool *kv_extra, const int32_t *idx_extra, int k2,
+                       void *out, float *lse, void *ws, size_t ws_bytes, int32_t *err_flag,
+                       dsa_stream_t stream) {
+  int st = check_mla_shape(q, T, H, D, Dv, kv, idx, k, kv_extra, idx_extra, k2, out, lse);
+  if (st != DSA_OK) return st;
+  if (T == 0) return DSA_OK;
+  const size_t need = dsa_sparse_mla_workspace_size(T, H, Dv, k, k2);
+  if (ws_bytes < need || (need && !ws)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  MlaArgs a{};
+  a.q = q; a.T = T; a.H = H; a.D = D; a.Dv = Dv; a.softmax_scale = softmax_scale;
+  a.kv = to_dev(kv); a.idx = idx; a.k = k;
+  a.kv2 = to_dev(k2 > 0 ? kv_extra : nullptr); a.idx2 = k2 > 0 ? idx_extra : nullptr; a.k2 = k2;
+  a.out = out; a.lse = lse; a.err_flag = err_flag;
+  a.n_splits = mla_num_splits(T, H, k + k2);
+  if (a.n_splits > 1) mla_ws_layout(T, H, Dv, k + k2, ws, &a.part_o, &a.part_lse);
+  return status_of(sparse_mla_launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t dsa_decode_workspace_size(int B, int64_t max_seq_len, int k, int H, int Dv, int k_swa) {
+  if (B <= 0 || k <= 0 || H <= 0 || max_seq_len < 0 || k_swa < 0) return 0;
+  return decode_layout(B, max_seq_len, k, H, Dv, k_swa, nullptr).bytes;
+}
+
+int dsa_decode(const void *q_idx, int idx_dtype, const float *q_scale, const void *k_idx,
+               const float *k_scale, int64_t k_rows, const float *w, int H_I, int d_idx, int B,
+               const int32_t *seq_lens, const int32_t *slot_base, int64_t max_seq_len, int k,
+               const void *q, int H, int D, int Dv, float softmax_scale, const dsa_kv_pool *kv,
+               const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa, int32_t *idx_out,
+               void *out, float *lse, void *ws, size_t ws_bytes, int32_t *err_flag,
+               dsa_stream_t stream) {
+  if (B < 0 || max_seq_len < 0) return DSA_ERR_INVALID_ARG;
+  if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  int st = check_indexer(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, B, H_I, d_idx);
+  if (st != DSA_OK) return st;
+  // idx_out is optional: the selection then lives in the workspace
+  st = check_mla_shape(q, B, H, D, Dv, kv, idx_out, k, kv_swa, idx_swa, k_swa, out, lse,
+                       /*need_idx=*/false);
+  if (st != DSA_OK) return st;
+  if (B == 0) return DSA_OK;
+  if (!seq_lens || !slot_base) return DSA_ERR_INVALID_ARG;
+  const size_t need = dsa_decode_workspace_size(B, max_seq_len, k, H, Dv, k_swa);
+  if (ws_bytes < need || !ws) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DecodeLayout L = decode_layout(B, max_seq_len, k, H, Dv, k_swa, ws);
+  const int64_t ld = scores_ld(max_seq_len);
+  int32_t *idx = idx_out ? idx_out : L.idx;
+
+  cudaError_t e = topk_clear(L.topk, B, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  IndexScoreArgs ia{};
+  ia.q_idx = q_idx; ia.idx_dtype = idx_dtype; ia.q_scale = q_scale;
+  ia.k_idx = k_idx; ia.k_scale = k_scale; ia.k_rows = k_rows; ia.w = w;
+  ia.slot_base = slot_base; ia.seq_lens = seq_lens;
+  ia.T = B; ia.H_I = H_I; ia.d = d_idx; ia.max_len = max_seq_len;
+  ia.scores = L.scores; ia.ld_scores = ld; ia.hist = L.topk.hist; ia.topk_k = k;
+  ia.err_flag = err_flag;
+  e = index_score_launch(ia, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  e = topk_select(L.scores, ld, seq_lens, B, max_seq_len, k, slot_base, idx, nullptr, L.topk,
+                  err_flag, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  MlaArgs a{};
+  a.q = q; a.T = B; a.H = H; a.D = D; a.Dv = Dv; a.softmax_scale = softmax_scale;
+  a.kv = to_dev(kv); a.idx = idx; a.k = k;
+  a.kv2 = to_dev(k_swa > 0 ? kv_swa : nullptr); a.idx2 = k_swa > 0 ? idx_swa : nullptr;
+  a.k2 = k_swa;
+  a.out = out; a.lse = lse; a.err_flag = err_flag;
+  a.n_splits = mla_num_splits(B, H, k + k_swa);
+  a.part_o = L.part_o; a.part_lse = L.part_lse;
+  return status_of(sparse_mla_launch(a, s));
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// Internal launchers shared by the C-ABI layer (dsa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// ------------------------------------------------------------------ top-k
+constexpr int kHistBins = 4096;   // first radix level: top 12 bits of the key
+constexpr int kCandCap = 8192;    // candidates per row kept for the resolve pass
+
+struct TopkWs {
+  uint32_t *hist;    // [T][kHistBins]        zeroed before the histogram pass
+  uint32_t *cnt;     // [T][2] (gt, eq)       zeroed before the collect pass
+  int32_t *gt_list;  // [T][k]
+  uint2 *cand;       // [T][kCandCap]  (key, position)
+};
+size_t topk_ws_layout(int T, int k, void *ws, TopkWs *out);  // returns bytes
+
+// Clears hist and cnt (one memset each, stream-ordered).
+cudaError_t topk_clear(const TopkWs &w, int T, cudaStream_t s);
+// Histogram pass over a score matrix (the standalone entry point; the fused
+// decode builds the histogram in the index-score epilogue instead).
+cudaError_t topk_hist(const float *scores, int64_t ld, const int32_t *row_len, int T,
+                      int64_t max_len, int k, const TopkWs &w, cudaStream_t s);
+cudaError_t topk_select(const float *scores, int64_t ld, const int32_t *row_len, int T,
+                        int64_t max_len, int k, const int32_t *index_base, int32_t *idx,
+                        int32_t *lens, const TopkWs &w, int32_t *err_flag, cudaStream_t s);
+
+// ------------------------------------------------------------------ index score
+struct IndexScoreArgs {
+  const void *q_idx;
+  int idx_dtype;
+  const float *q_scale;
+  const void *k_idx;
+  const float *k_scale;
+  int64_t k_rows;
+  const float *w;
+  const int32_t *row_start;  // [T] (or NULL when slot_base/seq_lens are used)
+  const int32_t *row_end;    // [T]
+  const int32_t *slot_base;  // decode form: rows [slot_base[t], slot_base[t]+seq_lens[t])
+  const int32_t *seq_lens;
+  int T, H_I, d;
+  int64_t max_len;
+  float *scores;
+  int64_t ld_scores;
+  uint32_t *hist;            // optional [T][kHistBins]: fused top-k histogram
+  int topk_k;                // rows of length <= topk_k skip the histogram
+  int32_t *err_flag;
+};
+cudaError_t index_score_launch(const IndexScoreArgs &a, cudaStream_t s);
+
+// ------------------------------------------------------------------ sparse MLA
+struct PoolDev {
+  const uint8_t *data;
+  const float *scales;
+  int64_t rows;
+  int format;
+  int block;
+};
+
+struct MlaArgs {
+  const void *q;             // bf16 [T, H, D]
+  int T, H, D, Dv;
+  float softmax_scale;
+  PoolDev kv, kv2;
+  const int32_t *idx;        // [T, k]
+  int k;
+  const int32_t *idx2;       // [T, k2] or NULL
+  int k2;
+  void *out;                 // bf16 [T, H, Dv]
+  float *lse;                // [T, H]
+  float *part_o;             // workspace partials
+  float *part_lse;
+  int n_splits;
+  int32_t *err_flag;
+};
+int mla_num_splits(int T, int H, int k_total);
+size_t mla_ws_bytes(int T, int H, int Dv, int k_total);
+void mla_ws_layout(int T, int H, int Dv, int k_total, void *ws, float **part_o, float **part_lse);
+cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s);
+
+}  // namespace dsa

@@ -1,0 +1,324 @@
+// Absorbed-MLA sparse attention forward over gathered latent rows
+// (the "sparse attn" stage of tokenspeed PR #627 "Add gluon kernel for DSA";
+// semantics of miles PR #3608: natural-log lse, -1 entries masked; pool
+// formats and the two-loop list of aiter PR #4382).
+//
+// Split-KV: the concatenated list (idx then idx2) of a token is cut into
+// n_splits pieces; each CTA handles one (token, piece, group of <= 64 heads)
+// with an online softmax and writes a normalised partial output and its lse;
+// a combine kernel merges the pieces (lse = ln sum exp lse_i, out = sum
+// exp(lse_i - lse) out_i).  With one piece the CTA writes the result itself.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRows = 8;        // rows gathered per step
+constexpr int kHeadsPerCta = 64;
+constexpr int kKStride = 580;   // float row stride of the gathered tile (bank spread)
+constexpr int kQStride = 584;   // bf16 row stride of q in shared memory
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Fetch list entry j (of the concatenated list) for token t: slot and pool.
+struct ListRef {
+  const PoolDev *pool;
+  int64_t slot;
+};
+
+__device__ __forceinline__ ListRef list_entry(const MlaArgs &a, int t, int j) {
+  ListRef r;
+  if (j < a.k) {
+    r.pool = &a.kv;
+    r.slot = a.idx[(size_t)t * a.k + j];
+  } else {
+    r.pool = &a.kv2;
+    r.slot = a.idx2[(size_t)t * a.k2 + (j - a.k)];
+  }
+  return r;
+}
+
+// Dequantise one latent row into dst[0..D) (fp32).  32 threads (one warp).
+__device__ __forceinline__ void load_row(const PoolDev &p, int64_t slot, int D, float *dst) {
+  const unsigned lane = lane_id();
+  if (p.format == DSA_KV_BF16) {
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(p.data + slot * (int64_t)D * 2);
+    for (int c = 2 * lane; c < D; c += 64) {
+      const uint32_t v = __ldg(src + c / 2);
+      dst[c] = __uint_as_float(v << 16);
+      dst[c + 1] = __uint_as_float(v & 0xffff0000u);
+    }
+  } else if (p.format == DSA_KV_FP8_UNIFORM) {
+    const uint16_t *src = reinterpret_cast<const uint16_t *>(p.data + slot * (int64_t)D);
+    const float *sc = p.scales + slot * (int64_t)(D / 64);
+    for (int c = 2 * lane; c < D; c += 64) {
+      const float s = __ldg(sc + c / 64);
+      const float2 v = e4m3x2_to_float2(__ldg(src + c / 2));
+      dst[c] = v.x * s;
+      dst[c + 1] = v.y * s;
+    }
+  } else {  // fp8_ds_mla: 448 NoPE fp8 + 64 RoPE bf16, UE8M0 per 64 NoPE dims
+    const int64_t page = slot / p.block, pos = slot % p.block;
+    const uint8_t *pg = p.data + page * (int64_t)p.block * 584;
+    const uint8_t *row = pg + pos * 576;
+    const uint8_t *ex = pg + (int64_t)p.block * 576 + pos * 8;
+    const uint16_t *nope = reinterpret_cast<const uint16_t *>(row);
+    for (int c = 2 * lane; c < 448; c += 64) {
+      const float s = ue8m0_to_float(__ldg(ex + c / 64));
+      const float2 v = e4m3x2_to_float2(__ldg(nope + c / 2));
+      dst[c] = v.x * s;
+      dst[c + 1] = v.y * s;
+    }
+    const uint32_t *rope = reinterpret_cast<const uint32_t *>(row + 448);
+    const uint32_t v = __ldg(rope + lane);
+    dst[448 + 2 * lane] = __uint_as_float(v << 16);
+    dst[448 + 2 * lane + 1] = __uint_as_float(v & 0xffff0000u);
+  }
+}
+
+template <int DV>
+__global__ void __launch_bounds__(kThreads)
+sparse_mla_simt_kernel(MlaArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float *k_s = reinterpret_cast<float *>(smem_raw);                       // [kRows][kKStride]
+  float *p_s = k_s + kRows * kKStride;                                      // [64][kRows]
+  __nv_bfloat16 *q_s = reinterpret_cast<__nv_bfloat16 *>(p_s + kHeadsPerCta * kRows);  // [64][kQStride]
+  __shared__ int s_valid[kRows];
+
+  const int t = blockIdx.x;
+  const int split = blockIdx.y;
+  const int h0 = blockIdx.z * kHeadsPerCta;
+  const int nh = min(kHeadsPerCta, a.H - h0);
+  const int D = a.D;
+  const int total = a.k + a.k2;
+  const int per = (total + a.n_splits - 1) / a.n_splits;
+  const int jb = split * per;
+  const int je = min(total, jb + per);
+
+  // q for this head group
+  {
+    const uint16_t *qg = static_cast<const uint16_t *>(a.q) + ((size_t)t * a.H + h0) * D;
+    uint16_t *qs = reinterpret_cast<uint16_t *>(q_s);
+    for (int i = threadIdx.x; i < kHeadsPerCta * D; i += blockDim.x) {
+      const int h = i / D, c = i % D;
+      qs[h * kQStride + c] = h < nh ? qg[(size_t)h * D + c] : (uint16_t)0;
+    }
+  }
+  const int hl = threadIdx.x >> 2;     // head within the group
+  const int part = threadIdx.x & 3;    // which quarter of the row work
+  constexpr int NACC = DV / 16 * 4;    // dv values owned: dv = 16*i + 4*part + e
+  float o[NACC];
+#pragma unroll
+  for (int i = 0; i < NACC; ++i) o[i] = 0.f;
+  float m = -INFINITY, l = 0.f;
+  const float sc = a.softmax_scale * kLog2e;
+  __syncthreads();
+
+  for (int j0 = jb; j0 < je; j0 += kRows) {
+    // gather: warp w loads row j0 + w
+    const int w = threadIdx.x >> 5;
+    if (w < kRows) {
+      const int j = j0 + w;
+      int ok = 0;
+      if (j < je) {
+        ListRef e = list_entry(a, t, j);
+        if (e.slot >= 0 && e.slot < e.pool->rows) {
+          ok = 1;
+          load_row(*e.pool, e.slot, D, k_s + w * kKStride);
+        } else if (e.slot != -1 && lane_id() == 0) {
+          raise_flag(a.err_flag, DSA_DEVERR_INDEX_RANGE);
+        }
+      }
+      if (lane_id() == 0) s_valid[w] = ok;
+    }
+    __syncthreads();
+    // scores: thread (hl, part) takes rows 2*part, 2*part+1
+    float s2[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = 2 * part + rr;
+      float x = 0.f;
+      if (s_valid[r]) {
+        const float *kr = k_s + r * kKStride;
+        const __nv_bfloat162 *qh = reinterpret_cast<const __nv_bfloat162 *>(q_s + hl * kQStride);
+        for (int c = 0; c < D; c += 4) {
+          const float4 kv = *reinterpret_cast<const float4 *>(kr + c);
+          const float2 qa = __bfloat1622float2(qh[c / 2]);
+          const float2 qb = __bfloat1622float2(qh[c / 2 + 1]);
+          x = fmaf(qa.x, kv.x, x);
+          x = fmaf(qa.y, kv.y, x);
+          x = fmaf(qb.x, kv.z, x);
+          x = fmaf(qb.y, kv.w, x);
+        }
+        x *= sc;
+      } else {
+        x = -INFINITY;
+      }
+      s2[rr] = x;
+    }
+    // online softmax over the 8 rows for this head (4 lanes share a head)
+    float cmax = fmaxf(s2[0], s2[1]);
+    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
+    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 2));
+    const float mn = fmaxf(m, cmax);
+    float alpha, p0, p1;
+    if (mn == -INFINITY) {
+      alpha = 1.f; p0 = 0.f; p1 = 0.f;
+    } else {
+      alpha = exp2f(m - mn);
+      p0 = exp2f(s2[0] - mn);
+      p1 = exp2f(s2[1] - mn);
+    }
+    float ps = p0 + p1;
+    ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+    l = l * alpha + ps;
+    m = mn;
+    p_s[hl * kRows + 2 * part] = p0;
+    p_s[hl * kRows + 2 * part + 1] = p1;
+    __syncthreads();
+    float pr[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) pr[r] = p_s[hl * kRows + r];
+#pragma unroll
+    for (int i = 0; i < DV / 16; ++i) {
+      const int dv = 16 * i + 4 * part;
+      float4 acc = make_float4(o[4 * i] * alpha, o[4 * i + 1] * alpha, o[4 * i + 2] * alpha,
+                               o[4 * i + 3] * alpha);
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        if (pr[r] != 0.f) {
+          const float4 v = *reinterpret_cast<const float4 *>(k_s + r * kKStride + dv);
+          acc.x = fmaf(pr[r], v.x, acc.x);
+          acc.y = fmaf(pr[r], v.y, acc.y);
+          acc.z = fmaf(pr[r], v.z, acc.z);
+          acc.w = fmaf(pr[r], v.w, acc.w);
+        }
+      }
+      o[4 * i] = acc.x; o[4 * i + 1] = acc.y; o[4 * i + 2] = acc.z; o[4 * i + 3] = acc.w;
+    }
+    __syncthreads();
+  }
+
+  if (hl >= nh) return;
+  const int h = h0 + hl;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+  if (a.n_splits == 1) {
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + ((size_t)t * a.H + h) * a.Dv;
+#pragma unroll
+    for (int i = 0; i < DV / 16; ++i) {
+      const int dv = 16 * i + 4 * part;
+      uint2 pk;
+      pk.x = pack_bf16x2(o[4 * i] * inv, o[4 * i + 1] * inv);
+      pk.y = pack_bf16x2(o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+      *reinterpret_cast<uint2 *>(out + dv) = pk;
+    }
+    if (part == 0) a.lse[(size_t)t * a.H + h] = lse_v;
+  } else {
+    const size_t rec = ((size_t)t * a.n_splits + split) * a.H + h;
+    float *po = a.part_o + rec * a.Dv;
+#pragma unroll
+    for (int i = 0; i < DV / 16; ++i) {
+      const int dv = 16 * i + 4 * part;
+      *reinterpret_cast<float4 *>(po + dv) =
+          make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+    }
+    if (part == 0) a.part_lse[rec] = lse_v;
+  }
+}
+
+// Merge split partials: one CTA per (token, head), 128 threads x 4 values.
+__global__ void __launch_bounds__(128)
+mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
+                   int H, int Dv, int n_splits, __nv_bfloat16 *__restrict__ out,
+                   float *__restrict__ lse) {
+  const int t = blockIdx.x, h = blockIdx.y;
+  float mx = -INFINITY;
+  for (int i = 0; i < n_splits; ++i)
+    mx = fmaxf(mx, part_lse[((size_t)t * n_splits + i) * H + h]);
+  float tot = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int dv = 4 * threadIdx.x;
+  for (int i = 0; i < n_splits; ++i) {
+    const size_t rec = ((size_t)t * n_splits + i) * H + h;
+    const float li = part_lse[rec];
+    if (li == -INFINITY) continue;
+    const float wgt = __expf(li - mx);
+    tot += wgt;
+    if (dv < Dv) {
+      const float4 v = *reinterpret_cast<const float4 *>(part_o + rec * Dv + dv);
+      acc.x = fmaf(wgt, v.x, acc.x);
+      acc.y = fmaf(wgt, v.y, acc.y);
+      acc.z = fmaf(wgt, v.z, acc.z);
+      acc.w = fmaf(wgt, v.w, acc.w);
+    }
+  }
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  if (dv < Dv) {
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2 *>(out + ((size_t)t * H + h) * Dv + dv) = pk;
+  }
+  if (threadIdx.x == 0) lse[(size_t)t * H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+}
+
+}  // namespace
+
+int mla_num_splits(int T, int H, int k_total) {
+  const int hgroups = (H + kHeadsPerCta - 1) / kHeadsPerCta;
+  const int ctas_per_split = T * hgroups;
+  const int target = 2 * num_sms();
+  int s = (target + ctas_per_split - 1) / ctas_per_split;
+  s = min(s, (k_total + 63) / 64);  // at least 64 rows a piece
+  return max(s, 1);
+}
+
+size_t mla_ws_bytes(int T, int H, int Dv, int k_total) {
+  const int s = mla_num_splits(T, H, k_total);
+  if (s <= 1) return 0;
+  WsCarver c(nullptr);
+  c.take<float>((size_t)T * s * H * Dv);
+  c.take<float>((size_t)T * s * H);
+  return c.bytes();
+}
+
+void mla_ws_layout(int T, int H, int Dv, int k_total, void *ws, float **part_o,
+                   float **part_lse) {
+  const int s = mla_num_splits(T, H, k_total);
+  WsCarver c(ws);
+  *part_o = c.take<float>((size_t)T * s * H * Dv);
+  *part_lse = c.take<float>((size_t)T * s * H);
+}
+
+cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s) {
+  if (a.T == 0) return cudaSuccess;
+  const size_t smem = sizeof(float) * (kRows * kKStride + kHeadsPerCta * kRows) +
+                      sizeof(__nv_bfloat16) * kHeadsPerCta * kQStride;
+  dim3 grid((unsigned)a.T, (unsigned)a.n_splits, (unsigned)((a.H + kHeadsPerCta - 1) / kHeadsPerCta));
+  cudaError_t e;
+  if (a.Dv == 512) {
+    e = cudaFuncSetAttribute(sparse_mla_simt_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    sparse_mla_simt_kernel<512><<<grid, kThreads, smem, s>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(sparse_mla_simt_kernel<448>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    sparse_mla_simt_kernel<448><<<grid, kThreads, smem, s>>>(a);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.n_splits == 1) return e;
+  mla_combine_kernel<<<dim3((unsigned)a.T, (unsigned)a.H), 128, 0, s>>>(
+      a.part_o, a.part_lse, a.H, a.Dv, a.n_splits, static_cast<__nv_bfloat16 *>(a.out), a.lse);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -1,0 +1,240 @@
+"""Thin ctypes binding of libdsa_gb300.so (C ABI: include/dsa.h).
+
+Argument marshalling only: tensors become device pointers, shapes become the
+size arguments, and the call is enqueued on torch's current CUDA stream.
+Every step of the computation runs in the library's CUDA kernels.  There is
+no fallback: if the library is missing or a GPU is absent, the first call
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+from . import inputs as _inp
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa_gb300.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "dsa.h")
+
+DSA_OK = 0
+DEVERR_INDEX_RANGE = 1
+DEVERR_TIMEOUT = 2
+MAX_TOPK = 2048
+
+c_p = ctypes.c_void_p
+c_i32 = ctypes.c_int32
+c_i64 = ctypes.c_int64
+c_f32 = ctypes.c_float
+c_sz = ctypes.c_size_t
+
+
+class DsaKvPool(ctypes.Structure):
+    _fields_ = [("data", c_p), ("scales", c_p), ("rows", c_i64), ("format", c_i32),
+                ("block", c_i32), ("d_nope", c_i32), ("d_rope", c_i32)]
+
+
+_SIGS = {
+    "dsa_status_string": (ctypes.c_char_p, [c_i32]),
+    "dsa_abi_version": (c_i32, []),
+    "dsa_index_score": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_p, c_p, c_i32, c_i32,
+                                c_i32, c_i64, c_p, c_i64, c_p, c_p]),
+    "dsa_topk_workspace_size": (c_sz, [c_i32, c_i64, c_i32]),
+    "dsa_topk": (c_i32, [c_p, c_i64, c_p, c_i32, c_i64, c_i32, c_p, c_p, c_p, c_p, c_sz, c_p,
+                         c_p]),
+    "dsa_sparse_mla_workspace_size": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "dsa_sparse_mla_fwd": (c_i32, [c_p, c_i32, c_i32, c_i32, c_i32, c_f32,
+                                   ctypes.POINTER(DsaKvPool), c_p, c_i32,
+                                   ctypes.POINTER(DsaKvPool), c_p, c_i32,
+                                   c_p, c_p, c_p, c_sz, c_p, c_p]),
+    "dsa_decode_workspace_size": (c_sz, [c_i32, c_i64, c_i32, c_i32, c_i32, c_i32]),
+    "dsa_decode": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_i32, c_i32,
+                           c_i32, c_p, c_p, c_i64, c_i32,
+                           c_p, c_i32, c_i32, c_i32, c_f32, ctypes.POINTER(DsaKvPool),
+                           ctypes.POINTER(DsaKvPool), c_p, c_i32,
+                           c_p, c_p, c_p, c_p, c_sz, c_p, c_p]),
+}
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libdsa_gb300.so is missing (%s); build it with "
+                               "`python -m deepseek_sparse_attention_index_gb300.build`" % LIB_PATH)
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def header_functions() -> list:
+    """Names of the functions include/dsa.h declares."""
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(dsa_\w+)\s*\(", txt, flags=re.M)))
+
+
+class DsaError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str):
+    if status != DSA_OK:
+        msg = load().dsa_status_string(status).decode()
+        raise DsaError("%s failed: status %d (%s)" % (what, status, msg))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def kv_pool_struct(pool: Optional[_inp.KVPool]):
+    if pool is None:
+        return None
+    s = DsaKvPool()
+    s.data = _ptr(pool.data).value
+    s.scales = None if pool.scales is None else _ptr(pool.scales).value
+    s.rows = int(pool.rows)
+    s.format = int(pool.format)
+    s.block = int(pool.block)
+    s.d_nope = int(pool.d_nope)
+    s.d_rope = int(pool.d_rope)
+    return s
+
+
+def _ref(s):
+    return None if s is None else ctypes.byref(s)
+
+
+# ---------------------------------------------------------------- entry points
+
+def dsa_index_score(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, row_start, row_end,
+                    max_len: int, scores=None, err_flag=None):
+    """Scores [T, ld] fp32 (see dsa_index_score in include/dsa.h)."""
+    T, H_I, d = q_idx.shape
+    if scores is None:
+        ld = (int(max_len) + 3) // 4 * 4
+        scores = torch.full((T, max(ld, 1)), float("nan"), dtype=torch.float32, device=q_idx.device)
+    st = load().dsa_index_score(_ptr(q_idx), idx_dtype, _ptr(q_scale), _ptr(k_idx), _ptr(k_scale),
+                                k_idx.shape[0], _ptr(w), _ptr(row_start), _ptr(row_end), T, H_I, d,
+                                int(max_len), _ptr(scores), scores.shape[1], _ptr(err_flag),
+                                _stream())
+    _check(st, "dsa_index_score")
+    return scores
+
+
+def dsa_topk_workspace_size(T: int, max_len: int, k: int) -> int:
+    return int(load().dsa_topk_workspace_size(T, int(max_len), k))
+
+
+def dsa_topk(scores, row_len, k: int, max_len: int, index_base=None, idx=None, lens=None,
+             ws=None, err_flag=None):
+    """idx [T, k] int32 (and lens [T]) from scores [T, ld] (see dsa_topk)."""
+    T, ld = scores.shape
+    dev = scores.device
+    if idx is None:
+        idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if lens is None:
+        lens = torch.empty((T,), dtype=torch.int32, device=dev)
+    need = dsa_topk_workspace_size(T, max_len, k)
+    if ws is None:
+        ws = workspace(need, dev)
+    st = load().dsa_topk(_ptr(scores), ld, _ptr(row_len), T, int(max_len), k, _ptr(index_base),
+                         _ptr(idx), _ptr(lens), _ptr(ws), ws.numel(), _ptr(err_flag), _stream())
+    _check(st, "dsa_topk")
+    return idx, lens
+
+
+def dsa_sparse_mla_workspace_size(T, H, Dv, k, k2=0) -> int:
+    return int(load().dsa_sparse_mla_workspace_size(T, H, Dv, k, k2))
+
+
+def dsa_sparse_mla_fwd(q, softmax_scale: float, kv: _inp.KVPool, idx, kv_extra=None,
+                       idx_extra=None, out=None, lse=None, ws=None, err_flag=None):
+    """out bf16 [T, H, Dv], lse fp32 [T, H] (see dsa_sparse_mla_fwd)."""
+    T, H, D = q.shape
+    Dv = kv.d_nope if kv.format != _inp.KV_BF16 else 512
+    k = idx.shape[1]
+    k2 = 0 if idx_extra is None else idx_extra.shape[1]
+    dev = q.device
+    if out is None:
+        out = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    need = dsa_sparse_mla_workspace_size(T, H, Dv, k, k2)
+    if ws is None:
+        ws = workspace(need, dev)
+    s1, s2 = kv_pool_struct(kv), kv_pool_struct(kv_extra)
+    st = load().dsa_sparse_mla_fwd(_ptr(q), T, H, D, Dv, float(softmax_scale), _ref(s1), _ptr(idx),
+                                   k, _ref(s2), _ptr(idx_extra), k2, _ptr(out), _ptr(lse), _ptr(ws),
+                                   ws.numel(), _ptr(err_flag), _stream())
+    _check(st, "dsa_sparse_mla_fwd")
+    return out, lse
+
+
+def dsa_decode_workspace_size(B, max_seq_len, k, H, Dv, k_swa=0) -> int:
+    return int(load().dsa_decode_workspace_size(B, int(max_seq_len), k, H, Dv, k_swa))
+
+
+def dsa_decode(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, slot_base,
+               max_seq_len: int, k: int, q, softmax_scale: float, kv: _inp.KVPool,
+               kv_swa=None, idx_swa=None, idx_out=None, out=None, lse=None, ws=None,
+               err_flag=None):
+    """One fused decode step (see dsa_decode).  Returns (idx_out, out, lse)."""
+    B, H_I, d_idx = q_idx.shape
+    _, H, D = q.shape
+    Dv = kv.d_nope if kv.format != _inp.KV_BF16 else 512
+    k_swa = 0 if idx_swa is None else idx_swa.shape[1]
+    dev = q.device
+    if idx_out is None:
+        idx_out = torch.empty((B, k), dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty((B, H, Dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    need = dsa_decode_workspace_size(B, max_seq_len, k, H, Dv, k_swa)
+    if ws is None:
+        ws = workspace(need, dev)
+    s1, s2 = kv_pool_struct(kv), kv_pool_struct(kv_swa)
+    st = load().dsa_decode(_ptr(q_idx), idx_dtype, _ptr(q_scale), _ptr(k_idx), _ptr(k_scale),
+                           k_idx.shape[0], _ptr(w), H_I, d_idx, B, _ptr(seq_lens), _ptr(slot_base),
+                           int(max_seq_len), k, _ptr(q), H, D, Dv, float(softmax_scale), _ref(s1),
+                           _ref(s2), _ptr(idx_swa), k_swa, _ptr(idx_out), _ptr(out), _ptr(lse),
+                           _ptr(ws), ws.numel(), _ptr(err_flag), _stream())
+    _check(st, "dsa_decode")
+    return idx_out, out, lse
+
+
+def decode_case(case: _inp.DecodeCase, ws=None, err_flag=None, idx_out=None, out=None, lse=None):
+    """dsa_decode on a generated DecodeCase."""
+    ind = case.indexer
+    return dsa_decode(ind["q_idx"], ind["idx_dtype"], ind["q_scale"], ind["k_idx"], ind["k_scale"],
+                      ind["w"], case.seq_lens, case.slot_base, case.max_seq_len, case.k, case.q,
+                      case.softmax_scale, case.kv, case.kv_swa, case.idx_swa, idx_out=idx_out,
+                      out=out, lse=lse, ws=ws, err_flag=err_flag)

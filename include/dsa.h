@@ -1,0 +1,215 @@
+/*
+ * dsa.h -- C ABI of the DeepSeek Sparse Attention (DSA) forward hot path
+ * on NVIDIA GB300 (sm_103a).  Library: libdsa_gb300.so.
+ *
+ * One decode or prefill step has three stages per query token t:
+ *   1. index score  I[t,s] = sum_h w[t,h] * ReLU(q_idx[t,h,:] . k_idx[s,:])
+ *      over the keys s that t may see;
+ *   2. top-k        the k highest-scoring positions, -1 padded;
+ *   3. sparse MLA   softmax attention of q[t] over the selected latent KV
+ *      rows (K = the whole row, V = its leading Dv dims), out + lse.
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller, contiguous
+ *    row-major, unless a comment says "host".  The library never allocates or
+ *    frees device memory: scratch comes from a caller workspace whose size
+ *    the matching *_workspace_size() function returns.
+ *  - Work is enqueued on the caller's stream (cudaStream_t passed as
+ *    dsa_stream_t; NULL = the legacy default stream).  No entry point
+ *    synchronises the host, so results are ready when the stream says so.
+ *  - The return value reports errors found on the HOST, before anything is
+ *    launched (DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED,
+ *    DSA_ERR_WORKSPACE_TOO_SMALL), or a failed launch (DSA_ERR_CUDA).  When
+ *    the return is not DSA_OK nothing of that call ran, except for
+ *    DSA_ERR_CUDA, where earlier launches of the same call may have run.
+ *  - err_flag (optional, device int32, may be NULL) collects errors found on
+ *    the DEVICE by OR-ing DSA_DEVERR_* bits into it.  The offending entries
+ *    are masked (treated like -1), never read.  The library never clears it.
+ *  - Index lists use -1 for "no entry".  A -1 is masked, never clamped into a
+ *    read (miles PR #3608 "per-arch DSA sparse attention dispatch", What /
+ *    Padding).
+ *  - The entry points hold no state between calls and may be captured in a
+ *    CUDA graph.
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dsa_stream_t; /* a cudaStream_t */
+
+/* Host-side status codes. */
+enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,         /* null pointer, bad size or range   */
+  DSA_ERR_UNSUPPORTED = 2,         /* shape / format this build lacks   */
+  DSA_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes below *_workspace_size() */
+  DSA_ERR_CUDA = 4                 /* a launch or driver call failed    */
+};
+
+/* Device-side error bits OR-ed into *err_flag. */
+enum {
+  DSA_DEVERR_INDEX_RANGE = 1, /* an index list entry < -1 or >= the pool's rows,
+                                 or a key range outside the index-k cache     */
+  DSA_DEVERR_TIMEOUT = 2      /* an internal bounded wait gave up             */
+};
+
+/* Indexer operand types. */
+enum { DSA_IDX_BF16 = 0, DSA_IDX_FP8_E4M3 = 1 };
+
+/* KV pool formats (aiter PR #4382 "Paged Sparse Attention Gluon Kernel",
+ * section "Supported formats & dtypes"). */
+enum {
+  DSA_KV_BF16 = 0,        /* data: bf16 [rows, d_nope + d_rope] (576 wide)  */
+  DSA_KV_FP8_UNIFORM = 1, /* section "Uniform fp8 pool - 2D": data uint8
+                             [rows, D] OCP e4m3, scales fp32 [rows, D/64];
+                             x = fp8(byte) * scales[slot, col / 64] for every
+                             column, RoPE included                         */
+  DSA_KV_FP8_DS_MLA = 2   /* section "Packed fp8 fp8_ds_mla - 3D": data uint8
+                             [nb, block, 584]; page = block x 576 data bytes
+                             then block x 8 scale bytes; data row = 448 e4m3
+                             NoPE bytes + 64 bf16 RoPE; scale row = 7 UE8M0
+                             exponents + 1 pad; NoPE x = fp8 * 2^(e - 127)   */
+};
+
+/* Limits of this build. */
+#define DSA_MAX_TOPK 2048     /* k of dsa_topk / dsa_decode                 */
+#define DSA_MAX_INDEX_HEADS 64
+#define DSA_MAX_HEADS 128     /* H of dsa_sparse_mla_fwd                    */
+
+/* A latent KV pool.  Slots index rows (bf16, uniform) or tokens
+ * (fp8_ds_mla: slot -> page slot / block, row slot % block). */
+typedef struct dsa_kv_pool {
+  const void *data;     /* device; layout per format above; 16-byte aligned   */
+  const float *scales;  /* device; DSA_KV_FP8_UNIFORM only, else NULL          */
+  int64_t rows;         /* addressable slots (nb * block for fp8_ds_mla)       */
+  int32_t format;       /* DSA_KV_*                                            */
+  int32_t block;        /* tokens per page for fp8_ds_mla; 1 otherwise         */
+  int32_t d_nope;       /* 512 (bf16) or 448 (fp8 formats)                     */
+  int32_t d_rope;       /* 64                                                  */
+} dsa_kv_pool;
+
+/* Text for a status code (static storage). */
+const char *dsa_status_string(int status);
+
+/* ABI version of this library: 1. */
+int dsa_abi_version(void);
+
+/*
+ * dsa_index_score -- lightning-indexer scores.
+ * The "scores" stage of tokenspeed PR #627 "Add gluon kernel for DSA"
+ * (Benchmark results, Decode and Prefill tables); the formula is the DSA
+ * indexer's definition:
+ *   scores[t*ld_scores + j] = sum_h w[t,h] * ReLU(sq[t,h] * sk[s] *
+ *                              (q_idx[t,h,:] . k_idx[s,:])),   s = row_start[t] + j
+ * for 0 <= j < row_end[t] - row_start[t].  Entries of a row past its own
+ * length are left untouched.  sq, sk are the fp8 per-row scales (all 1 for
+ * bf16).
+ *   q_idx     [T, H_I, d]  bf16 or e4m3 bytes (idx_dtype)
+ *   q_scale   [T, H_I]     fp32, fp8 only (NULL for bf16)
+ *   k_idx     [k_rows, d]  same type as q_idx (the index-k cache)
+ *   k_scale   [k_rows]     fp32, fp8 only (NULL for bf16)
+ *   w         [T, H_I]     fp32 head weights (any sign)
+ *   row_start, row_end [T] int32 key rows [row_start, row_end) of k_idx;
+ *             decode: [slot_base, slot_base + seq_len); causal prefill:
+ *             [segment start, t + 1)
+ *   max_len   host: an upper bound of row_end - row_start over all t
+ *   scores    fp32 [T, ld_scores], ld_scores >= max_len
+ * Limits: H_I <= 64 and a multiple of 8; d in {64, 128} (bf16) or 128 (fp8).
+ * A row range outside [0, k_rows] sets DSA_DEVERR_INDEX_RANGE and that row
+ * is skipped.
+ */
+int dsa_index_score(const void *q_idx, int idx_dtype, const float *q_scale,
+                    const void *k_idx, const float *k_scale, int64_t k_rows,
+                    const float *w, const int32_t *row_start, const int32_t *row_end,
+                    int T, int H_I, int d, int64_t max_len,
+                    float *scores, int64_t ld_scores,
+                    int32_t *err_flag, dsa_stream_t stream);
+
+/*
+ * dsa_topk -- per-row top-k with -1 padding.
+ * The "TopK" stage of tokenspeed PR #627 (Benchmark results; the selector
+ * counts "greater" and "equal" elements against a threshold) with the -1
+ * padding of miles PR #3608 (What / Padding).
+ * Row t holds row_len[t] valid scores scores[t*ld_scores + 0 .. len-1].
+ * Output row t: the min(len, k) positions with the highest scores, then -1
+ * up to k.  Ties: the lower position wins, so the selected SET is unique.
+ * Order inside a row: deterministic, positions ascending within each of two
+ * runs (those strictly above the threshold bucket, then the rest).
+ * -0.0 ties +0.0.  Scores must not be NaN (unchecked).
+ *   index_base [T] int32 or NULL: added to every selected position
+ *              (turns request-local positions into pool slots); -1 stays -1
+ *   idx        int32 [T, k];  lens int32 [T] or NULL: min(row_len, k)
+ *   max_len    host: an upper bound of row_len
+ * Workspace: dsa_topk_workspace_size(T, max_len, k) bytes, 256-byte aligned.
+ */
+size_t dsa_topk_workspace_size(int T, int64_t max_len, int k);
+int dsa_topk(const float *scores, int64_t ld_scores, const int32_t *row_len, int T,
+             int64_t max_len, int k, const int32_t *index_base,
+             int32_t *idx, int32_t *lens, void *ws, size_t ws_bytes,
+             int32_t *err_flag, dsa_stream_t stream);
+
+/*
+ * dsa_sparse_mla_fwd -- absorbed-MLA attention over selected latent rows.
+ * The "sparse attn" stage of tokenspeed PR #627; semantics of miles PR #3608
+ * (FlashMLA-style forward: natural-log lse; -1 masked) and the pool formats
+ * and two-loop (main + extra list) layout of aiter PR #4382.
+ * For each token t and head h:
+ *   s_j = softmax_scale * q[t,h,0:D] . K_j   over valid entries j of idx[t,:]
+ *         (slots into kv) and of idx_extra[t,:] (slots into kv_extra)
+ *   out[t,h,0:Dv] = sum_j softmax(s)_j * K_j[0:Dv],  lse[t,h] = ln sum_j exp(s_j)
+ * K_j is the dequantised row, D = d_nope + d_rope of the pool.  A token with
+ * no valid entry gets out = 0 and lse = -inf.
+ *   q        bf16 [T, H, D]
+ *   idx      int32 [T, k] (-1 masked); kv_extra / idx_extra [T, k2] optional
+ *            (both NULL with k2 = 0); kv_extra must have kv's D
+ *   out      bf16 [T, H, Dv];  lse fp32 [T, H]
+ * Limits: D = 576 with Dv = 512 (bf16 pool) or D = 512 with Dv = 448 (fp8
+ * pools); 1 <= H <= 128; k + k2 >= 1.
+ * Workspace: dsa_sparse_mla_workspace_size(T, H, Dv, k, k2) bytes.
+ */
+size_t dsa_sparse_mla_workspace_size(int T, int H, int Dv, int k, int k2);
+int dsa_sparse_mla_fwd(const void *q, int T, int H, int D, int Dv, float softmax_scale,
+                       const dsa_kv_pool *kv, const int32_t *idx, int k,
+                       const dsa_kv_pool *kv_extra, const int32_t *idx_extra, int k2,
+                       void *out, float *lse, void *ws, size_t ws_bytes,
+                       int32_t *err_flag, dsa_stream_t stream);
+
+/*
+ * dsa_decode -- one fused decode step: score -> top-k -> sparse MLA for B
+ * requests with one query token each (tokenspeed PR #627, Decode table:
+ * "scores + TopK + sparse attn = total").
+ * Request b sees context positions 0 .. seq_lens[b]-1; position j lives at
+ * slot slot_base[b] + j of BOTH the index-k cache and the KV pool kv.
+ *   indexer:  q_idx [B, H_I, d_idx], q_scale [B, H_I] (fp8) , k_idx / k_scale
+ *             [k_rows, ...], w [B, H_I]   (as dsa_index_score)
+ *   top-k:    k <= DSA_MAX_TOPK; max_seq_len (host) >= every seq_lens[b]
+ *   attention: q bf16 [B, H, D], kv the pool the top-k indexes; optional
+ *             second list kv_swa / idx_swa [B, k_swa] (e.g. a sliding
+ *             window held in its own cache) in the same softmax
+ *   idx_out   int32 [B, k] or NULL: the selected pool slots, -1 padded
+ *   out bf16 [B, H, Dv], lse fp32 [B, H]
+ * Workspace: dsa_decode_workspace_size(...) bytes.
+ */
+size_t dsa_decode_workspace_size(int B, int64_t max_seq_len, int k, int H, int Dv, int k_swa);
+int dsa_decode(const void *q_idx, int idx_dtype, const float *q_scale,
+               const void *k_idx, const float *k_scale, int64_t k_rows,
+               const float *w, int H_I, int d_idx,
+               int B, const int32_t *seq_lens, const int32_t *slot_base,
+               int64_t max_seq_len, int k,
+               const void *q, int H, int D, int Dv, float softmax_scale,
+               const dsa_kv_pool *kv,
+               const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa,
+               int32_t *idx_out, void *out, float *lse,
+               void *ws, size_t ws_bytes, int32_t *err_flag, dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_H */

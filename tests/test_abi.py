@@ -1,0 +1,109 @@
+"""The C-ABI library builds, loads and exports every function include/dsa.h
+declares; host-side argument checks reject bad calls before any launch.
+No GPU is needed: nothing here reaches a kernel."""
+import ctypes
+
+import pytest
+
+from deepseek_sparse_attention_index_gb300 import build as B
+from deepseek_sparse_attention_index_gb300 import ops
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return ops.load()
+
+
+def test_header_declares_the_boundary():
+    names = ops.header_functions()
+    for n in ["dsa_index_score", "dsa_topk", "dsa_sparse_mla_fwd", "dsa_decode",
+              "dsa_topk_workspace_size", "dsa_sparse_mla_workspace_size",
+              "dsa_decode_workspace_size", "dsa_status_string", "dsa_abi_version"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in ops.header_functions():
+        assert hasattr(lib, n), n
+        assert n in ops._SIGS, "binding lacks a signature for " + n
+
+
+def test_version_and_status_strings(lib):
+    assert lib.dsa_abi_version() == 1
+    for code in range(5):
+        assert lib.dsa_status_string(code)
+    assert lib.dsa_status_string(99) == b"unknown status"
+
+
+FAKE = ctypes.c_void_p(0x10000)  # 16-byte aligned, never dereferenced
+
+
+def test_topk_rejects_bad_arguments(lib):
+    # k out of range
+    assert lib.dsa_topk(FAKE, 8, FAKE, 1, 8, 0, None, FAKE, None, FAKE, 1 << 20, None,
+                        None) == 2
+    assert lib.dsa_topk(FAKE, 8, FAKE, 1, 8, ops.MAX_TOPK + 1, None, FAKE, None, FAKE, 1 << 20,
+                        None, None) == 2
+    # ld smaller than max_len
+    assert lib.dsa_topk(FAKE, 4, FAKE, 1, 8, 2, None, FAKE, None, FAKE, 1 << 20, None, None) == 1
+    # workspace too small
+    need = lib.dsa_topk_workspace_size(3, 100, 16)
+    assert need > 0
+    assert lib.dsa_topk(FAKE, 100, FAKE, 3, 100, 16, None, FAKE, None, FAKE, need - 1, None,
+                        None) == 3
+    # T = 0 is a no-op
+    assert lib.dsa_topk(None, 0, None, 0, 0, 4, None, None, None, None, 0, None, None) == 0
+
+
+def _pool(fmt, rows=16, block=1, d_nope=512, scales=True):
+    p = ops.DsaKvPool()
+    p.data = FAKE.value
+    p.scales = FAKE.value if scales else None
+    p.rows = rows
+    p.format = fmt
+    p.block = block
+    p.d_nope = d_nope
+    p.d_rope = 64
+    return p
+
+
+def _mla(lib, pool, D=576, Dv=512, H=8, k=4, idx=FAKE, ws_bytes=1 << 30):
+    return lib.dsa_sparse_mla_fwd(FAKE, 2, H, D, Dv, 0.1, ctypes.byref(pool), idx, k, None, None,
+                                  0, FAKE, FAKE, FAKE, ws_bytes, None, None)
+
+
+def test_sparse_mla_rejects_bad_arguments(lib):
+    assert _mla(lib, _pool(0, d_nope=512), D=512, Dv=448) == 2        # bf16 pool must be 576
+    assert _mla(lib, _pool(0, d_nope=512), D=576, Dv=448) == 2        # (D, Dv) pair
+    assert _mla(lib, _pool(0, d_nope=512), H=0) == 2
+    assert _mla(lib, _pool(0, d_nope=512), H=ops.MAX_TOPK) == 2
+    assert _mla(lib, _pool(1, d_nope=448, scales=False), D=512, Dv=448) == 1  # no scales
+    assert _mla(lib, _pool(2, rows=512, block=255, d_nope=448), D=512, Dv=448) == 2  # odd block
+    assert _mla(lib, _pool(2, rows=500, block=256, d_nope=448), D=512, Dv=448) == 1  # rows % block
+    assert _mla(lib, _pool(0, d_nope=512), idx=None) == 1
+    p = _pool(0, d_nope=512)
+    p.data = 0x10004                                                      # misaligned pool
+    assert _mla(lib, p) == 1
+    need = lib.dsa_sparse_mla_workspace_size(2, 8, 512, 4, 0)
+    if need:
+        assert _mla(lib, _pool(0, d_nope=512), ws_bytes=need - 1) == 3
+
+
+def test_index_score_rejects_bad_arguments(lib):
+    def call(idx_dtype=1, H_I=64, d=128, q_scale=FAKE, ld=128, max_len=100):
+        return lib.dsa_index_score(FAKE, idx_dtype, q_scale, FAKE, FAKE, 1000, FAKE, FAKE, FAKE,
+                                   2, H_I, d, max_len, FAKE, ld, None, None)
+    assert call(H_I=65) == 2
+    assert call(H_I=12) == 2
+    assert call(d=64) == 2           # fp8 needs d = 128
+    assert call(idx_dtype=7) == 2
+    assert call(q_scale=None) == 1   # fp8 needs scales
+    assert call(ld=50) == 1          # ld < max_len
+
+
+def test_workspace_sizes_grow_with_the_problem(lib):
+    a = lib.dsa_decode_workspace_size(1, 1 << 14, 2048, 64, 512, 0)
+    b = lib.dsa_decode_workspace_size(32, 1 << 17, 2048, 64, 512, 0)
+    assert 0 < a < b
+    assert b >= 32 * (1 << 17) * 4   # the score rows live in the workspace

@@ -1,0 +1,347 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Small cases are compared element by element; the full-size workloads are
+compared on sampled requests the oracle computes one by one."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.dsa_oracle as O
+from deepseek_sparse_attention_index_gb300 import build as B
+from deepseek_sparse_attention_index_gb300 import inputs as I
+from deepseek_sparse_attention_index_gb300 import ops
+from tests.helpers import raw, pool_np, decode_case_np, prefill_case_np
+from tests.parity import check_index_sets, check_out_lse
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    B.build()
+    ops.load()
+
+
+def _flag():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+# ---------------------------------------------------------------- index score
+
+def _oracle_scores(ind_np, t, r0, r1):
+    fp8 = ind_np["is_fp8"]
+    q = O.index_values(ind_np["q_idx"][t], None if not fp8 else ind_np["q_scale"][t], fp8)
+    k = O.index_values(ind_np["k_idx"][r0:r1], None if not fp8 else ind_np["k_scale"][r0:r1], fp8)
+    return O.index_scores_one(q, ind_np["w"][t].astype(np.float64), k)
+
+
+def _ind_np(ind):
+    return dict(q_idx=raw(ind["q_idx"]), q_scale=raw(ind["q_scale"]), k_idx=raw(ind["k_idx"]),
+                k_scale=raw(ind["k_scale"]), w=raw(ind["w"]), is_fp8=ind["idx_dtype"] == 1)
+
+
+@pytest.mark.parametrize("H_I,d", [(8, 64), (16, 128), (64, 128)])
+def test_index_score_integer_grid_bit_exact(H_I, d):
+    lens = [1, 127, 128, 129, 3000]
+    S = sum(lens)
+    ind = I.indexer_grid_bf16(len(lens), S, H_I, d, seed=1, device="cuda")
+    starts = np.cumsum([0] + lens[:-1])
+    rs = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    re = torch.tensor(starts + np.array(lens), dtype=torch.int32, device="cuda")
+    flag = _flag()
+    sc = ops.dsa_index_score(ind["q_idx"], 0, None, ind["k_idx"], None, ind["w"], rs, re, max(lens),
+                             err_flag=flag)
+    sc = sc.cpu().numpy()
+    inp = _ind_np(ind)
+    for t, L in enumerate(lens):
+        ref = _oracle_scores(inp, t, starts[t], starts[t] + L)
+        assert np.array_equal(sc[t, :L].astype(np.float64), ref), t
+        assert np.isnan(sc[t, L:]).all()    # past the row: untouched
+    assert flag.item() == 0
+
+
+def test_index_score_fp8_prefill_ranges():
+    case = I.prefill_case([1, 1, 100, 198, 700], k=64, H=8, device="cuda")
+    ind = case.indexer
+    sc = ops.dsa_index_score(ind["q_idx"], 1, ind["q_scale"], ind["k_idx"], ind["k_scale"],
+                             ind["w"], case.row_start, case.row_end, 700).cpu().numpy()
+    inp = _ind_np(ind)
+    rs, re = raw(case.row_start), raw(case.row_end)
+    for t in list(range(0, case.T, 7)) + [case.T - 1]:
+        ref = _oracle_scores(inp, t, rs[t], re[t])
+        got = sc[t, :re[t] - rs[t]].astype(np.float64)
+        tol = 1e-5 * np.abs(ref).max() + 1e-5 * np.abs(ref)
+        assert (np.abs(got - ref) <= tol).all(), t
+
+
+def test_index_score_flags_bad_ranges():
+    ind = I.indexer_grid_bf16(2, 100, 8, 64, seed=2, device="cuda")
+    rs = torch.tensor([0, 50], dtype=torch.int32, device="cuda")
+    re = torch.tensor([10, 101], dtype=torch.int32, device="cuda")   # row 1 runs past k_rows
+    flag = _flag()
+    sc = ops.dsa_index_score(ind["q_idx"], 0, None, ind["k_idx"], None, ind["w"], rs, re, 51,
+                             err_flag=flag).cpu().numpy()
+    assert flag.item() & ops.DEVERR_INDEX_RANGE
+    assert np.isnan(sc[1]).all() and not np.isnan(sc[0, :10]).any()
+
+
+# ---------------------------------------------------------------- top-k
+
+def _run_topk(rows, k, base=None):
+    T = len(rows)
+    maxL = max(max(len(r) for r in rows), 1)
+    ld = (maxL + 3) // 4 * 4
+    S = np.zeros((T, ld), dtype=np.float32)
+    for t, r in enumerate(rows):
+        S[t, :len(r)] = r
+        S[t, len(r):] = np.float32(1e30)     # beyond the row: must be ignored
+    sc = torch.from_numpy(S).cuda()
+    rl = torch.tensor([len(r) for r in rows], dtype=torch.int32, device="cuda")
+    bt = None if base is None else torch.tensor(base, dtype=torch.int32, device="cuda")
+    flag = _flag()
+    idx, lens = ops.dsa_topk(sc, rl, k, maxL, index_base=bt, err_flag=flag)
+    assert flag.item() == 0
+    return idx.cpu().numpy(), lens.cpu().numpy()
+
+
+@pytest.mark.parametrize("k", [1, 7, 128, 2048])
+def test_topk_bit_exact(k):
+    rng = np.random.default_rng(k)
+    rows = [np.zeros(0, np.float32),
+            rng.standard_normal(1).astype(np.float32),
+            (np.round(rng.standard_normal(k) * 8) / 4).astype(np.float32),
+            (np.round(rng.standard_normal(k + 1) * 8) / 4).astype(np.float32),
+            rng.standard_normal(3 * k + 5).astype(np.float32),
+            (np.round(rng.standard_normal(70001) * 40) / 8).astype(np.float32),
+            np.full(20000, 0.5, np.float32),                      # every score tied
+            np.where(rng.random(5000) < 0.5, -0.0, 0.0).astype(np.float32),
+            (-np.abs(rng.standard_normal(9000)) * 1e-30).astype(np.float32)]
+    base = [int(x) for x in rng.integers(0, 1000, len(rows))]
+    idx, lens = _run_topk(rows, k, base)
+    for t, r in enumerate(rows):
+        ref = O.topk_row(r.astype(np.float64), k)
+        n = min(len(r), k)
+        assert lens[t] == n
+        got = idx[t]
+        assert (got[n:] == -1).all()
+        assert np.array_equal(got[:n], np.sort(ref[:n]) + base[t]), t   # ascending positions
+
+
+def test_topk_random_fp32_many_rows():
+    rng = np.random.default_rng(11)
+    rows = [rng.standard_normal(int(L)).astype(np.float32) * rng.uniform(0.01, 100)
+            for L in rng.integers(1, 40000, 48)]
+    idx, lens = _run_topk(rows, 2048)
+    for t, r in enumerate(rows):
+        ref = O.topk_row(r.astype(np.float64), 2048)
+        n = min(len(r), 2048)
+        assert np.array_equal(idx[t, :n], np.sort(ref[:n]))
+
+
+# ---------------------------------------------------------------- sparse MLA
+
+def _mla_case(fmt, T, H, k, neg=0.1, seed=0, rows=4096, all_neg_row=True):
+    g = torch.Generator().manual_seed(seed)
+    if fmt == I.KV_BF16:
+        pool = I.kv_bf16_pool(rows, seed, 5, "cuda")
+        D = 576
+    elif fmt == I.KV_FP8_UNIFORM:
+        pool = I.kv_uniform_fp8_pool(rows, seed, 5, "cuda")
+        D = 512
+    else:
+        pool = I.kv_packed_pool(rows, 256, seed, 5, "cuda")
+        D = 512
+    idx = torch.stack([torch.randperm(pool.rows, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    idx[torch.rand(T, k, generator=g) < neg] = -1
+    if all_neg_row and T > 1:
+        idx[1] = -1
+    q = I.to_bf16(torch.randn(T, H, D, generator=g)).cuda()
+    return pool, idx.cuda(), q, D
+
+
+@pytest.mark.parametrize("fmt,H,k", [(I.KV_BF16, 8, 300), (I.KV_BF16, 64, 2048),
+                                     (I.KV_BF16, 128, 100), (I.KV_BF16, 16, 1),
+                                     (I.KV_FP8_UNIFORM, 64, 1152), (I.KV_FP8_UNIFORM, 16, 77),
+                                     (I.KV_FP8_DS_MLA, 64, 1024), (I.KV_FP8_DS_MLA, 8, 200)])
+def test_sparse_mla_matches_oracle(fmt, H, k):
+    T = 3
+    pool, idx, q, D = _mla_case(fmt, T, H, k)
+    scale = 1 / math.sqrt(192.0) if D == 576 else 1 / math.sqrt(512.0)
+    flag = _flag()
+    out, lse = ops.dsa_sparse_mla_fwd(q, scale, pool, idx, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(pool), raw(idx), scale,
+                                    out.shape[2])
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "mla")
+    assert (out[1] == 0).all() and torch.isneginf(lse[1]).all()   # all-padded token
+
+
+def test_sparse_mla_two_loop_packed():
+    T, H = 2, 64
+    main = I.kv_packed_pool(T * 256, 256, 3, 6, "cuda")
+    extra = I.kv_packed_pool(8192, 256, 4, 5, "cuda")
+    g = torch.Generator().manual_seed(9)
+    idx_main = (torch.arange(T)[:, None] * 256 + torch.arange(128)[None, :]).to(torch.int32).cuda()
+    idx_extra = torch.stack([torch.randperm(8192, generator=g)[:1024] for _ in range(T)]).to(torch.int32)
+    idx_extra[:, ::9] = -1
+    idx_extra = idx_extra.cuda()
+    q = I.to_bf16(torch.randn(T, H, 512, generator=g)).cuda()
+    scale = 1 / math.sqrt(512.0)
+    out, lse = ops.dsa_sparse_mla_fwd(q, scale, main, idx_main, extra, idx_extra)
+    ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(main), raw(idx_main), scale, 448,
+                                    pool_np(extra), raw(idx_extra))
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "2-loop")
+
+
+def test_sparse_mla_masks_and_flags_out_of_range_entries():
+    pool, idx, q, D = _mla_case(I.KV_BF16, 2, 16, 64, neg=0.0, all_neg_row=False)
+    bad = idx.clone()
+    bad[0, 3] = pool.rows          # one past the end
+    bad[1, 5] = -7                 # below -1
+    flag = _flag()
+    out, lse = ops.dsa_sparse_mla_fwd(q, 0.05, pool, bad, err_flag=flag)
+    assert flag.item() & ops.DEVERR_INDEX_RANGE
+    masked = raw(bad).copy()
+    masked[masked >= pool.rows] = -1
+    masked[masked < -1] = -1
+    ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(pool), masked, 0.05, 512)
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "masked")
+
+
+# ---------------------------------------------------------------- fused decode
+
+def _check_decode(case, idx_gpu, out_gpu, lse_gpu, requests, bit_exact=False):
+    c = decode_case_np(case)
+    idx_gpu = idx_gpu.cpu().numpy()
+    out_gpu = out_gpu.float().cpu().numpy()
+    lse_gpu = lse_gpu.cpu().numpy()
+    for b in requests:
+        r = O.decode_request(b, c)
+        base = int(c["slot_base"][b])
+        pos = np.where(idx_gpu[b] >= 0, idx_gpu[b] - base, -1)
+        n = min(int(c["seq_lens"][b]), case.k)
+        assert (pos[:n] >= 0).all() and (pos[n:] == -1).all(), b
+        if bit_exact:
+            assert np.array_equal(np.sort(pos[:n]), np.sort(r["idx"][:n])), b
+            ref_out, ref_lse = r["out"], r["lse"]
+        else:
+            gset = check_index_sets(pos, r["idx"], r["scores"], case.k)
+            if gset is None:
+                ref_out, ref_lse = r["out"], r["lse"]
+            else:   # tolerated ties: compare attention on the GPU's own selection
+                rows = O.gather_valid(c["kv"], gset + base)
+                if c.get("idx_swa") is not None:
+                    rows = np.concatenate([O.gather_valid(c["kv_swa"], c["idx_swa"][b]), rows])
+                ref_out, ref_lse = O.sparse_mla_one(O.decode_bf16(c["q"][b]), rows,
+                                                    c["softmax_scale"], c["Dv"])
+        check_out_lse(out_gpu[b], lse_gpu[b], ref_out, ref_lse, "request %d" % b)
+
+
+def test_decode_tiny_bit_exact_indices():
+    case = I.tiny_decode(device="cuda")
+    flag = _flag()
+    idx, out, lse = ops.decode_case(case, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    _check_decode(case, idx, out, lse, [0], bit_exact=True)
+
+
+def test_decode_ragged_fp8():
+    case = I.decode_case("ragged", 5, [1, 300, 2048, 2049, 10000], 64, 128, "fp8", 2048, 64,
+                         I.KV_BF16, device="cuda")
+    idx, out, lse = ops.decode_case(case)
+    _check_decode(case, idx, out, lse, range(5))
+
+
+def test_decode_grid_ragged_many_ties_bit_exact():
+    case = I.decode_case("grid", 4, [129, 700, 5000, 33000], 16, 128, "bf16_grid", 128, 16,
+                         I.KV_BF16, device="cuda")
+    idx, out, lse = ops.decode_case(case)
+    _check_decode(case, idx, out, lse, range(4), bit_exact=True)
+
+
+def test_decode_is_deterministic():
+    case = I.decode_case("det", 3, [5000, 20000, 70000], 64, 128, "fp8", 2048, 64, I.KV_BF16,
+                         device="cuda")
+    first = [x.clone() for x in ops.decode_case(case)]
+    for _ in range(5):
+        again = ops.decode_case(case)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
+
+
+def test_decode_sweep_full_size_sampled():
+    """Batch 32 x 128k context, the bench workload; three requests checked."""
+    case = I.decode_sweep(32, 131072, device="cuda")
+    flag = _flag()
+    idx, out, lse = ops.decode_case(case, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    _check_decode(case, idx, out, lse, [0, 17, 31])
+
+
+@pytest.mark.parametrize("N", [512, 2048, 8192])
+def test_decode_sweep_short_contexts(N):
+    case = I.decode_sweep(32 if N < 8192 else 8, N, device="cuda")
+    idx, out, lse = ops.decode_case(case)
+    _check_decode(case, idx, out, lse, [0, case.B - 1])
+
+
+def test_packed_long_context_two_loop_full_size():
+    """1M-token context on packed fp8_ds_mla pages, SWA 128 + top-k 1024."""
+    case = I.packed_long_decode(device="cuda")
+    flag = _flag()
+    idx, out, lse = ops.decode_case(case, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    _check_decode(case, idx, out, lse, [0])
+
+
+def test_uniform_fp8_swa_topk_full_size():
+    """Batch 32, 64k context, uniform fp8 pool, shuffled SWA + top-k lists with 10% -1."""
+    case = I.uniform_fp8_swa_topk_case(device="cuda")
+    flag = _flag()
+    out, lse = ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, case.idx, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    assert (case.idx < 0).sum(dim=1).eq(115).all()
+    qn = O.decode_bf16(raw(case.q))
+    idx = raw(case.idx)
+    pool = pool_np(case.kv)
+    for t in range(case.T):
+        o, l = O.sparse_mla_one(qn[t], O.gather_valid(pool, idx[t]), case.softmax_scale, 448)
+        check_out_lse(out[t].float().cpu().numpy(), lse[t].cpu().numpy(), o, l, "token %d" % t)
+
+
+# ---------------------------------------------------------------- prefill pipeline
+
+def test_prefill_packed_segments_pipeline():
+    """Causal prefill over packed segments (1-token segments included) through
+    the three separate entry points: index score -> top-k -> sparse MLA."""
+    case = I.prefill_case([1, 1, 700, 2600, 300], k=2048, H=16, device="cuda")
+    ind = case.indexer
+    maxL = int((case.row_end - case.row_start).max())
+    sc = ops.dsa_index_score(ind["q_idx"], 1, ind["q_scale"], ind["k_idx"], ind["k_scale"],
+                             ind["w"], case.row_start, case.row_end, maxL)
+    rl = (case.row_end - case.row_start).contiguous()
+    idx, lens = ops.dsa_topk(sc, rl, case.k, maxL, index_base=case.row_start)
+    out, lse = ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, idx)
+    c = prefill_case_np(case)
+    idx_np = idx.cpu().numpy()
+    out_np, lse_np = out.float().cpu().numpy(), lse.cpu().numpy()
+    r0 = raw(case.row_start)
+    for t in [0, 1, 2, 500, 701, 702, 2800, 3301, case.T - 1]:
+        r = O.prefill_token(t, c)
+        pos = np.where(idx_np[t] >= 0, idx_np[t] - r0[t], -1)
+        gset = check_index_sets(pos, r["idx"], r["scores"], case.k)
+        if gset is None:
+            ref_out, ref_lse = r["out"], r["lse"]
+        else:
+            ref_out, ref_lse = O.sparse_mla_one(O.decode_bf16(c["q"][t]),
+                                                O.gather_valid(c["kv"], gset + r0[t]),
+                                                c["softmax_scale"], 512)
+        check_out_lse(out_np[t], lse_np[t], ref_out, ref_lse, "token %d" % t)
