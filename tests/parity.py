@@ -3,7 +3,12 @@
 * indices on integer-grid inputs (fp32 scores exact): bit-exact sets;
 * indices on Gaussian inputs: the selected sets may differ only by positions
   whose oracle score lies within 1e-5 (relative) of the k-th score;
-* out: max-abs <= 1e-2 and relative L2 <= 2e-3 against the fp64 oracle;
+* out: max-abs <= 1e-2 and relative L2 <= 2e-3 against the fp64 oracle.  The
+  max-abs bound is read on the unit scale: |out - ref| <= 1e-2 * max(1, |ref|)
+  element by element.  The output is bf16, whose rounding alone moves a value
+  of magnitude v by up to 2^-9 v; outputs of the fp8 pools with fp32 or UE8M0
+  scales reach tens or thousands, where an absolute 1e-2 is below half a
+  bf16 ulp;
 * lse: |lse - lse_ref| <= 1e-4 * max(1, |lse_ref|); -inf must match -inf.
 When two index sets differ only by tolerated ties, out / lse are compared
 with the oracle evaluated on the GPU's own set.
@@ -43,8 +48,8 @@ def check_out_lse(out, lse, ref_out, ref_lse, what=""):
     ref_lse = np.asarray(ref_lse, dtype=np.float64)
     assert out.shape == ref_out.shape, (out.shape, ref_out.shape)
     assert np.isfinite(out).all(), what + ": non-finite output"
-    err = np.abs(out - ref_out)
-    assert err.max() <= OUT_MAX_ABS, (what, "max-abs", err.max())
+    err = np.abs(out - ref_out) / np.maximum(1.0, np.abs(ref_out))
+    assert err.max() <= OUT_MAX_ABS, (what, "max-abs (unit scale)", err.max())
     den = np.linalg.norm(ref_out)
     if den > 0:
         rel = np.linalg.norm(out - ref_out) / den
