@@ -139,8 +139,7 @@ int dsa_index_score(const void *q_idx, int idx_dtype, const float *q_scale,
  * Row t holds row_len[t] valid scores scores[t*ld_scores + 0 .. len-1].
  * Output row t: the min(len, k) positions with the highest scores, then -1
  * up to k.  Ties: the lower position wins, so the selected SET is unique.
- * Order inside a row: deterministic, positions ascending within each of two
- * runs (those strictly above the threshold bucket, then the rest).
+ * Order inside a row: positions ascending (deterministic).
  * -0.0 ties +0.0.  Scores must not be NaN (unchecked).
  *   index_base [T] int32 or NULL: added to every selected position
  *              (turns request-local positions into pool slots); -1 stays -1
