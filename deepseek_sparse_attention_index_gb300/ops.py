@@ -47,6 +47,7 @@ _SIGS = {
     "dsa_topk_workspace_size": (c_sz, [c_i32, c_i64, c_i32]),
     "dsa_topk": (c_i32, [c_p, c_i64, c_p, c_i32, c_i64, c_i32, c_p, c_p, c_p, c_p, c_sz, c_p,
                          c_p]),
+    "dsa_topk_noalloc": (c_i32, [c_p, c_i64, c_p, c_i32, c_i64, c_i32, c_p, c_p, c_p, c_p, c_p]),
     "dsa_sparse_mla_workspace_size": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "dsa_sparse_mla_fwd": (c_i32, [c_p, c_i32, c_i32, c_i32, c_i32, c_f32,
                                    ctypes.POINTER(DsaKvPool), c_p, c_i32,

@@ -154,6 +154,30 @@ int dsa_topk(const float *scores, int64_t ld_scores, const int32_t *row_len, int
              int32_t *err_flag, dsa_stream_t stream);
 
 /*
+ * dsa_topk_noalloc -- dsa_topk for callers that cannot allocate device memory.
+ * No passage of the DSA pages has a counterpart: this is a service of this
+ * library.  Some callers cannot call cudaMalloc or reach an allocator -- for
+ * example a plugin whose host framework hands it only its input and output
+ * buffers, or code on a latency-critical path where an allocation (which may
+ * synchronise the device) is not allowed.  This entry point takes the same
+ * arguments as dsa_topk minus the workspace and produces the same result; its
+ * scratch memory is a static device array of DSA_TOPK_NOALLOC_SCRATCH_BYTES
+ * (4 MiB) that every GPU loading the library holds until the process exits.
+ * Limit: the scratch of T rows must fit, i.e. dsa_topk_workspace_size(T,
+ * max_len, k) <= 4 MiB (up to 46 rows at k = 2048); larger calls return
+ * DSA_ERR_UNSUPPORTED without launching anything.
+ * The first call on a device looks up the array's device address (with that
+ * device current), so make that first call before any stream capture.  All
+ * calls share the array and it keeps the last call's contents; each call
+ * clears what must start at zero.  Calls whose work overlaps on the GPU race
+ * on the array: serialise them.  The function allocates nothing.
+ */
+#define DSA_TOPK_NOALLOC_SCRATCH_BYTES (4u << 20)
+int dsa_topk_noalloc(const float *scores, int64_t ld_scores, const int32_t *row_len, int T,
+                     int64_t max_len, int k, const int32_t *index_base,
+                     int32_t *idx, int32_t *lens, int32_t *err_flag, dsa_stream_t stream);
+
+/*
  * dsa_sparse_mla_fwd -- absorbed-MLA attention over selected latent rows.
  * The "sparse attn" stage of tokenspeed PR #627; semantics of miles PR #3608
  * (FlashMLA-style forward: natural-log lse; -1 masked) and the pool formats
