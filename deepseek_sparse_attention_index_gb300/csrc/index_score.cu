@@ -1,146 +1,381 @@
-// Lightning-indexer scores  I[t,s] = sum_h w[t,h] * ReLU(sq[t,h] sk[s] q[t,h,:].k[s,:])
-// (the "scores" stage of tokenspeed PR #627 "Add gluon kernel for DSA").
+// Lightning-indexer scores on the 5th-generation tensor cores
+// (the "scores" stage of tokenspeed PR #627 "Add gluon kernel for DSA"):
 //
-// Since the fp8 scales are positive, sk[s] leaves the ReLU and the head sum
-// (ReLU(c x) = c ReLU(x) for c > 0) and sq[t,h] is folded into the query
-// once per CTA: score = sk[s] * sum_h w[t,h] * ReLU((sq[t,h] q8[t,h,:]) . k8[s,:]).
+//   I[t,s] = sum_h w[t,h] * ReLU(sq[t,h] sk[s] q[t,h,:].k[s,:])
 //
-// The optional fused histogram feeds the first radix level of the top-k
-// (topk.cu): the 12-bit bin of each stored score is counted per row.
+// One 128-key tile of the index-k cache is the A operand (M = 128 rows,
+// K = d, K-major, 128-byte swizzle, loaded by TMA); the query's H_I head rows
+// are the B operand (N = H_I rounded up to 16).  D = A B^T lands in TMEM as
+// one key per lane and one head per column, so the epilogue's weighted ReLU
+// reduction over heads is thread-local.  The fp8 scales are positive, so
+// sq[t,h] folds into the head weight and sk[s] leaves the head sum:
+//   I[t,s] = sk[s] * sum_h (w[t,h] sq[t,h]) * ReLU(q8[t,h,:].k8[s,:]).
+//
+// Persistent warp-specialised CTA (one per SM): warp 0 issues TMA loads into
+// an 8-stage ring (fp8 d = 128 or bf16 d = 64; 4 stages for bf16 d = 128),
+// warp 1 issues tcgen05.mma into two TMEM accumulators, warps 2-5 drain the
+// accumulators, write the score row and (decode) count each score's 12-bit
+// bin for the first radix level of the top-k (topk.cu).
+// Every wait is bounded (tc::mbar_wait): a stuck CTA raises
+// DSA_DEVERR_TIMEOUT and winds down instead of hanging.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace dsa {
 
 namespace {
 
-constexpr int kKeysPerCta = 128;
-constexpr int kChunk = 32;  // key dims decoded per step
+constexpr int kTileKeys = 128;
+constexpr int kThreads = 192;     // 6 warps
+constexpr int kEpiThreads = 128;  // warps 2..5
+constexpr int kHistBinsLocal = kHistBins;
 
-template <int HMAX>
-__global__ void __launch_bounds__(kKeysPerCta)
-index_score_simt_kernel(IndexScoreArgs a) {
-  extern __shared__ float smem[];
-  float *q_s = smem;                 // [HMAX][d], scales folded in
-  float *w_s = smem + HMAX * a.d;    // [HMAX]
-  const int t = blockIdx.y;
-  int64_t r0, r1;
+struct IdxSmem {
+  // offsets in bytes from the 1024-aligned base
+  uint32_t stage0, stage_bytes, q0, q_bytes, hist, bars;
+  int stages;
+  uint32_t total;
+};
+
+__host__ __device__ inline IdxSmem idx_smem_layout(int N, int kblocks) {
+  IdxSmem L;
+  L.stage_bytes = kTileKeys * 128 * kblocks;
+  L.stages = kblocks == 1 ? 8 : 4;
+  L.stage0 = 0;
+  L.q0 = L.stage0 + L.stage_bytes * L.stages;
+  L.q_bytes = N * 128 * kblocks;  // N * 128 is a multiple of 1024 for N >= 8
+  L.hist = L.q0 + 2 * L.q_bytes;
+  L.bars = L.hist + kHistBinsLocal * 4;
+  L.total = L.bars + 256;
+  return L;
+}
+
+struct RowInfo {
+  int64_t r0;
+  int64_t len;
+  bool bad;
+};
+
+__device__ __forceinline__ RowInfo row_info(const IndexScoreArgs &a, int t) {
+  RowInfo r;
+  int64_t s, e;
   if (a.slot_base) {
-    r0 = a.slot_base[t];
-    r1 = r0 + a.seq_lens[t];
+    s = a.slot_base[t];
+    e = s + a.seq_lens[t];
   } else {
-    r0 = a.row_start[t];
-    r1 = a.row_end[t];
+    s = a.row_start[t];
+    e = a.row_end[t];
   }
-  if (r0 < 0 || r1 < r0 || r1 > a.k_rows) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) raise_flag(a.err_flag, DSA_DEVERR_INDEX_RANGE);
-    return;
-  }
-  const int64_t L = r1 - r0;
-  const int64_t j0 = (int64_t)blockIdx.x * kKeysPerCta;
-  if (j0 >= L) return;
-  const int H = a.H_I, d = a.d;
-  const bool fp8 = a.idx_dtype == DSA_IDX_FP8_E4M3;
-  for (int i = threadIdx.x; i < H * d; i += blockDim.x) {
-    const int h = i / d;
-    float v;
-    if (fp8) {
-      v = e4m3_to_float(static_cast<const uint8_t *>(a.q_idx)[(size_t)t * H * d + i]) *
-          a.q_scale[(size_t)t * H + h];
-    } else {
-      v = bf16_bits_to_float(static_cast<const uint16_t *>(a.q_idx)[(size_t)t * H * d + i]);
-    }
-    q_s[h * d + (i % d)] = v;
-  }
-  for (int h = threadIdx.x; h < H; h += blockDim.x) w_s[h] = a.w[(size_t)t * H + h];
-  __syncthreads();
+  r.bad = s < 0 || e < s || e > a.k_rows;
+  r.r0 = s;
+  r.len = r.bad ? 0 : e - s;
+  return r;
+}
 
-  const int64_t j = j0 + threadIdx.x;
-  const bool valid = j < L;
-  float score = 0.f;
-  if (valid) {
-    const int64_t s = r0 + j;
-    float acc[HMAX];
-#pragma unroll
-    for (int h = 0; h < HMAX; ++h) acc[h] = 0.f;
-    for (int c0 = 0; c0 < d; c0 += kChunk) {
-      float kf[kChunk];
-      if (fp8) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            static_cast<const uint8_t *>(a.k_idx) + s * d + c0);
-#pragma unroll
-        for (int v = 0; v < kChunk / 16; ++v) {
-          uint4 raw = __ldg(src + v);
-          const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float2 lo = e4m3x2_to_float2((uint16_t)(wds[q] & 0xffffu));
-            float2 hi = e4m3x2_to_float2((uint16_t)(wds[q] >> 16));
-            kf[v * 16 + q * 4 + 0] = lo.x;
-            kf[v * 16 + q * 4 + 1] = lo.y;
-            kf[v * 16 + q * 4 + 2] = hi.x;
-            kf[v * 16 + q * 4 + 3] = hi.y;
+template <bool FP8, int N, int KB>
+__global__ void __launch_bounds__(kThreads, 1)
+index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap qmap, IndexScoreArgs a,
+                      int64_t tiles_per_row, int64_t tiles_per_cta) {
+  extern __shared__ unsigned char smem_raw[];
+  const IdxSmem L = idx_smem_layout(N, KB);
+  unsigned char *base = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(base + L.bars);
+  uint64_t *full = bars;                 // [8]
+  uint64_t *empty = bars + 8;            // [8]
+  uint64_t *qfull = bars + 16;           // [2]
+  uint64_t *qempty = bars + 18;          // [2]
+  uint64_t *tfull = bars + 20;           // [2]
+  uint64_t *tempty = bars + 22;          // [2]
+  uint64_t *done = bars + 24;            // [1]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 25);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 26);
+  uint32_t *hist_s = reinterpret_cast<uint32_t *>(base + L.hist);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = L.stages;
+  constexpr uint32_t kTmemCols = (2 * N < 32) ? 32 : 2 * N;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&qfull[i], 1);
+      tc::mbar_init(&qempty[i], 1);
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], 4);
+    }
+    tc::mbar_init(done, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp >= 2) {
+    for (int i = threadIdx.x - 64; i < kHistBinsLocal; i += kEpiThreads) hist_s[i] = 0;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int64_t total = (int64_t)a.T * tiles_per_row;
+  const int64_t v0 = (int64_t)blockIdx.x * tiles_per_cta;
+  const int64_t v1 = min(total, v0 + tiles_per_cta);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&kmap);
+      tc::prefetch_tmap(&qmap);
+      int stage = 0;
+      uint32_t phase = 0;
+      int qs = 0;
+      uint32_t qphase = 0;
+      int cur_t = -1;
+      uint32_t issued = 0;         // bit i: stage i has had a load
+      uint32_t last_phase = 0;     // bit i: parity of stage i's last load
+      uint32_t q_issued = 0, q_last = 0;
+      bool ok = true;
+      for (int64_t v = v0; v < v1 && ok; ++v) {
+        const int t = (int)(v / tiles_per_row);
+        const int64_t j = v % tiles_per_row;
+        const RowInfo ri = row_info(a, t);
+        if (j * kTileKeys >= ri.len) continue;
+        if (t != cur_t) {
+          if (cur_t >= 0) {
+            qs ^= 1;
+            if (qs == 0) qphase ^= 1;
           }
+          if (!tc::mbar_wait(&qempty[qs], qphase ^ 1, abort_flag)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(&qfull[qs], L.q_bytes);
+          for (int kb = 0; kb < KB; ++kb)
+            tc::tma_load_2d(&qmap, &qfull[qs], base + L.q0 + qs * L.q_bytes + kb * N * 128,
+                            kb * (FP8 ? 128 : 64), t * a.H_I);
+          q_issued |= 1u << qs;
+          q_last = (q_last & ~(1u << qs)) | (qphase << qs);
+          cur_t = t;
         }
-      } else {
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            static_cast<const uint16_t *>(a.k_idx) + s * d + c0);
-#pragma unroll
-        for (int v = 0; v < kChunk / 8; ++v) {
-          uint4 raw = __ldg(src + v);
-          const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            kf[v * 8 + q * 2 + 0] = __uint_as_float(wds[q] << 16);
-            kf[v * 8 + q * 2 + 1] = __uint_as_float(wds[q] & 0xffff0000u);
-          }
+        if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+        tc::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
+        const int y = (int)(ri.r0 + j * kTileKeys);
+        for (int kb = 0; kb < KB; ++kb)
+          tc::tma_load_2d(&kmap, &full[stage], base + L.stage0 + stage * L.stage_bytes + kb * 16384,
+                          kb * (FP8 ? 128 : 64), y);
+        issued |= 1u << stage;
+        last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
         }
       }
-#pragma unroll
-      for (int h = 0; h < HMAX; ++h) {
-        if (h < H) {
-          const float *qh = q_s + h * d + c0;
-          float x = acc[h];
-#pragma unroll
-          for (int c = 0; c < kChunk; ++c) x = fmaf(qh[c], kf[c], x);
-          acc[h] = x;
+      // every load this thread issued must land before the CTA exits
+      for (int i = 0; i < S; ++i)
+        if (issued & (1u << i)) tc::mbar_wait_drain(&full[i], (last_phase >> i) & 1u);
+      for (int i = 0; i < 2; ++i)
+        if (q_issued & (1u << i)) tc::mbar_wait_drain(&qfull[i], (q_last >> i) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc =
+          tc::idesc_f32acc(FP8 ? 0u : 1u, FP8 ? 0u : 1u, 0u, 0u, (uint32_t)N, 128u);
+      int stage = 0;
+      uint32_t phase = 0;
+      int qs = 0;
+      uint32_t qphase = 0;
+      int cur_t = -1;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool any = false;
+      for (int64_t v = v0; v < v1; ++v) {
+        const int t = (int)(v / tiles_per_row);
+        const int64_t j = v % tiles_per_row;
+        const RowInfo ri = row_info(a, t);
+        if (j * kTileKeys >= ri.len) continue;
+        if (t != cur_t) {
+          if (cur_t >= 0) {
+            tc::mma_commit(&qempty[qs]);  // the old query slot is free once its MMAs finish
+            qs ^= 1;
+            if (qs == 0) qphase ^= 1;
+          }
+          if (!tc::mbar_wait(&qfull[qs], qphase, abort_flag)) break;
+          cur_t = t;
         }
+        if (!tc::mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) break;
+        if (!tc::mbar_wait(&full[stage], phase, abort_flag)) break;
+        tc::fence_after_sync();
+        const uint32_t a_addr = tc::smem_u32(base + L.stage0 + stage * L.stage_bytes);
+        const uint32_t b_addr = tc::smem_u32(base + L.q0 + qs * L.q_bytes);
+        const uint64_t adesc0 = tc::sdesc_sw128(a_addr, 16, 1024);
+        const uint64_t bdesc0 = tc::sdesc_sw128(b_addr, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4 * KB; ++kk) {
+          // 32 bytes of K per instruction (K = 32 fp8 or 16 bf16), 4 per 128 B block
+          const uint32_t a_off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint32_t b_off = (kk >> 2) * N * 128 + (kk & 3) * 32;
+          const uint64_t ad = adesc0 + (a_off >> 4);
+          const uint64_t bd = bdesc0 + (b_off >> 4);
+          if constexpr (FP8)
+            tc::mma_f8f6f4(tmem_base + acc * N, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          else
+            tc::mma_f16(tmem_base + acc * N, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&empty[stage]);
+        tc::mma_commit(&tfull[acc]);
+        any = true;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (any) {
+        // all MMAs retired before TMEM is released
+        tc::mma_commit(done);
+        tc::mbar_wait_drain(done, 0);
       }
     }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;         // 0..127
+    const int quad = warp & 3;               // TMEM lane quadrant this warp may read
+    const int row_in_tile = quad * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int cur_t = -1;
+    bool hist_on = false;
+    RowInfo ri{0, 0, false};
+    float wq[N];
+    for (int64_t v = v0; v < v1; ++v) {
+      const int t = (int)(v / tiles_per_row);
+      const int64_t j = v % tiles_per_row;
+      if (t != cur_t) {
+        ri = row_info(a, t);
+        if (ri.bad && j == 0 && et == 0) raise_flag(a.err_flag, DSA_DEVERR_INDEX_RANGE);
+      }
+      if (j * kTileKeys >= ri.len) continue;
+      if (t != cur_t) {
+        if (hist_on) {  // flush the previous row's bin counts
+          tc::named_bar_sync(1, kEpiThreads);
+          uint32_t *gh = a.hist + (size_t)cur_t * kHistBins;
+          for (int i = et; i < kHistBinsLocal; i += kEpiThreads) {
+            const uint32_t c = hist_s[i];
+            if (c) {
+              atomicAdd(&gh[i], c);
+              hist_s[i] = 0;
+            }
+          }
+          tc::named_bar_sync(1, kEpiThreads);
+        }
+        hist_on = a.hist != nullptr && ri.len > a.topk_k;
 #pragma unroll
-    for (int h = 0; h < HMAX; ++h)
-      if (h < H) score = fmaf(w_s[h], fmaxf(acc[h], 0.f), score);
-    if (fp8) score *= a.k_scale[s];
-    a.scores[(int64_t)t * a.ld_scores + j] = score;
-  }
-  if (a.hist && L > a.topk_k) {
-    // warp-aggregated count of this warp's bins
-    const uint32_t bin = score_key(score) >> 20;
-    const unsigned act = __ballot_sync(0xffffffffu, valid);
-    if (valid) {
-      const unsigned peers = __match_any_sync(act, bin);
-      if ((int)lane_id() == __ffs(peers) - 1)
-        atomicAdd(&a.hist[(size_t)t * kHistBins + bin], (uint32_t)__popc(peers));
+        for (int h = 0; h < N; ++h) {
+          float wv = 0.f;
+          if (h < a.H_I) {
+            wv = a.w[(size_t)t * a.H_I + h];
+            if (FP8) wv *= a.q_scale[(size_t)t * a.H_I + h];
+          }
+          wq[h] = wv;
+        }
+        cur_t = t;
+      }
+      if (!tc::mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
+      tc::fence_after_sync();
+      float d[N];
+      tc::tmem_ld_cols<N>(tmem_base + ((uint32_t)(quad * 32) << 16) + acc * N, d);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+      const int64_t key = j * kTileKeys + row_in_tile;
+      const bool valid = key < ri.len;
+      float score = 0.f;
+#pragma unroll
+      for (int h = 0; h < N; ++h)
+        if (h < a.H_I) score = fmaf(wq[h], fmaxf(d[h], 0.f), score);
+      if (valid) {
+        if (FP8) score *= a.k_scale[ri.r0 + key];
+        a.scores[(int64_t)t * a.ld_scores + key] = score;
+      }
+      if (hist_on) {
+        const uint32_t bin = score_key(score) >> 20;
+        const unsigned act = __ballot_sync(0xffffffffu, valid);
+        if (valid) {
+          const unsigned peers = __match_any_sync(act, bin);
+          if (lane == __ffs(peers) - 1) atomicAdd(&hist_s[bin], (uint32_t)__popc(peers));
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    if (hist_on) {
+      tc::named_bar_sync(1, kEpiThreads);
+      uint32_t *gh = a.hist + (size_t)cur_t * kHistBins;
+      for (int i = et; i < kHistBinsLocal; i += kEpiThreads) {
+        const uint32_t c = hist_s[i];
+        if (c) atomicAdd(&gh[i], c);
+      }
     }
   }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) raise_flag(a.err_flag, DSA_DEVERR_TIMEOUT);
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <bool FP8, int N, int KB>
+cudaError_t launch_tc(const IndexScoreArgs &a, cudaStream_t s) {
+  CUtensorMap kmap, qmap;
+  const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int eb = FP8 ? 1 : 2;
+  const uint32_t box_cols = FP8 ? 128 : 64;  // 128 bytes
+  if (!make_tmap_2d(&kmap, a.k_idx, dt, eb, (uint64_t)a.k_rows, (uint64_t)a.d, kTileKeys, box_cols))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&qmap, a.q_idx, dt, eb, (uint64_t)a.T * a.H_I, (uint64_t)a.d, N, box_cols))
+    return cudaErrorInvalidValue;
+  const int64_t tiles_per_row = (a.max_len + kTileKeys - 1) / kTileKeys;
+  const int64_t total = (int64_t)a.T * tiles_per_row;
+  const int64_t grid = std::min<int64_t>(num_sms(), total);
+  const int64_t per = (total + grid - 1) / grid;
+  const IdxSmem L = idx_smem_layout(N, KB);
+  const size_t smem = L.total + 1024;
+  auto kern = index_score_tc_kernel<FP8, N, KB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)grid, kThreads, smem, s>>>(kmap, qmap, a, tiles_per_row, per);
+  return cudaGetLastError();
+}
+
+template <bool FP8, int KB>
+cudaError_t launch_heads(const IndexScoreArgs &a, cudaStream_t s) {
+  if (a.H_I <= 16) return launch_tc<FP8, 16, KB>(a, s);
+  if (a.H_I <= 32) return launch_tc<FP8, 32, KB>(a, s);
+  return launch_tc<FP8, 64, KB>(a, s);
 }
 
 }  // namespace
 
 cudaError_t index_score_launch(const IndexScoreArgs &a, cudaStream_t s) {
   if (a.T == 0 || a.max_len == 0) return cudaSuccess;
-  dim3 grid((unsigned)((a.max_len + kKeysPerCta - 1) / kKeysPerCta), (unsigned)a.T);
-  const size_t smem = sizeof(float) * ((size_t)DSA_MAX_INDEX_HEADS * a.d + DSA_MAX_INDEX_HEADS);
-  if (a.H_I <= 8) {
-    index_score_simt_kernel<8><<<grid, kKeysPerCta, smem, s>>>(a);
-  } else if (a.H_I <= 16) {
-    index_score_simt_kernel<16><<<grid, kKeysPerCta, smem, s>>>(a);
-  } else if (a.H_I <= 32) {
-    index_score_simt_kernel<32><<<grid, kKeysPerCta, smem, s>>>(a);
-  } else {
-    index_score_simt_kernel<64><<<grid, kKeysPerCta, smem, s>>>(a);
-  }
-  return cudaGetLastError();
+  if (a.idx_dtype == DSA_IDX_FP8_E4M3) return launch_heads<true, 1>(a, s);
+  if (a.d == 64) return launch_heads<false, 1>(a, s);
+  return launch_heads<false, 2>(a, s);
 }
 
 }  // namespace dsa
