@@ -272,11 +272,12 @@ mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ p
 }  // namespace
 
 int mla_num_splits(int T, int H, int k_total) {
+  // one CTA per SM: as many pieces per (token, head group) as fit in one wave,
+  // each piece at least one 64-row tile
   const int hgroups = (H + kHeadsPerCta - 1) / kHeadsPerCta;
   const int ctas_per_split = T * hgroups;
-  const int target = 2 * num_sms();
-  int s = (target + ctas_per_split - 1) / ctas_per_split;
-  s = min(s, (k_total + 63) / 64);  // at least 64 rows a piece
+  int s = num_sms() / max(ctas_per_split, 1);
+  s = min(s, (k_total + 63) / 64);
   return max(s, 1);
 }
 
@@ -303,7 +304,9 @@ cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s) {
                       sizeof(__nv_bfloat16) * kHeadsPerCta * kQStride;
   dim3 grid((unsigned)a.T, (unsigned)a.n_splits, (unsigned)((a.H + kHeadsPerCta - 1) / kHeadsPerCta));
   cudaError_t e;
-  if (a.Dv == 512) {
+  if (a.kv.format == DSA_KV_BF16 && (a.k2 == 0 || a.kv2.format == DSA_KV_BF16)) {
+    e = sparse_mla_tc_bf16_launch(a, s);
+  } else if (a.Dv == 512) {
     e = cudaFuncSetAttribute(sparse_mla_simt_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;

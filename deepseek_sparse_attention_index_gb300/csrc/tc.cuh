@@ -190,6 +190,33 @@ DSA_DEVINLINE void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
   for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 32 bits stores, 16 / 32 / 64 consecutive columns of this lane.
+DSA_DEVINLINE void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+DSA_DEVINLINE void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Multiply N consecutive fp32 columns of this lane by alpha[0..N) (in place).
+template <int N>
+DSA_DEVINLINE void tmem_scale_cols(uint32_t taddr, const float *alpha) {
+#pragma unroll
+  for (int c0 = 0; c0 < N; c0 += 16) {
+    uint32_t r[16];
+    tmem_ld_x16(taddr + c0, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha[c0 + i]);
+    tmem_st_x16(taddr + c0, r);
+  }
+  tmem_st_wait();
+}
+
 // Named barrier over `count` threads (warp multiples), id 1..15.
 DSA_DEVINLINE void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -214,7 +241,7 @@ DSA_DEVINLINE uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
 // Instruction descriptor for kind::f16 / kind::f8f6f4 with fp32 accumulate.
 // a_fmt / b_fmt: kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3.
 // a_mn / b_mn: 0 = K-major, 1 = MN-major.
-constexpr uint32_t idesc_f32acc(uint32_t a_fmt, uint32_t b_fmt, uint32_t a_mn, uint32_t b_mn,
+__host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t a_fmt, uint32_t b_fmt, uint32_t a_mn, uint32_t b_mn,
                                 uint32_t N, uint32_t M) {
   return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (a_mn << 15) | (b_mn << 16) |
          ((N >> 3) << 17) | ((M >> 4) << 24);
