@@ -32,6 +32,7 @@ constexpr int kTileKeys = 128;
 constexpr int kThreads = 192;     // 6 warps
 constexpr int kEpiThreads = 128;  // warps 2..5
 constexpr int kHistBinsLocal = kHistBins;
+constexpr int kAcc = 4;           // TMEM accumulators in flight
 
 struct IdxSmem {
   // offsets in bytes from the 1024-aligned base
@@ -89,17 +90,17 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   uint64_t *empty = bars + 8;            // [8]
   uint64_t *qfull = bars + 16;           // [2]
   uint64_t *qempty = bars + 18;          // [2]
-  uint64_t *tfull = bars + 20;           // [2]
-  uint64_t *tempty = bars + 22;          // [2]
-  uint64_t *done = bars + 24;            // [1]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 25);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 26);
+  uint64_t *tfull = bars + 20;           // [kAcc]
+  uint64_t *tempty = bars + 24;          // [kAcc]
+  uint64_t *done = bars + 28;            // [1]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 29);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 30);
   uint32_t *hist_s = reinterpret_cast<uint32_t *>(base + L.hist);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = L.stages;
-  constexpr uint32_t kTmemCols = (2 * N < 32) ? 32 : 2 * N;
+  constexpr uint32_t kTmemCols = (kAcc * N < 32) ? 32 : kAcc * N;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -109,6 +110,8 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&qfull[i], 1);
       tc::mbar_init(&qempty[i], 1);
+    }
+    for (int i = 0; i < kAcc; ++i) {
       tc::mbar_init(&tfull[i], 1);
       tc::mbar_init(&tempty[i], 4);
     }
@@ -238,8 +241,10 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           stage = 0;
           phase ^= 1;
         }
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if (++acc == kAcc) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
       if (any) {
         // all MMAs retired before TMEM is released
@@ -259,7 +264,22 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     bool hist_on = false;
     RowInfo ri{0, 0, false};
     float wq[N];
+    // per-key fp8 scale of this lane's key, loaded two tiles ahead so that the
+    // memory round trip overlaps the work on earlier tiles
+    auto load_sk = [&](int64_t v) -> float {
+      if (!FP8 || v >= v1) return 1.f;
+      const int tt = (int)(v / tiles_per_row);
+      const int64_t jj = v % tiles_per_row;
+      const RowInfo r2 = row_info(a, tt);
+      const int64_t key = jj * kTileKeys + row_in_tile;
+      return key < r2.len ? __ldg(a.k_scale + r2.r0 + key) : 1.f;
+    };
+    float sk0 = load_sk(v0), sk1 = load_sk(v0 + 1);
     for (int64_t v = v0; v < v1; ++v) {
+      const float sk2 = load_sk(v + 2);
+      const float sk = sk0;
+      sk0 = sk1;
+      sk1 = sk2;
       const int t = (int)(v / tiles_per_row);
       const int64_t j = v % tiles_per_row;
       if (t != cur_t) {
@@ -305,10 +325,8 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
       for (int h = 0; h < N; ++h)
         if (h < a.H_I) score = fmaf(wq[h], fmaxf(d[h], 0.f), score);
-      if (valid) {
-        if (FP8) score *= a.k_scale[ri.r0 + key];
-        a.scores[(int64_t)t * a.ld_scores + key] = score;
-      }
+      if (FP8) score *= sk;
+      if (valid) a.scores[(int64_t)t * a.ld_scores + key] = score;
       if (hist_on) {
         const uint32_t bin = score_key(score) >> 20;
         const unsigned act = __ballot_sync(0xffffffffu, valid);
@@ -317,8 +335,10 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           if (lane == __ffs(peers) - 1) atomicAdd(&hist_s[bin], (uint32_t)__popc(peers));
         }
       }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if (++acc == kAcc) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
     }
     if (hist_on) {
       tc::named_bar_sync(1, kEpiThreads);

@@ -256,9 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
                         (kb > 0 || ko > 0) ? 1u : 0u);
         }
         tc::mma_commit(&sfull[st]);
-        if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
+        // PV(i) right after S(i): the stage of tile i is then freed as early as
+        // possible, so the gather of tile i + 2 overlaps S(i+1), softmax(i+1)
+        // and PV(i+1)
+        if (!issue_pv(i)) { ok = false; break; }
       }
-      if (ok && nt > 0) ok = issue_pv(nt - 1);
       if (nt > 0) {
         tc::mma_commit(done);
         tc::mbar_wait_drain(done, 0);
