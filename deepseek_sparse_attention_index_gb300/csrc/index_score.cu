@@ -33,10 +33,12 @@ constexpr int kThreads = 192;     // 6 warps
 constexpr int kEpiThreads = 128;  // warps 2..5
 constexpr int kHistBinsLocal = kHistBins;
 constexpr int kAcc = 4;           // TMEM accumulators in flight
+constexpr int kScBox = 132;       // fp32 scales per tile load: 128 keys + up to 3 lead-in
+constexpr int kScBytes = 640;     // kScBox * 4 rounded up to 128 (TMA destinations are 128-byte aligned)
 
 struct IdxSmem {
   // offsets in bytes from the 1024-aligned base
-  uint32_t stage0, stage_bytes, q0, q_bytes, hist, bars;
+  uint32_t stage0, stage_bytes, q0, q_bytes, hist, sc, bars;
   int stages;
   uint32_t total;
 };
@@ -49,7 +51,8 @@ __host__ __device__ inline IdxSmem idx_smem_layout(int N, int kblocks) {
   L.q0 = L.stage0 + L.stage_bytes * L.stages;
   L.q_bytes = N * 128 * kblocks;  // N * 128 is a multiple of 1024 for N >= 8
   L.hist = L.q0 + 2 * L.q_bytes;
-  L.bars = L.hist + kHistBinsLocal * 4;
+  L.sc = L.hist + kHistBinsLocal * 4;   // per stage: the tile's 128 key scales (+4 lead-in)
+  L.bars = L.sc + L.stages * kScBytes;
   L.total = L.bars + 256;
   return L;
 }
@@ -79,7 +82,8 @@ __device__ __forceinline__ RowInfo row_info(const IndexScoreArgs &a, int t) {
 template <bool FP8, int N, int KB>
 __global__ void __launch_bounds__(kThreads, 1)
 index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap qmap, IndexScoreArgs a,
+                      const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap smap, IndexScoreArgs a,
                       int64_t tiles_per_row, int64_t tiles_per_cta) {
   extern __shared__ unsigned char smem_raw[];
   const IdxSmem L = idx_smem_layout(N, KB);
@@ -96,6 +100,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 29);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 30);
   uint32_t *hist_s = reinterpret_cast<uint32_t *>(base + L.hist);
+  const float *sc_s = reinterpret_cast<const float *>(base + L.sc);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -105,7 +110,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 1);
+      tc::mbar_init(&empty[i], FP8 ? 5 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&qfull[i], 1);
@@ -140,6 +145,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     if (lane == 0) {
       tc::prefetch_tmap(&kmap);
       tc::prefetch_tmap(&qmap);
+      if (FP8) tc::prefetch_tmap(&smap);
       int stage = 0;
       uint32_t phase = 0;
       int qs = 0;
@@ -149,10 +155,15 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       uint32_t last_phase = 0;     // bit i: parity of stage i's last load
       uint32_t q_issued = 0, q_last = 0;
       bool ok = true;
+      RowInfo ri{0, 0, false};
+      int ri_t = -1;
       for (int64_t v = v0; v < v1 && ok; ++v) {
         const int t = (int)(v / tiles_per_row);
         const int64_t j = v % tiles_per_row;
-        const RowInfo ri = row_info(a, t);
+        if (t != ri_t) {
+          ri = row_info(a, t);
+          ri_t = t;
+        }
         if (j * kTileKeys >= ri.len) continue;
         if (t != cur_t) {
           if (cur_t >= 0) {
@@ -169,11 +180,13 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           cur_t = t;
         }
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-        tc::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
+        tc::mbar_arrive_expect_tx(&full[stage], L.stage_bytes + (FP8 ? kScBox * 4 : 0));
         const int y = (int)(ri.r0 + j * kTileKeys);
         for (int kb = 0; kb < KB; ++kb)
           tc::tma_load_2d(&kmap, &full[stage], base + L.stage0 + stage * L.stage_bytes + kb * 16384,
                           kb * (FP8 ? 128 : 64), y);
+        // the 128 key scales, from the nearest 16-byte boundary at or below y
+        if (FP8) tc::tma_load_1d(&smap, &full[stage], base + L.sc + stage * kScBytes, y & ~3);
         issued |= 1u << stage;
         last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == S) {
@@ -201,10 +214,15 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       int acc = 0;
       uint32_t acc_phase = 0;
       bool any = false;
+      RowInfo ri{0, 0, false};
+      int ri_t = -1;
       for (int64_t v = v0; v < v1; ++v) {
         const int t = (int)(v / tiles_per_row);
         const int64_t j = v % tiles_per_row;
-        const RowInfo ri = row_info(a, t);
+        if (t != ri_t) {
+          ri = row_info(a, t);
+          ri_t = t;
+        }
         if (j * kTileKeys >= ri.len) continue;
         if (t != cur_t) {
           if (cur_t >= 0) {
@@ -264,22 +282,9 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     bool hist_on = false;
     RowInfo ri{0, 0, false};
     float wq[N];
-    // per-key fp8 scale of this lane's key, loaded two tiles ahead so that the
-    // memory round trip overlaps the work on earlier tiles
-    auto load_sk = [&](int64_t v) -> float {
-      if (!FP8 || v >= v1) return 1.f;
-      const int tt = (int)(v / tiles_per_row);
-      const int64_t jj = v % tiles_per_row;
-      const RowInfo r2 = row_info(a, tt);
-      const int64_t key = jj * kTileKeys + row_in_tile;
-      return key < r2.len ? __ldg(a.k_scale + r2.r0 + key) : 1.f;
-    };
-    float sk0 = load_sk(v0), sk1 = load_sk(v0 + 1);
+    int stage = 0;                           // stage of the tile (same sequence as the producer)
+    uint32_t phase = 0;
     for (int64_t v = v0; v < v1; ++v) {
-      const float sk2 = load_sk(v + 2);
-      const float sk = sk0;
-      sk0 = sk1;
-      sk1 = sk2;
       const int t = (int)(v / tiles_per_row);
       const int64_t j = v % tiles_per_row;
       if (t != cur_t) {
@@ -321,20 +326,26 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       if (lane == 0) tc::mbar_arrive(&tempty[acc]);
       const int64_t key = j * kTileKeys + row_in_tile;
       const bool valid = key < ri.len;
+      float sk = 1.f;
+      if (FP8) {
+        // the stage's scales landed with the tile (already complete); then
+        // release the stage from the epilogue side
+        if (!tc::mbar_wait(&full[stage], phase, abort_flag)) break;
+        sk = sc_s[stage * (kScBytes / 4) + (int)((ri.r0 + j * kTileKeys) & 3) + row_in_tile];
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[stage]);
+      }
+      if (++stage == L.stages) {
+        stage = 0;
+        phase ^= 1;
+      }
       float score = 0.f;
 #pragma unroll
       for (int h = 0; h < N; ++h)
         if (h < a.H_I) score = fmaf(wq[h], fmaxf(d[h], 0.f), score);
       if (FP8) score *= sk;
       if (valid) a.scores[(int64_t)t * a.ld_scores + key] = score;
-      if (hist_on) {
-        const uint32_t bin = score_key(score) >> 20;
-        const unsigned act = __ballot_sync(0xffffffffu, valid);
-        if (valid) {
-          const unsigned peers = __match_any_sync(act, bin);
-          if (lane == __ffs(peers) - 1) atomicAdd(&hist_s[bin], (uint32_t)__popc(peers));
-        }
-      }
+      if (hist_on && valid) atomicAdd(&hist_s[score_key(score) >> 20], 1u);
       if (++acc == kAcc) {
         acc = 0;
         acc_phase ^= 1;
@@ -369,6 +380,10 @@ cudaError_t launch_tc(const IndexScoreArgs &a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   if (!make_tmap_2d(&qmap, a.q_idx, dt, eb, (uint64_t)a.T * a.H_I, (uint64_t)a.d, N, box_cols))
     return cudaErrorInvalidValue;
+  CUtensorMap smap = kmap;   // unused for bf16
+  if (FP8 && !make_tmap_1d(&smap, a.k_scale, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                           (uint64_t)a.k_rows, kScBox))
+    return cudaErrorInvalidValue;
   const int64_t tiles_per_row = (a.max_len + kTileKeys - 1) / kTileKeys;
   const int64_t total = (int64_t)a.T * tiles_per_row;
   const int64_t grid = std::min<int64_t>(num_sms(), total);
@@ -378,7 +393,7 @@ cudaError_t launch_tc(const IndexScoreArgs &a, cudaStream_t s) {
   auto kern = index_score_tc_kernel<FP8, N, KB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)grid, kThreads, smem, s>>>(kmap, qmap, a, tiles_per_row, per);
+  kern<<<(unsigned)grid, kThreads, smem, s>>>(kmap, qmap, smap, a, tiles_per_row, per);
   return cudaGetLastError();
 }
 

@@ -14,7 +14,7 @@ constexpr int kCandCap = 8192;    // candidates per row kept for the resolve pas
 
 struct TopkWs {
   uint32_t *hist;    // [T][kHistBins]        zeroed before the histogram pass
-  uint32_t *cnt;     // [T][2] (gt, eq)       zeroed before the collect pass
+  uint32_t *cnt;     // [T][4] (gt, eq, CTAs done, pad), zeroed before the collect pass
   int32_t *gt_list;  // [T][k]
   uint2 *cand;       // [T][kCandCap]  (key, position)
 };

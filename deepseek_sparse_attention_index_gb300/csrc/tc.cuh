@@ -90,6 +90,12 @@ DSA_DEVINLINE void tma_load_2d(const CUtensorMap *map, uint64_t *bar, void *dst,
       : "memory");
 }
 
+// Tile load of `box` elements starting at element x of a map made by
+// make_tmap_1d.  The caller keeps x * element size a multiple of 16 bytes.
+DSA_DEVINLINE void tma_load_1d(const CUtensorMap *map, uint64_t *bar, void *dst, int x) {
+  tma_load_2d(map, bar, dst, x, 0);
+}
+
 DSA_DEVINLINE void prefetch_tmap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -289,5 +295,9 @@ DSA_DEVINLINE bool elect_one() {
 // [box_rows, box_cols], 128-byte swizzle, zero fill out of bounds.
 bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
                   uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols);
+// Tiled tensor map over a vector of n elements (one row of a 2-D map), box
+// `box` elements, no swizzle, zero fill out of bounds.
+bool make_tmap_1d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                  uint64_t n, uint32_t box);
 
 }  // namespace dsa

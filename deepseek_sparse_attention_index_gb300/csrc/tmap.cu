@@ -34,4 +34,20 @@ bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_1d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                  uint64_t n, uint32_t box) {
+  // encoded as one row of a 2-D tensor (the row stride only has to be a
+  // multiple of 16 bytes; with a single row it is never stepped)
+  std::call_once(g_once, resolve);
+  if (!g_encode) return false;
+  cuuint64_t dims[2] = {n, 1};
+  cuuint64_t strides[1] = {((n * (cuuint64_t)elem_bytes) + 15) & ~(cuuint64_t)15};
+  cuuint32_t boxd[2] = {box, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base), dims, strides, boxd, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace dsa

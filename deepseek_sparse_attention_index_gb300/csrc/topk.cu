@@ -30,7 +30,6 @@ namespace dsa {
 namespace {
 
 constexpr int kCollectThreads = 512;
-constexpr int kResolveThreads = 1024;
 constexpr int kHistThreads = 512;
 
 // Exclusive prefix sum over the block (blockDim.x a multiple of 32, <= 1024).
@@ -93,6 +92,31 @@ __device__ void find_bin(const uint32_t *h, int nbins, uint32_t need, bool desce
   __syncthreads();
 }
 
+
+// Loads this thread's 16 elements of the chunk window starting at `base`:
+// element (r, c) is position base + 4 * (r * blockDim.x + threadIdx.x) + c.
+// Four float4 loads in flight at once when the row is 16-byte aligned, else
+// scalar loads.  Positions at or past `hi` are reported invalid.
+struct Elems16 {
+  float v[16];
+  int64_t p0[4];
+};
+__device__ __forceinline__ void load16(const float *row, int64_t base, int64_t hi, bool vec,
+                                       Elems16 &E) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int64_t p = base + 4 * ((int64_t)r * blockDim.x + threadIdx.x);
+    E.p0[r] = p;
+    if (vec && p + 3 < hi) {
+      const float4 q = __ldcg(reinterpret_cast<const float4 *>(row + p));
+      E.v[4 * r] = q.x; E.v[4 * r + 1] = q.y; E.v[4 * r + 2] = q.z; E.v[4 * r + 3] = q.w;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) E.v[4 * r + c] = (p + c < hi) ? __ldcg(row + p + c) : 0.f;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kHistThreads)
 topk_hist_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restrict__ row_len,
                  int k, int chunk, uint32_t *__restrict__ hist) {
@@ -105,67 +129,18 @@ topk_hist_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
   __syncthreads();
   const float *row = scores + (int64_t)t * ld;
-  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x)
-    atomicAdd(&sh[score_key(row[i]) >> 20], 1u);
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+  for (int64_t base = lo; base < hi; base += 16 * (int64_t)blockDim.x) {
+    Elems16 E;
+    load16(row, base, hi, vec, E);
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (E.p0[e >> 2] + (e & 3) < hi) atomicAdd(&sh[score_key(E.v[e]) >> 20], 1u);
+  }
   __syncthreads();
   uint32_t *gh = hist + (size_t)t * kHistBins;
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
     if (sh[i]) atomicAdd(&gh[i], sh[i]);
-}
-
-__global__ void __launch_bounds__(kCollectThreads)
-topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
-                    const int32_t *__restrict__ row_len, int k, int chunk,
-                    const uint32_t *__restrict__ hist, uint32_t *__restrict__ cnt,
-                    int32_t *__restrict__ gt_list, uint2 *__restrict__ cand) {
-  __shared__ uint32_t sh[kHistBins];
-  __shared__ uint32_t warp_sums[32];
-  __shared__ int s_bin;
-  __shared__ uint32_t s_before;
-  const int t = blockIdx.y;
-  const int64_t L = max(row_len[t], 0);
-  const int64_t lo = (int64_t)blockIdx.x * chunk;
-  if (L <= k || lo >= L) return;
-  const int64_t hi = min(L, lo + chunk);
-  const uint32_t *gh = hist + (size_t)t * kHistBins;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = gh[i];
-  if (threadIdx.x == 0) { s_bin = 0; s_before = 0; }
-  __syncthreads();
-  find_bin(sh, kHistBins, (uint32_t)k, true, warp_sums, &s_bin, &s_before);
-  const uint32_t b1 = (uint32_t)s_bin;
-  const float *row = scores + (int64_t)t * ld;
-  const unsigned lane = lane_id();
-  const unsigned lt_mask = (1u << lane) - 1u;
-  uint32_t *c_gt = cnt + 2 * t;
-  uint32_t *c_eq = c_gt + 1;
-  int32_t *gl = gt_list + (size_t)t * k;
-  uint2 *cl = cand + (size_t)t * kCandCap;
-  for (int64_t base = lo; base < hi; base += blockDim.x) {
-    const int64_t i = base + threadIdx.x;
-    const bool valid = i < hi;
-    const uint32_t key = valid ? score_key(row[i]) : 0u;
-    const uint32_t bin = key >> 20;
-    const bool is_gt = valid && bin > b1;
-    const bool is_eq = valid && bin == b1;
-    const unsigned mg = __ballot_sync(0xffffffffu, is_gt);
-    if (mg) {
-      uint32_t off = 0;
-      const int leader = __ffs(mg) - 1;
-      if ((int)lane == leader) off = atomicAdd(c_gt, (uint32_t)__popc(mg));
-      off = __shfl_sync(0xffffffffu, off, leader);
-      const uint32_t my = off + __popc(mg & lt_mask);
-      if (is_gt && my < (uint32_t)k) gl[my] = (int32_t)i;
-    }
-    const unsigned me = __ballot_sync(0xffffffffu, is_eq);
-    if (me) {
-      uint32_t off = 0;
-      const int leader = __ffs(me) - 1;
-      if ((int)lane == leader) off = atomicAdd(c_eq, (uint32_t)__popc(me));
-      off = __shfl_sync(0xffffffffu, off, leader);
-      const uint32_t my = off + __popc(me & lt_mask);
-      if (is_eq && my < (uint32_t)kCandCap) cl[my] = make_uint2(key, (uint32_t)i);
-    }
-  }
 }
 
 // Source of (key, position) pairs for the resolve passes: the candidate list,
@@ -189,21 +164,32 @@ struct Source {
   }
 };
 
-__global__ void __launch_bounds__(kResolveThreads)
-topk_resolve_kernel(const float *__restrict__ scores, int64_t ld,
-                    const int32_t *__restrict__ row_len, int k,
-                    const int32_t *__restrict__ index_base,
-                    const uint32_t *__restrict__ hist, const uint32_t *__restrict__ cnt,
-                    const int32_t *__restrict__ gt_list, const uint2 *__restrict__ cand,
-                    int32_t *__restrict__ idx, int32_t *__restrict__ lens,
-                    int32_t *err_flag) {
-  __shared__ uint32_t sh[kHistBins];
-  __shared__ int32_t sel[DSA_MAX_TOPK];
-  __shared__ uint32_t warp_sums[32];
-  __shared__ int s_bin;
-  __shared__ uint32_t s_before;
-  __shared__ uint32_t s_fill;
-  const int t = blockIdx.x;
+// Resolves row t once its collect pass is complete: two more radix levels
+// over the candidates give the exact k-th key, a radix select over positions
+// breaks ties toward lower positions, and the k survivors are sorted by
+// position.  Run by one whole CTA (blockDim.x a multiple of 32 dividing 512).
+struct ResolveSmem {
+  uint32_t sh[kHistBins];
+  int32_t sel[DSA_MAX_TOPK];
+  uint32_t warp_sums[32];
+  int s_bin;
+  uint32_t s_before;
+  uint32_t s_fill;
+};
+
+__device__ __noinline__ void resolve_row(int t, ResolveSmem &S, const float *__restrict__ scores, int64_t ld,
+                            const int32_t *__restrict__ row_len, int k,
+                            const int32_t *__restrict__ index_base,
+                            const uint32_t *__restrict__ hist, const uint32_t *__restrict__ cnt,
+                            const int32_t *__restrict__ gt_list, const uint2 *__restrict__ cand,
+                            int32_t *__restrict__ idx, int32_t *__restrict__ lens,
+                            int32_t *err_flag) {
+  uint32_t *sh = S.sh;
+  int32_t *sel = S.sel;
+  uint32_t *warp_sums = S.warp_sums;
+  int &s_bin = S.s_bin;
+  uint32_t &s_before = S.s_before;
+  uint32_t &s_fill = S.s_fill;
   const int64_t L = max(row_len[t], 0);
   const int32_t base = index_base ? index_base[t] : 0;
   int32_t *out = idx + (size_t)t * k;
@@ -219,8 +205,8 @@ topk_resolve_kernel(const float *__restrict__ scores, int64_t ld,
   __syncthreads();
   find_bin(sh, kHistBins, (uint32_t)k, true, warp_sums, &s_bin, &s_before);
   const uint32_t b1 = (uint32_t)s_bin;
-  const uint32_t n_gt = cnt[2 * t];
-  const uint32_t n_eq = cnt[2 * t + 1];
+  const uint32_t n_gt = cnt[4 * t];
+  const uint32_t n_eq = cnt[4 * t + 1];
   if (n_gt != s_before || n_gt >= (uint32_t)k) {
     // histogram and collect pass disagree: only NaN scores can do this
     if (threadIdx.x == 0) raise_flag(err_flag, DSA_DEVERR_INDEX_RANGE);
@@ -257,11 +243,12 @@ topk_resolve_kernel(const float *__restrict__ scores, int64_t ld,
     if (src.get(i, key, pos) && ((key >> 8) & 0xFFFu) == b2) atomicAdd(&sh[key & 0xFFu], 1u);
   }
   __syncthreads();
-  // 256 bins: use a 256-thread view of find_bin by padding to blockDim bins
-  for (int i = 256 + threadIdx.x; i < kResolveThreads; i += blockDim.x) sh[i] = 0;
+  // 256 bins padded with zero bins to a multiple of the block size
+  const int nb3 = max(256, (int)blockDim.x);
+  for (int i = 256 + threadIdx.x; i < nb3; i += blockDim.x) sh[i] = 0;
   __syncthreads();
-  // bins 256..1023 are zero; walking descending from 1023 passes them first
-  find_bin(sh, kResolveThreads, r2, true, warp_sums, &s_bin, &s_before);
+  // the zero bins sit above bin 255; walking down from the top passes them first
+  find_bin(sh, nb3, r2, true, warp_sums, &s_bin, &s_before);
   const uint32_t b3 = (uint32_t)s_bin;
   const uint32_t r3 = r2 - s_before;  // how many elements equal to K* to keep
   const uint32_t m_eq = sh[b3];       // how many elements equal K*
@@ -333,6 +320,99 @@ topk_resolve_kernel(const float *__restrict__ scores, int64_t ld,
   if (lens && threadIdx.x == 0) lens[t] = k;
 }
 
+// Collect pass, and the resolve of each row by the last of its CTAs to finish
+// (every CTA fences its writes and bumps the row's done counter; the CTA that
+// sees the count complete resolves the row -- nobody waits on anybody).
+// Each CTA appends its "above the threshold bin" positions and its
+// "in the threshold bin" candidates with one atomic per list: per-thread
+// counts go through a block scan, thread 0 reserves the CTA's range.
+__global__ void __launch_bounds__(kCollectThreads, 2)
+topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
+                    const int32_t *__restrict__ row_len, int k, int chunk,
+                    const int32_t *__restrict__ index_base, const uint32_t *__restrict__ hist,
+                    uint32_t *__restrict__ cnt, int32_t *__restrict__ gt_list,
+                    uint2 *__restrict__ cand, int32_t *__restrict__ idx,
+                    int32_t *__restrict__ lens, int32_t *err_flag) {
+  __shared__ ResolveSmem S;
+  __shared__ uint32_t s_base_gt, s_base_eq;
+  __shared__ int s_last;
+  const int t = blockIdx.y;
+  const int64_t L = max(row_len[t], 0);
+  if (L <= k) {                     // every position is selected: no search
+    if (blockIdx.x == 0) {
+      const int32_t base = index_base ? index_base[t] : 0;
+      int32_t *out = idx + (size_t)t * k;
+      for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < L ? (int32_t)j + base : -1;
+      if (lens && threadIdx.x == 0) lens[t] = (int32_t)L;
+    }
+    return;
+  }
+  const int64_t lo = (int64_t)blockIdx.x * chunk;
+  if (lo >= L) return;
+  const int64_t hi = min(L, lo + chunk);
+  const float *row = scores + (int64_t)t * ld;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+  Elems16 E;
+  load16(row, lo, hi, vec, E);   // first window in flight while the threshold is found
+  const uint32_t *gh = hist + (size_t)t * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) S.sh[i] = gh[i];
+  if (threadIdx.x == 0) { S.s_bin = 0; S.s_before = 0; }
+  __syncthreads();
+  find_bin(S.sh, kHistBins, (uint32_t)k, true, S.warp_sums, &S.s_bin, &S.s_before);
+  const uint32_t b1 = (uint32_t)S.s_bin;
+  uint32_t *c_gt = cnt + 4 * t;
+  uint32_t *c_eq = c_gt + 1;
+  uint32_t *c_done = c_gt + 2;
+  int32_t *gl = gt_list + (size_t)t * k;
+  uint2 *cl = cand + (size_t)t * kCandCap;
+  for (int64_t base = lo; base < hi; base += 16 * (int64_t)blockDim.x) {
+    if (base != lo) load16(row, base, hi, vec, E);
+    uint32_t mgt = 0, meq = 0;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const bool valid = E.p0[e >> 2] + (e & 3) < hi;
+      const uint32_t bin = score_key(E.v[e]) >> 20;
+      mgt |= (valid && bin > b1) ? (1u << e) : 0u;
+      meq |= (valid && bin == b1) ? (1u << e) : 0u;
+    }
+    // counts packed (gt << 16 | eq): a CTA round holds at most 16 * 1024 elements
+    uint32_t tot;
+    const uint32_t pre = block_excl_scan(((uint32_t)__popc(mgt) << 16) | (uint32_t)__popc(meq),
+                                         S.warp_sums, &tot);
+    if (threadIdx.x == 0) {
+      s_base_gt = (tot >> 16) ? atomicAdd(c_gt, tot >> 16) : 0u;
+      s_base_eq = (tot & 0xffffu) ? atomicAdd(c_eq, tot & 0xffffu) : 0u;
+    }
+    __syncthreads();
+    uint32_t og = s_base_gt + (pre >> 16), oe = s_base_eq + (pre & 0xffffu);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int64_t i = E.p0[e >> 2] + (e & 3);
+      if ((mgt >> e) & 1u) {
+        if (og < (uint32_t)k) gl[og] = (int32_t)i;
+        ++og;
+      }
+      if ((meq >> e) & 1u) {
+        if (oe < (uint32_t)kCandCap) cl[oe] = make_uint2(score_key(E.v[e]), (uint32_t)i);
+        ++oe;
+      }
+    }
+    __syncthreads();   // s_base_* are reused by the next round
+  }
+  // publish this CTA's appends; the last CTA of the row resolves it
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t nch = (uint32_t)((L + chunk - 1) / chunk);
+    s_last = atomicAdd(c_done, 1u) == nch - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  resolve_row(t, S, scores, ld, row_len, k, index_base, hist, cnt, gt_list, cand, idx, lens,
+              err_flag);
+}
+
 int collect_chunk(int T, int64_t max_len) {
   // enough CTAs to cover the GPU about twice, 2k..16k positions each
   int64_t target = 2LL * num_sms();
@@ -347,7 +427,7 @@ size_t topk_ws_layout(int T, int k, void *ws, TopkWs *out) {
   WsCarver c(ws);
   TopkWs w;
   w.hist = c.take<uint32_t>((size_t)T * kHistBins);
-  w.cnt = c.take<uint32_t>((size_t)T * 2);
+  w.cnt = c.take<uint32_t>((size_t)T * 4);   // gt, eq, CTAs done, pad
   w.gt_list = c.take<int32_t>((size_t)T * k);
   w.cand = c.take<uint2>((size_t)T * kCandCap);
   if (out) *out = w;
@@ -357,7 +437,7 @@ size_t topk_ws_layout(int T, int k, void *ws, TopkWs *out) {
 cudaError_t topk_clear(const TopkWs &w, int T, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(w.hist, 0, sizeof(uint32_t) * (size_t)T * kHistBins, s);
   if (e != cudaSuccess) return e;
-  return cudaMemsetAsync(w.cnt, 0, sizeof(uint32_t) * (size_t)T * 2, s);
+  return cudaMemsetAsync(w.cnt, 0, sizeof(uint32_t) * (size_t)T * 4, s);
 }
 
 cudaError_t topk_hist(const float *scores, int64_t ld, const int32_t *row_len, int T,
@@ -372,17 +452,12 @@ cudaError_t topk_hist(const float *scores, int64_t ld, const int32_t *row_len, i
 cudaError_t topk_select(const float *scores, int64_t ld, const int32_t *row_len, int T,
                         int64_t max_len, int k, const int32_t *index_base, int32_t *idx,
                         int32_t *lens, const TopkWs &w, int32_t *err_flag, cudaStream_t s) {
-  if (max_len > k) {
-    const int chunk = collect_chunk(T, max_len);
-    dim3 grid((unsigned)((max_len + chunk - 1) / chunk), (unsigned)T);
-    topk_collect_kernel<<<grid, kCollectThreads, 0, s>>>(scores, ld, row_len, k, chunk, w.hist,
-                                                          w.cnt, w.gt_list, w.cand);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  topk_resolve_kernel<<<T, kResolveThreads, 0, s>>>(scores, ld, row_len, k, index_base, w.hist,
-                                                    w.cnt, w.gt_list, w.cand, idx, lens,
-                                                    err_flag);
+  const int chunk = collect_chunk(T, max_len);
+  const int64_t nch = max_len > k ? (max_len + chunk - 1) / chunk : 1;
+  dim3 grid((unsigned)nch, (unsigned)T);
+  topk_collect_kernel<<<grid, kCollectThreads, 0, s>>>(scores, ld, row_len, k, chunk, index_base,
+                                                        w.hist, w.cnt, w.gt_list, w.cand, idx,
+                                                        lens, err_flag);
   return cudaGetLastError();
 }
 
