@@ -29,12 +29,13 @@ namespace dsa {
 namespace {
 
 constexpr int kTileKeys = 128;
-constexpr int kThreads = 192;     // 6 warps
-constexpr int kEpiThreads = 128;  // warps 2..5
+constexpr int kThreads = 320;     // 10 warps
+constexpr int kEpiThreads = 256;  // warps 2..9: two groups of four, alternate tiles
 constexpr int kHistBinsLocal = kHistBins;
-constexpr int kAcc = 4;           // TMEM accumulators in flight
+constexpr int kAcc = 8;           // TMEM accumulators in flight (8 x 64 columns = all of TMEM)
 constexpr int kScBox = 132;       // fp32 scales per tile load: 128 keys + up to 3 lead-in
 constexpr int kScBytes = 640;     // kScBox * 4 rounded up to 128 (TMA destinations are 128-byte aligned)
+constexpr int kScSlots = 16;      // ring of per-tile scale slots, released by the epilogue
 
 struct IdxSmem {
   // offsets in bytes from the 1024-aligned base
@@ -46,14 +47,14 @@ struct IdxSmem {
 __host__ __device__ inline IdxSmem idx_smem_layout(int N, int kblocks) {
   IdxSmem L;
   L.stage_bytes = kTileKeys * 128 * kblocks;
-  L.stages = kblocks == 1 ? 8 : 4;
+  L.stages = kblocks == 1 ? 11 : 5;
   L.stage0 = 0;
   L.q0 = L.stage0 + L.stage_bytes * L.stages;
   L.q_bytes = N * 128 * kblocks;  // N * 128 is a multiple of 1024 for N >= 8
   L.hist = L.q0 + 2 * L.q_bytes;
-  L.sc = L.hist + kHistBinsLocal * 4;   // per stage: the tile's 128 key scales (+4 lead-in)
-  L.bars = L.sc + L.stages * kScBytes;
-  L.total = L.bars + 256;
+  L.sc = L.hist + kHistBinsLocal * 4;   // kScSlots x (the tile's 128 key scales, +4 lead-in)
+  L.bars = L.sc + kScSlots * kScBytes;
+  L.total = L.bars + 640;
   return L;
 }
 
@@ -90,15 +91,17 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   unsigned char *base = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(base + L.bars);
-  uint64_t *full = bars;                 // [8]
-  uint64_t *empty = bars + 8;            // [8]
-  uint64_t *qfull = bars + 16;           // [2]
-  uint64_t *qempty = bars + 18;          // [2]
-  uint64_t *tfull = bars + 20;           // [kAcc]
-  uint64_t *tempty = bars + 24;          // [kAcc]
-  uint64_t *done = bars + 28;            // [1]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 29);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 30);
+  uint64_t *full = bars;                 // [stages <= 12]
+  uint64_t *empty = bars + 12;           // [stages]
+  uint64_t *scfull = bars + 24;          // [kScSlots]
+  uint64_t *scempty = bars + 40;         // [kScSlots]
+  uint64_t *qfull = bars + 56;           // [2]
+  uint64_t *qempty = bars + 58;          // [2]
+  uint64_t *tfull = bars + 60;           // [kAcc]
+  uint64_t *tempty = bars + 68;          // [kAcc]
+  uint64_t *done = bars + 76;            // [1]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 77);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 78);
   uint32_t *hist_s = reinterpret_cast<uint32_t *>(base + L.hist);
   const float *sc_s = reinterpret_cast<const float *>(base + L.sc);
 
@@ -110,7 +113,11 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], FP8 ? 5 : 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < kScSlots; ++i) {
+      tc::mbar_init(&scfull[i], 1);
+      tc::mbar_init(&scempty[i], 4);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&qfull[i], 1);
@@ -154,12 +161,19 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       uint32_t issued = 0;         // bit i: stage i has had a load
       uint32_t last_phase = 0;     // bit i: parity of stage i's last load
       uint32_t q_issued = 0, q_last = 0;
+      int ss = 0;                  // scale slot (FP8)
+      uint32_t sphase = 0;
+      uint32_t s_issued = 0, s_last = 0;
       bool ok = true;
       RowInfo ri{0, 0, false};
       int ri_t = -1;
-      for (int64_t v = v0; v < v1 && ok; ++v) {
-        const int t = (int)(v / tiles_per_row);
-        const int64_t j = v % tiles_per_row;
+      // tile v = t * tiles_per_row + j: one division up front, then counters
+      int t_it = (int)(v0 / tiles_per_row);
+      int64_t j_it = v0 - (int64_t)t_it * tiles_per_row;
+      for (int64_t v = v0; v < v1 && ok;
+           ++v, (++j_it == tiles_per_row ? (j_it = 0, ++t_it) : 0)) {
+        const int t = t_it;
+        const int64_t j = j_it;
         if (t != ri_t) {
           ri = row_info(a, t);
           ri_t = t;
@@ -180,13 +194,24 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           cur_t = t;
         }
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-        tc::mbar_arrive_expect_tx(&full[stage], L.stage_bytes + (FP8 ? kScBox * 4 : 0));
+        tc::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
         const int y = (int)(ri.r0 + j * kTileKeys);
         for (int kb = 0; kb < KB; ++kb)
           tc::tma_load_2d(&kmap, &full[stage], base + L.stage0 + stage * L.stage_bytes + kb * 16384,
                           kb * (FP8 ? 128 : 64), y);
-        // the 128 key scales, from the nearest 16-byte boundary at or below y
-        if (FP8) tc::tma_load_1d(&smap, &full[stage], base + L.sc + stage * kScBytes, y & ~3);
+        if (FP8) {
+          // the 128 key scales, from the nearest 16-byte boundary at or below y,
+          // into their own ring (held until the epilogue has read them)
+          if (!tc::mbar_wait(&scempty[ss], sphase ^ 1, abort_flag)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(&scfull[ss], kScBox * 4);
+          tc::tma_load_1d(&smap, &scfull[ss], base + L.sc + ss * kScBytes, y & ~3);
+          s_issued |= 1u << ss;
+          s_last = (s_last & ~(1u << ss)) | (sphase << ss);
+          if (++ss == kScSlots) {
+            ss = 0;
+            sphase ^= 1;
+          }
+        }
         issued |= 1u << stage;
         last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == S) {
@@ -199,6 +224,8 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         if (issued & (1u << i)) tc::mbar_wait_drain(&full[i], (last_phase >> i) & 1u);
       for (int i = 0; i < 2; ++i)
         if (q_issued & (1u << i)) tc::mbar_wait_drain(&qfull[i], (q_last >> i) & 1u);
+      for (int i = 0; i < kScSlots; ++i)
+        if (s_issued & (1u << i)) tc::mbar_wait_drain(&scfull[i], (s_last >> i) & 1u);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -216,9 +243,13 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       bool any = false;
       RowInfo ri{0, 0, false};
       int ri_t = -1;
-      for (int64_t v = v0; v < v1; ++v) {
-        const int t = (int)(v / tiles_per_row);
-        const int64_t j = v % tiles_per_row;
+      // tile v = t * tiles_per_row + j: one division up front, then counters
+      int t_it = (int)(v0 / tiles_per_row);
+      int64_t j_it = v0 - (int64_t)t_it * tiles_per_row;
+      for (int64_t v = v0; v < v1;
+           ++v, (++j_it == tiles_per_row ? (j_it = 0, ++t_it) : 0)) {
+        const int t = t_it;
+        const int64_t j = j_it;
         if (t != ri_t) {
           ri = row_info(a, t);
           ri_t = t;
@@ -273,27 +304,35 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int et = threadIdx.x - 64;         // 0..127
+    // Two groups of four warps (each group covers the four TMEM lane
+    // quadrants) take alternate tiles.  Both groups walk the same tile
+    // sequence, so they meet at the same row-change flushes.  A warp whose
+    // wait gave up keeps walking (doing no work) so that no warp is left alone
+    // at a named barrier.
+    const int et = threadIdx.x - 64;         // 0..255
+    const int group = et >> 7;
     const int quad = warp & 3;               // TMEM lane quadrant this warp may read
     const int row_in_tile = quad * 32 + lane;
-    int acc = 0;
-    uint32_t acc_phase = 0;
     int cur_t = -1;
     bool hist_on = false;
+    bool dead = false;
     RowInfo ri{0, 0, false};
     float wq[N];
-    int stage = 0;                           // stage of the tile (same sequence as the producer)
-    uint32_t phase = 0;
-    for (int64_t v = v0; v < v1; ++v) {
-      const int t = (int)(v / tiles_per_row);
-      const int64_t j = v % tiles_per_row;
+    int64_t n = 0;                           // valid tiles so far (same sequence as the producer)
+    // tile v = t * tiles_per_row + j: one division up front, then counters
+    int t_it = (int)(v0 / tiles_per_row);
+    int64_t j_it = v0 - (int64_t)t_it * tiles_per_row;
+    for (int64_t v = v0; v < v1;
+         ++v, (++j_it == tiles_per_row ? (j_it = 0, ++t_it) : 0)) {
+      const int t = t_it;
+      const int64_t j = j_it;
       if (t != cur_t) {
         ri = row_info(a, t);
         if (ri.bad && j == 0 && et == 0) raise_flag(a.err_flag, DSA_DEVERR_INDEX_RANGE);
       }
       if (j * kTileKeys >= ri.len) continue;
       if (t != cur_t) {
-        if (hist_on) {  // flush the previous row's bin counts
+        if (hist_on) {  // flush the previous row's bin counts (both groups)
           tc::named_bar_sync(1, kEpiThreads);
           uint32_t *gh = a.hist + (size_t)cur_t * kHistBins;
           for (int i = et; i < kHistBinsLocal; i += kEpiThreads) {
@@ -317,7 +356,11 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         cur_t = t;
       }
-      if (!tc::mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
+      const int64_t my_n = n++;
+      if (dead || (int)(my_n & 1) != group) continue;
+      const int acc = (int)(my_n % kAcc);
+      const uint32_t acc_phase = (uint32_t)((my_n / kAcc) & 1);
+      if (!tc::mbar_wait(&tfull[acc], acc_phase, abort_flag)) { dead = true; continue; }
       tc::fence_after_sync();
       float d[N];
       tc::tmem_ld_cols<N>(tmem_base + ((uint32_t)(quad * 32) << 16) + acc * N, d);
@@ -328,16 +371,14 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       const bool valid = key < ri.len;
       float sk = 1.f;
       if (FP8) {
-        // the stage's scales landed with the tile (already complete); then
-        // release the stage from the epilogue side
-        if (!tc::mbar_wait(&full[stage], phase, abort_flag)) break;
-        sk = sc_s[stage * (kScBytes / 4) + (int)((ri.r0 + j * kTileKeys) & 3) + row_in_tile];
+        const int ss = (int)(my_n % kScSlots);
+        if (!tc::mbar_wait(&scfull[ss], (uint32_t)((my_n / kScSlots) & 1), abort_flag)) {
+          dead = true;
+          continue;
+        }
+        sk = sc_s[ss * (kScBytes / 4) + (int)((ri.r0 + j * kTileKeys) & 3) + row_in_tile];
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&empty[stage]);
-      }
-      if (++stage == L.stages) {
-        stage = 0;
-        phase ^= 1;
+        if (lane == 0) tc::mbar_arrive(&scempty[ss]);
       }
       float score = 0.f;
 #pragma unroll
@@ -346,10 +387,6 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       if (FP8) score *= sk;
       if (valid) a.scores[(int64_t)t * a.ld_scores + key] = score;
       if (hist_on && valid) atomicAdd(&hist_s[score_key(score) >> 20], 1u);
-      if (++acc == kAcc) {
-        acc = 0;
-        acc_phase ^= 1;
-      }
     }
     if (hist_on) {
       tc::named_bar_sync(1, kEpiThreads);

@@ -57,8 +57,21 @@ DSA_DEVINLINE bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Wait until the phase of `bar` with the given parity has completed.
 // Returns false (and sets *abort) if the wait gave up or another role of the
 // CTA already aborted.
+// Non-blocking test of the phase with the given parity.
+DSA_DEVINLINE bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 DSA_DEVINLINE bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;   // already complete: no suspend
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort) return false;
