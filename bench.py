@@ -8,8 +8,11 @@ inputs.  One step = index score -> top-k -> sparse MLA (-> split combine) for
 all 32 requests, through the C ABI entry point dsa_decode.
 
 Timing: W warm-up steps, then K steps each bracketed by CUDA events on the
-launching stream; between timed steps a 256 MiB buffer is written to flush
-the L2 (the flush is outside the events).  Multi-GPU runs (torchrun) are
+launching stream; between timed steps a 256 MiB buffer is written and a
+second 256 MiB buffer is read, so the L2 holds neither step inputs nor dirty
+lines whose write-back would be charged to the next step (the flush is
+outside the events).  A GPU-side sleep ahead of each timed loop lets the host
+queue its launches first, so host launch latency stays out of the events.  Multi-GPU runs (torchrun) are
 independent replicas: the path does not shard across GPUs.
 
 Prints one JSON line.  `--impl reference` times the CPU oracle instead (the
@@ -45,7 +48,7 @@ def workload_config(B, N, k):
     return {"workload": "decode_b%d_n%d" % (B, N), "batch": B, "context": N, "topk": k,
             "heads": 64, "index_heads": 64, "index_dim": 128, "index_dtype": "fp8_e4m3",
             "kv_format": "bf16 latent 576 (Dv 512)",
-            "l2": "flushed between timed steps (256 MiB write); index-k sweep 553 MB > L2",
+            "l2": "flushed between timed steps (256 MiB write, then 256 MiB read); index-k sweep 553 MB > L2",
             "parallelism": "replicas"}
 
 
@@ -126,6 +129,11 @@ def run_ours(args, rank, world):
     out = torch.empty((Bsz, H, Dv), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((Bsz, H), dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def l2_flush(i):
+        flush.fill_(i & 0xff)
+        flush_rd.sum()
     stream = torch.cuda.current_stream()
 
     def step():
@@ -144,8 +152,9 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
+    torch.cuda._sleep(50_000_000)   # ~25 ms of GPU time while the host queues the steps
     for i in range(args.steps):
-        flush.fill_(i & 0xff)
+        l2_flush(i)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -168,8 +177,11 @@ def run_ours(args, rank, world):
     tws = ops.workspace(ops.dsa_topk_workspace_size(Bsz, N, k), dev)
     mws = ops.workspace(ops.dsa_sparse_mla_workspace_size(Bsz, H, Dv, k, 0), dev)
     stage_ms = {"index_score": [], "topk": [], "sparse_mla": []}
-    for i in range(max(3, min(args.steps, 10))):
-        flush.fill_(i & 0xff)
+    n_stage = max(3, min(args.steps, 10))
+    stage_ev = []
+    torch.cuda._sleep(50_000_000)
+    for i in range(n_stage):
+        l2_flush(i)
         e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         e[0].record(stream)
         ops.dsa_index_score(ind["q_idx"], ind["idx_dtype"], ind["q_scale"], ind["k_idx"],
@@ -180,7 +192,9 @@ def run_ours(args, rank, world):
         ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, idx_out, out=out, lse=lse,
                                ws=mws)
         e[3].record(stream)
-        torch.cuda.synchronize()
+        stage_ev.append(e)
+    torch.cuda.synchronize()
+    for e in stage_ev:
         stage_ms["index_score"].append(e[0].elapsed_time(e[1]))
         stage_ms["topk"].append(e[1].elapsed_time(e[2]))
         stage_ms["sparse_mla"].append(e[2].elapsed_time(e[3]))
@@ -228,7 +242,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = []
     for i in range(args.steps):
-        flush.fill_(i & 0xff)
+        l2_flush(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_step()

@@ -11,11 +11,14 @@
 // sq[t,h] folds into the head weight and sk[s] leaves the head sum:
 //   I[t,s] = sk[s] * sum_h (w[t,h] sq[t,h]) * ReLU(q8[t,h,:].k8[s,:]).
 //
-// Persistent warp-specialised CTA (one per SM): warp 0 issues TMA loads into
-// an 8-stage ring (fp8 d = 128 or bf16 d = 64; 4 stages for bf16 d = 128),
-// warp 1 issues tcgen05.mma into two TMEM accumulators, warps 2-5 drain the
-// accumulators, write the score row and (decode) count each score's 12-bit
-// bin for the first radix level of the top-k (topk.cu).
+// Persistent warp-specialised CTAs, two per SM (each pipeline's producer,
+// MMA issuer and epilogue are single threads of control, so two independent
+// pipelines per SM keep more loads in flight than one deeper ring): warp 0
+// issues TMA loads into a 4-stage ring (fp8 d = 128 or bf16 d = 64; 2 stages
+// for bf16 d = 128) plus a ring of key-scale slots, warp 1 issues
+// tcgen05.mma into four TMEM accumulators, warps 2-5 drain the accumulators,
+// write the score row and (decode) count each score's 12-bit bin for the
+// first radix level of the top-k (topk.cu).
 // Every wait is bounded (tc::mbar_wait): a stuck CTA raises
 // DSA_DEVERR_TIMEOUT and winds down instead of hanging.
 #include <algorithm>
@@ -29,13 +32,15 @@ namespace dsa {
 namespace {
 
 constexpr int kTileKeys = 128;
-constexpr int kThreads = 320;     // 10 warps
-constexpr int kEpiThreads = 256;  // warps 2..9: two groups of four, alternate tiles
+constexpr int kGroups = 1;        // epilogue groups of four warps (alternate tiles)
+constexpr int kEpiThreads = 128 * kGroups;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kCtasPerSm = 2;     // two independent pipelines per SM
 constexpr int kHistBinsLocal = kHistBins;
-constexpr int kAcc = 8;           // TMEM accumulators in flight (8 x 64 columns = all of TMEM)
+constexpr int kAcc = 4;           // TMEM accumulators in flight (4 x 64 columns: half of TMEM)
 constexpr int kScBox = 132;       // fp32 scales per tile load: 128 keys + up to 3 lead-in
 constexpr int kScBytes = 640;     // kScBox * 4 rounded up to 128 (TMA destinations are 128-byte aligned)
-constexpr int kScSlots = 16;      // ring of per-tile scale slots, released by the epilogue
+constexpr int kScSlots = 8;       // ring of per-tile scale slots, released by the epilogue
 
 struct IdxSmem {
   // offsets in bytes from the 1024-aligned base
@@ -47,7 +52,7 @@ struct IdxSmem {
 __host__ __device__ inline IdxSmem idx_smem_layout(int N, int kblocks) {
   IdxSmem L;
   L.stage_bytes = kTileKeys * 128 * kblocks;
-  L.stages = kblocks == 1 ? 11 : 5;
+  L.stages = kblocks == 1 ? 4 : 2;
   L.stage0 = 0;
   L.q0 = L.stage0 + L.stage_bytes * L.stages;
   L.q_bytes = N * 128 * kblocks;  // N * 128 is a multiple of 1024 for N >= 8
@@ -81,7 +86,7 @@ __device__ __forceinline__ RowInfo row_info(const IndexScoreArgs &a, int t) {
 }
 
 template <bool FP8, int N, int KB>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap smap, IndexScoreArgs a,
@@ -310,7 +315,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     // wait gave up keeps walking (doing no work) so that no warp is left alone
     // at a named barrier.
     const int et = threadIdx.x - 64;         // 0..255
-    const int group = et >> 7;
+    const int group = kGroups == 1 ? 0 : (et >> 7);
     const int quad = warp & 3;               // TMEM lane quadrant this warp may read
     const int row_in_tile = quad * 32 + lane;
     int cur_t = -1;
@@ -357,7 +362,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         cur_t = t;
       }
       const int64_t my_n = n++;
-      if (dead || (int)(my_n & 1) != group) continue;
+      if (dead || (int)(my_n % kGroups) != group) continue;
       const int acc = (int)(my_n % kAcc);
       const uint32_t acc_phase = (uint32_t)((my_n / kAcc) & 1);
       if (!tc::mbar_wait(&tfull[acc], acc_phase, abort_flag)) { dead = true; continue; }
@@ -423,7 +428,7 @@ cudaError_t launch_tc(const IndexScoreArgs &a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const int64_t tiles_per_row = (a.max_len + kTileKeys - 1) / kTileKeys;
   const int64_t total = (int64_t)a.T * tiles_per_row;
-  const int64_t grid = std::min<int64_t>(num_sms(), total);
+  const int64_t grid = std::min<int64_t>((int64_t)kCtasPerSm * num_sms(), total);
   const int64_t per = (total + grid - 1) / grid;
   const IdxSmem L = idx_smem_layout(N, KB);
   const size_t smem = L.total + 1024;
