@@ -100,9 +100,9 @@ DecodeLayout decode_layout(int B, int64_t max_seq_len, int k, int H, int Dv, int
   DecodeLayout L{};
   WsCarver c(ws);
   L.scores = c.take<float>((size_t)B * scores_ld(max_seq_len));
-  size_t tb = topk_ws_layout(B, k, nullptr, nullptr);
+  size_t tb = topk_ws_layout(B, max_seq_len, k, nullptr, nullptr);
   char *tp = c.take<char>(tb);
-  topk_ws_layout(B, k, tp, &L.topk);
+  topk_ws_layout(B, max_seq_len, k, tp, &L.topk);
   L.idx = c.take<int32_t>((size_t)B * k);
   size_t mb = mla_ws_bytes(B, H, Dv, k + k_swa);
   char *mp = c.take<char>(mb);
@@ -147,9 +147,8 @@ int dsa_index_score(const void *q_idx, int idx_dtype, const float *q_scale, cons
 }
 
 size_t dsa_topk_workspace_size(int T, int64_t max_len, int k) {
-  (void)max_len;
-  if (T <= 0 || k <= 0) return 0;
-  return topk_ws_layout(T, k, nullptr, nullptr);
+  if (T <= 0 || k <= 0 || max_len < 0) return 0;
+  return topk_ws_layout(T, max_len, k, nullptr, nullptr);
 }
 
 int dsa_topk(const float *scores, int64_t ld_scores, const int32_t *row_len, int T,
@@ -163,7 +162,7 @@ int dsa_topk(const float *scores, int64_t ld_scores, const int32_t *row_len, int
   if (ws_bytes < need || (need && !ws)) return DSA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   TopkWs w;
-  topk_ws_layout(T, k, ws, &w);
+  topk_ws_layout(T, max_len, k, ws, &w);
   cudaError_t e = topk_clear(w, T, s);
   if (e == cudaSuccess) e = topk_hist(scores, ld_scores, row_len, T, max_len, k, w, s);
   if (e == cudaSuccess)

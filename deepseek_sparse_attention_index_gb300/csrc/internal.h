@@ -10,15 +10,17 @@ namespace dsa {
 
 // ------------------------------------------------------------------ top-k
 constexpr int kHistBins = 4096;   // first radix level: top 12 bits of the key
-constexpr int kCandCap = 8192;    // candidates per row kept for the resolve pass
+constexpr int kListCap = 8192;    // (key, position) entries per row kept for the resolve pass
+constexpr int kMinChunk = 2048;   // smallest run of positions one collect CTA covers
 
 struct TopkWs {
   uint32_t *hist;    // [T][kHistBins]        zeroed before the histogram pass
-  uint32_t *cnt;     // [T][4] (gt, eq, CTAs done, pad), zeroed before the collect pass
-  int32_t *gt_list;  // [T][k]
-  uint2 *cand;       // [T][kCandCap]  (key, position)
+  uint32_t *cnt;     // [T][4] (list entries, -, CTAs done, -), zeroed before the collect pass
+  uint2 *list;       // [T][kListCap]  (key, position): the row's runs, one per collect CTA
+  uint2 *tab;        // [T][max_chunks] (run start, run length) by chunk
+  int max_chunks;    // ceil(max_len / kMinChunk)
 };
-size_t topk_ws_layout(int T, int k, void *ws, TopkWs *out);  // returns bytes
+size_t topk_ws_layout(int T, int64_t max_len, int k, void *ws, TopkWs *out);  // returns bytes
 
 // Clears hist and cnt (one memset each, stream-ordered).
 cudaError_t topk_clear(const TopkWs &w, int T, cudaStream_t s);

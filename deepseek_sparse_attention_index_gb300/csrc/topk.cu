@@ -10,18 +10,24 @@
 //   1. histogram  -- 4096 bins over the top 12 bits of an order-preserving
 //                    uint32 key of each score (fused into the index-score
 //                    epilogue in the decode path);
-//   2. collect    -- many CTAs per row: find the bin b1 where the count from
-//                    the top first reaches k; append positions in bins above
-//                    b1 (fewer than k of them) to a per-row list and the
-//                    (key, position) pairs of bin b1 to a candidate list;
-//   3. resolve    -- one CTA per row: two more radix levels over the
-//                    candidates (bits 19..8, then 7..0) give the exact k-th
-//                    key K*; a radix select over positions picks the lowest
-//                    positions among the elements equal to K*; the k
-//                    survivors are sorted by position and written out.
-// If a row's candidate list overflows (many near-equal scores), the resolve
-// pass reads that row's scores again instead of the list: slower, same
-// result.
+//   2. collect    -- several CTAs per row, each over one chunk of at most
+//                    16384 positions held in registers: find the bin b1 where
+//                    the count from the top first reaches k, then append the
+//                    (key, position) pair of every element in bin b1 or above
+//                    to the row's list as ONE run in ascending position order
+//                    (one atomic per CTA reserves it) and record the run's
+//                    start and length in the row's chunk table;
+//   3. resolve    -- by the row's last CTA to finish: two more radix levels
+//                    over the list's bin-b1 entries (bits 19..8, then 7..0)
+//                    give the exact k-th key K*; a radix select over
+//                    positions picks the lowest positions among the elements
+//                    equal to K*; an ordered compaction walks the runs in
+//                    chunk order and writes the survivors, which therefore
+//                    come out in ascending position order with no sort.
+// If a row's list overflows (many near-equal scores), the resolve pass reads
+// that row's scores again instead of the list: slower, same result.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -29,8 +35,14 @@ namespace dsa {
 
 namespace {
 
-constexpr int kCollectThreads = 512;
+constexpr int kThreads = 512;               // collect / resolve CTA
+constexpr int kPer = 16;                    // positions a thread holds per round
+constexpr int kRound = kPer * kThreads;     // 8192 positions per round
+constexpr int kRounds = 2;                  // a chunk is one or two rounds
+constexpr int kMaxChunk = kRound * kRounds; // 16384
+constexpr int kGather = 8;                  // entries per thread per compaction round
 constexpr int kHistThreads = 512;
+static_assert(kHistBins == 8 * kThreads, "threshold_bin gives each thread 8 bins");
 
 // Exclusive prefix sum over the block (blockDim.x a multiple of 32, <= 1024).
 // Returns this thread's exclusive prefix; *total gets the block sum.
@@ -93,6 +105,33 @@ __device__ void find_bin(const uint32_t *h, int nbins, uint32_t need, bool desce
 }
 
 
+
+// The first-level threshold straight from a row's histogram in global
+// memory: the bin where the count from the top first reaches `need`, and the
+// count above it.  Thread i owns bins [4088 - 8i, 4096 - 8i) (descending
+// walk positions 8i .. 8i + 7), read with two 16-byte loads.  blockDim.x must
+// be kThreads; the histogram must be 16-byte aligned.
+__device__ void threshold_bin(const uint32_t *gh, uint32_t need, uint32_t *warp_sums,
+                              int *bin_out, uint32_t *before_out) {
+  const uint4 *p = reinterpret_cast<const uint4 *>(gh + (kHistBins - 8) - 8 * threadIdx.x);
+  const uint4 lo = __ldcg(p), hi = __ldcg(p + 1);
+  const uint32_t h[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};
+  uint32_t sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) sum += h[j];
+  uint32_t tot;
+  uint32_t cum = block_excl_scan(sum, warp_sums, &tot);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (cum < need && cum + h[j] >= need) {
+      *bin_out = kHistBins - 1 - 8 * (int)threadIdx.x - j;
+      *before_out = cum;
+    }
+    cum += h[j];
+  }
+  __syncthreads();
+}
+
 // Loads this thread's 16 elements of the chunk window starting at `base`:
 // element (r, c) is position base + 4 * (r * blockDim.x + threadIdx.x) + c.
 // Four float4 loads in flight at once when the row is 16-byte aligned, else
@@ -143,116 +182,98 @@ topk_hist_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__
     if (sh[i]) atomicAdd(&gh[i], sh[i]);
 }
 
-// Source of (key, position) pairs for the resolve passes: the candidate list,
-// or -- after an overflow -- the row itself filtered to bin b1.
+
+// Where the resolve pass reads a row's (key, position) pairs: the list (the
+// entries at or above bin b1, in runs by chunk) or -- after an overflow --
+// the row itself.  Other CTAs wrote the list, so it is read through L2.
 struct Source {
-  const uint2 *cand;
+  const uint2 *list;
   const float *row;
   int64_t n;        // list length, or the row length when reading the row
   bool from_row;
-  uint32_t b1;
-  __device__ bool get(int64_t i, uint32_t &key, int32_t &pos) const {
+  __device__ __forceinline__ void get(int64_t i, uint32_t &key, int32_t &pos) const {
     if (!from_row) {
-      uint2 c = cand[i];
+      const uint2 c = __ldcg(list + i);
       key = c.x;
       pos = (int32_t)c.y;
-      return true;
+    } else {
+      key = score_key(__ldcg(row + i));
+      pos = (int32_t)i;
     }
-    key = score_key(row[i]);
-    pos = (int32_t)i;
-    return (key >> 20) == b1;
   }
 };
 
-// Resolves row t once its collect pass is complete: two more radix levels
-// over the candidates give the exact k-th key, a radix select over positions
-// breaks ties toward lower positions, and the k survivors are sorted by
-// position.  Run by one whole CTA (blockDim.x a multiple of 32 dividing 512).
 struct ResolveSmem {
   uint32_t sh[kHistBins];
-  int32_t sel[DSA_MAX_TOPK];
+  uint32_t run_pre[kThreads];    // ordered start of each run of a group of chunks
+  uint32_t run_at[kThreads];     // where that run sits in the list
   uint32_t warp_sums[32];
   int s_bin;
   uint32_t s_before;
-  uint32_t s_fill;
 };
 
-__device__ __noinline__ void resolve_row(int t, ResolveSmem &S, const float *__restrict__ scores, int64_t ld,
-                            const int32_t *__restrict__ row_len, int k,
-                            const int32_t *__restrict__ index_base,
-                            const uint32_t *__restrict__ hist, const uint32_t *__restrict__ cnt,
-                            const int32_t *__restrict__ gt_list, const uint2 *__restrict__ cand,
-                            int32_t *__restrict__ idx, int32_t *__restrict__ lens,
-                            int32_t *err_flag) {
+// Resolves row t once its collect pass is complete (b1 and n_gt = the count
+// above bin b1 come from the caller's threshold_bin): two more radix levels
+// over the bin-b1 entries give the exact k-th key K*, a radix select over
+// positions breaks ties toward lower positions, and an ordered compaction
+// writes the k survivors in ascending position order.  Run by one whole CTA
+// of kThreads threads.
+__device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uint32_t n_gt,
+                                         const float *__restrict__ scores, int64_t ld, int64_t L,
+                                         int k, int chunk, int max_chunks,
+                                         const int32_t *__restrict__ index_base,
+                                         const uint32_t *__restrict__ cnt,
+                                         const uint2 *__restrict__ list,
+                                         const uint2 *__restrict__ tab, int32_t *__restrict__ idx,
+                                         int32_t *__restrict__ lens, int32_t *err_flag) {
   uint32_t *sh = S.sh;
-  int32_t *sel = S.sel;
-  uint32_t *warp_sums = S.warp_sums;
-  int &s_bin = S.s_bin;
-  uint32_t &s_before = S.s_before;
-  uint32_t &s_fill = S.s_fill;
-  const int64_t L = max(row_len[t], 0);
   const int32_t base = index_base ? index_base[t] : 0;
   int32_t *out = idx + (size_t)t * k;
-  if (L <= k) {
-    for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < L ? (int32_t)j + base : -1;
-    if (lens && threadIdx.x == 0) lens[t] = (int32_t)L;
-    return;
-  }
-  // level 1 again: the bin b1 and the count above it
-  const uint32_t *gh = hist + (size_t)t * kHistBins;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = gh[i];
-  if (threadIdx.x == 0) { s_bin = 0; s_before = 0; }
-  __syncthreads();
-  find_bin(sh, kHistBins, (uint32_t)k, true, warp_sums, &s_bin, &s_before);
-  const uint32_t b1 = (uint32_t)s_bin;
-  const uint32_t n_gt = cnt[4 * t];
-  const uint32_t n_eq = cnt[4 * t + 1];
-  if (n_gt != s_before || n_gt >= (uint32_t)k) {
-    // histogram and collect pass disagree: only NaN scores can do this
+  const uint32_t n_list = __ldcg(cnt + 4 * t);   // entries at or above bin b1
+  if (n_gt >= (uint32_t)k || n_list < (uint32_t)k) {
+    // histogram and scores disagree (a histogram of other scores, or NaNs)
     if (threadIdx.x == 0) raise_flag(err_flag, DSA_DEVERR_INDEX_RANGE);
     for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
     if (lens && threadIdx.x == 0) lens[t] = 0;
     return;
   }
   Source src;
-  src.cand = cand + (size_t)t * kCandCap;
+  src.list = list + (size_t)t * kListCap;
   src.row = scores + (int64_t)t * ld;
-  src.from_row = n_eq > (uint32_t)kCandCap;
-  src.n = src.from_row ? L : (int64_t)n_eq;
-  src.b1 = b1;
+  src.from_row = n_list > (uint32_t)kListCap;
+  src.n = src.from_row ? L : (int64_t)n_list;
   const uint32_t r1 = (uint32_t)k - n_gt;  // to take from bin b1
 
-  // level 2: bits 19..8
-  __syncthreads();
+  // level 2: bits 19..8 of the bin-b1 keys
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
   __syncthreads();
   for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
     uint32_t key; int32_t pos;
-    if (src.get(i, key, pos)) atomicAdd(&sh[(key >> 8) & 0xFFFu], 1u);
+    src.get(i, key, pos);
+    if ((key >> 20) == b1) atomicAdd(&sh[(key >> 8) & 0xFFFu], 1u);
   }
   __syncthreads();
-  find_bin(sh, kHistBins, r1, true, warp_sums, &s_bin, &s_before);
-  const uint32_t b2 = (uint32_t)s_bin;
-  const uint32_t r2 = r1 - s_before;
+  find_bin(sh, kHistBins, r1, true, S.warp_sums, &S.s_bin, &S.s_before);
+  const uint32_t b2 = (uint32_t)S.s_bin;
+  const uint32_t r2 = r1 - S.s_before;
+  const uint32_t hi20 = (b1 << 12) | b2;   // bits 31..8 of K*
 
-  // level 3: bits 7..0 among keys whose bits 19..8 are b2
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) sh[i] = 0;
+  // level 3: bits 7..0 among keys whose bits 31..8 are hi20
+  for (int i = threadIdx.x; i < kThreads; i += blockDim.x) sh[i] = 0;
   __syncthreads();
   for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
     uint32_t key; int32_t pos;
-    if (src.get(i, key, pos) && ((key >> 8) & 0xFFFu) == b2) atomicAdd(&sh[key & 0xFFu], 1u);
+    src.get(i, key, pos);
+    if ((key >> 8) == hi20) atomicAdd(&sh[key & 0xFFu], 1u);
   }
   __syncthreads();
-  // 256 bins padded with zero bins to a multiple of the block size
-  const int nb3 = max(256, (int)blockDim.x);
-  for (int i = 256 + threadIdx.x; i < nb3; i += blockDim.x) sh[i] = 0;
-  __syncthreads();
-  // the zero bins sit above bin 255; walking down from the top passes them first
-  find_bin(sh, nb3, r2, true, warp_sums, &s_bin, &s_before);
-  const uint32_t b3 = (uint32_t)s_bin;
-  const uint32_t r3 = r2 - s_before;  // how many elements equal to K* to keep
-  const uint32_t m_eq = sh[b3];       // how many elements equal K*
-  const uint32_t kstar = (b1 << 20) | (b2 << 8) | b3;
+  // 256 bins padded with zero bins to the block size; walking down from the
+  // top passes the zero bins first
+  find_bin(sh, kThreads, r2, true, S.warp_sums, &S.s_bin, &S.s_before);
+  const uint32_t b3 = (uint32_t)S.s_bin;
+  const uint32_t r3 = r2 - S.s_before;   // how many elements equal to K* to keep
+  const uint32_t m_eq = sh[b3];          // how many elements equal K*
+  const uint32_t kstar = (hi20 << 8) | b3;
 
   // positions among the elements equal to K*: keep the r3 lowest
   int32_t pstar = 0x7fffffff;
@@ -269,7 +290,8 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, const float *__r
       __syncthreads();
       for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
         uint32_t key; int32_t pos;
-        if (src.get(i, key, pos) && key == kstar) {
+        src.get(i, key, pos);
+        if (key == kstar) {
           const uint32_t p = (uint32_t)pos;
           const uint32_t hi_bits = lvl == 0 ? 0u : (p >> (sft + widths[lvl]));
           if (hi_bits == prefix) atomicAdd(&sh[(p >> sft) & (nb - 1)], 1u);
@@ -278,63 +300,111 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, const float *__r
       __syncthreads();
       // ascending walk over max(nb, blockDim) bins (extra bins are zero)
       const int nbins = (int)max(nb, (uint32_t)blockDim.x);
-      find_bin(sh, nbins, need, false, warp_sums, &s_bin, &s_before);
-      need -= s_before;
-      prefix = (prefix << widths[lvl]) | (uint32_t)s_bin;
+      find_bin(sh, nbins, need, false, S.warp_sums, &S.s_bin, &S.s_before);
+      need -= S.s_before;
+      prefix = (prefix << widths[lvl]) | (uint32_t)S.s_bin;
     }
     pstar = (int32_t)prefix;
   }
 
-  // gather the survivors
-  if (threadIdx.x == 0) s_fill = n_gt;
-  const int32_t *gl = gt_list + (size_t)t * k;
-  for (int j = threadIdx.x; j < (int)n_gt; j += blockDim.x) sel[j] = gl[j];
-  __syncthreads();
-  for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
-    uint32_t key; int32_t pos;
-    if (src.get(i, key, pos) && (key > kstar || (key == kstar && pos <= pstar))) {
-      uint32_t slot = atomicAdd(&s_fill, 1u);
-      if (slot < (uint32_t)k) sel[slot] = pos;
-    }
-  }
-  __syncthreads();
-  if (s_fill != (uint32_t)k && threadIdx.x == 0) raise_flag(err_flag, DSA_DEVERR_INDEX_RANGE);
-  // bitonic sort of sel[0..kp) ascending, kp = next power of two >= k
-  int kp = 1;
-  while (kp < k) kp <<= 1;
-  for (int j = k + threadIdx.x; j < kp; j += blockDim.x) sel[j] = 0x7fffffff;
-  __syncthreads();
-  for (int size = 2; size <= kp; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (kp >> 1); i += blockDim.x) {
-        const int lo_i = 2 * i - (i & (stride - 1));
-        const int hi_i = lo_i + stride;
-        const bool up = (lo_i & size) == 0;
-        const int32_t a = sel[lo_i], b = sel[hi_i];
-        if ((a > b) == up) { sel[lo_i] = b; sel[hi_i] = a; }
+  // ordered compaction of the survivors: key > K*, or key == K* at a
+  // position <= pstar.  A thread takes kGather consecutive entries of the
+  // ordered sequence per round; a block scan of its survivor count gives
+  // where they go.
+  uint32_t written = 0;
+  if (src.from_row) {
+    for (int64_t r0 = 0; r0 < L; r0 += (int64_t)kGather * kThreads) {
+      const int64_t p0 = r0 + (int64_t)kGather * threadIdx.x;
+      uint32_t m = 0;
+#pragma unroll
+      for (int j = 0; j < kGather; ++j) {
+        if (p0 + j < L) {
+          const uint32_t key = score_key(__ldcg(src.row + p0 + j));
+          if (key > kstar || (key == kstar && (int32_t)(p0 + j) <= pstar)) m |= 1u << j;
+        }
       }
+      uint32_t tot;
+      uint32_t o = written + block_excl_scan((uint32_t)__popc(m), S.warp_sums, &tot);
+#pragma unroll
+      for (int j = 0; j < kGather; ++j)
+        if ((m >> j) & 1u) {
+          if (o < (uint32_t)k) out[o] = (int32_t)(p0 + j) + base;
+          ++o;
+        }
+      written += tot;
+    }
+  } else {
+    const int nch = (int)((L + chunk - 1) / chunk);
+    const uint2 *rt = tab + (size_t)t * max_chunks;
+    for (int g0 = 0; g0 < nch; g0 += kThreads) {
+      // the runs of chunks g0 .. g0 + ng - 1, their ordered starts by a block scan
+      const int ng = min(kThreads, nch - g0);
+      uint2 run = make_uint2(0u, 0u);
+      if ((int)threadIdx.x < ng) run = __ldcg(rt + g0 + threadIdx.x);
+      uint32_t n_group;
+      const uint32_t pre = block_excl_scan(run.y, S.warp_sums, &n_group);
+      S.run_pre[threadIdx.x] = pre;
+      S.run_at[threadIdx.x] = run.x;
       __syncthreads();
+      for (uint32_t r0 = 0; r0 < n_group; r0 += (uint32_t)kGather * kThreads) {
+        const uint32_t l0 = r0 + (uint32_t)kGather * threadIdx.x;
+        uint32_t m = 0;
+        int32_t posv[kGather];
+        if (l0 < n_group) {
+          // the last run starting at or before l0 (runs are non-empty there)
+          int lo = 0, hi = ng;
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (S.run_pre[mid] <= l0) lo = mid; else hi = mid;
+          }
+          int c = lo;
+#pragma unroll
+          for (int j = 0; j < kGather; ++j) {
+            const uint32_t l = l0 + j;
+            posv[j] = 0;
+            if (l < n_group) {
+              while (c + 1 < ng && S.run_pre[c + 1] <= l) ++c;
+              const uint2 e = __ldcg(src.list + S.run_at[c] + (l - S.run_pre[c]));
+              posv[j] = (int32_t)e.y;
+              if (e.x > kstar || (e.x == kstar && (int32_t)e.y <= pstar)) m |= 1u << j;
+            }
+          }
+        }
+        uint32_t tot;
+        uint32_t o = written + block_excl_scan((uint32_t)__popc(m), S.warp_sums, &tot);
+#pragma unroll
+        for (int j = 0; j < kGather; ++j)
+          if ((m >> j) & 1u) {
+            if (o < (uint32_t)k) out[o] = posv[j] + base;
+            ++o;
+          }
+        written += tot;
+      }
+      __syncthreads();   // run_pre / run_at are rewritten by the next group
     }
   }
-  for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = sel[j] + base;
-  if (lens && threadIdx.x == 0) lens[t] = k;
+  if (threadIdx.x == 0) {
+    if (written != (uint32_t)k) raise_flag(err_flag, DSA_DEVERR_INDEX_RANGE);
+    if (lens) lens[t] = k;
+  }
 }
 
 // Collect pass, and the resolve of each row by the last of its CTAs to finish
 // (every CTA fences its writes and bumps the row's done counter; the CTA that
 // sees the count complete resolves the row -- nobody waits on anybody).
-// Each CTA appends its "above the threshold bin" positions and its
-// "in the threshold bin" candidates with one atomic per list: per-thread
-// counts go through a block scan, thread 0 reserves the CTA's range.
-__global__ void __launch_bounds__(kCollectThreads, 2)
+// CTA (x, t) covers positions [x * chunk, (x + 1) * chunk) of row t, chunk <=
+// kMaxChunk: thread i holds positions x * chunk + r * kRound + 16 i + e
+// (round r < 2, e < 16), so the order (r, i, e) is position order and a
+// packed two-round block scan places every entry of the CTA's run.
+__global__ void __launch_bounds__(kThreads, 2)
 topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
-                    const int32_t *__restrict__ row_len, int k, int chunk,
+                    const int32_t *__restrict__ row_len, int k, int chunk, int max_chunks,
                     const int32_t *__restrict__ index_base, const uint32_t *__restrict__ hist,
-                    uint32_t *__restrict__ cnt, int32_t *__restrict__ gt_list,
-                    uint2 *__restrict__ cand, int32_t *__restrict__ idx,
+                    uint32_t *__restrict__ cnt, uint2 *__restrict__ list,
+                    uint2 *__restrict__ tab, int32_t *__restrict__ idx,
                     int32_t *__restrict__ lens, int32_t *err_flag) {
   __shared__ ResolveSmem S;
-  __shared__ uint32_t s_base_gt, s_base_eq;
+  __shared__ uint32_t s_base;
   __shared__ int s_last;
   const int t = blockIdx.y;
   const int64_t L = max(row_len[t], 0);
@@ -352,84 +422,106 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
   const int64_t hi = min(L, lo + chunk);
   const float *row = scores + (int64_t)t * ld;
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
-  Elems16 E;
-  load16(row, lo, hi, vec, E);   // first window in flight while the threshold is found
-  const uint32_t *gh = hist + (size_t)t * kHistBins;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) S.sh[i] = gh[i];
+
+  // this thread's scores, loads in flight while the threshold is found
+  uint32_t v[kRounds][kPer];
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int64_t p = lo + (int64_t)r * kRound + kPer * threadIdx.x;
+    if (vec && p + kPer <= hi) {
+      const float4 *q = reinterpret_cast<const float4 *>(row + p);
+#pragma unroll
+      for (int c = 0; c < kPer / 4; ++c) {
+        const float4 f = __ldcg(q + c);
+        v[r][4 * c] = __float_as_uint(f.x);
+        v[r][4 * c + 1] = __float_as_uint(f.y);
+        v[r][4 * c + 2] = __float_as_uint(f.z);
+        v[r][4 * c + 3] = __float_as_uint(f.w);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) v[r][e] = p + e < hi ? __float_as_uint(__ldcg(row + p + e)) : 0u;
+    }
+  }
   if (threadIdx.x == 0) { S.s_bin = 0; S.s_before = 0; }
   __syncthreads();
-  find_bin(S.sh, kHistBins, (uint32_t)k, true, S.warp_sums, &S.s_bin, &S.s_before);
+  threshold_bin(hist + (size_t)t * kHistBins, (uint32_t)k, S.warp_sums, &S.s_bin, &S.s_before);
   const uint32_t b1 = (uint32_t)S.s_bin;
-  uint32_t *c_gt = cnt + 4 * t;
-  uint32_t *c_eq = c_gt + 1;
-  uint32_t *c_done = c_gt + 2;
-  int32_t *gl = gt_list + (size_t)t * k;
-  uint2 *cl = cand + (size_t)t * kCandCap;
-  for (int64_t base = lo; base < hi; base += 16 * (int64_t)blockDim.x) {
-    if (base != lo) load16(row, base, hi, vec, E);
-    uint32_t mgt = 0, meq = 0;
+  const uint32_t n_gt = S.s_before;
+
+  // entries at or above bin b1, counted per round (packed: a round holds at
+  // most 8192 of them, so the two 16-bit halves of the scan never carry)
+  uint32_t m[kRounds];
+  uint32_t packed = 0;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const bool valid = E.p0[e >> 2] + (e & 3) < hi;
-      const uint32_t bin = score_key(E.v[e]) >> 20;
-      mgt |= (valid && bin > b1) ? (1u << e) : 0u;
-      meq |= (valid && bin == b1) ? (1u << e) : 0u;
-    }
-    // counts packed (gt << 16 | eq): a CTA round holds at most 16 * 1024 elements
-    uint32_t tot;
-    const uint32_t pre = block_excl_scan(((uint32_t)__popc(mgt) << 16) | (uint32_t)__popc(meq),
-                                         S.warp_sums, &tot);
-    if (threadIdx.x == 0) {
-      s_base_gt = (tot >> 16) ? atomicAdd(c_gt, tot >> 16) : 0u;
-      s_base_eq = (tot & 0xffffu) ? atomicAdd(c_eq, tot & 0xffffu) : 0u;
-    }
-    __syncthreads();
-    uint32_t og = s_base_gt + (pre >> 16), oe = s_base_eq + (pre & 0xffffu);
+  for (int r = 0; r < kRounds; ++r) {
+    const int64_t p = lo + (int64_t)r * kRound + kPer * threadIdx.x;
+    m[r] = 0;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int64_t i = E.p0[e >> 2] + (e & 3);
-      if ((mgt >> e) & 1u) {
-        if (og < (uint32_t)k) gl[og] = (int32_t)i;
-        ++og;
-      }
-      if ((meq >> e) & 1u) {
-        if (oe < (uint32_t)kCandCap) cl[oe] = make_uint2(score_key(E.v[e]), (uint32_t)i);
-        ++oe;
-      }
+    for (int e = 0; e < kPer; ++e) {
+      const uint32_t key = score_key(__uint_as_float(v[r][e]));
+      v[r][e] = key;
+      if (p + e < hi && (key >> 20) >= b1) m[r] |= 1u << e;
     }
-    __syncthreads();   // s_base_* are reused by the next round
+    packed += (uint32_t)__popc(m[r]) << (16 * r);
   }
-  // publish this CTA's appends; the last CTA of the row resolves it
+  uint32_t tot;
+  const uint32_t pre = block_excl_scan(packed, S.warp_sums, &tot);
+  const uint32_t tot0 = tot & 0xffffu;
+  if (threadIdx.x == 0) {
+    const uint32_t n = tot0 + (tot >> 16);
+    s_base = n ? atomicAdd(&cnt[4 * t], n) : 0u;
+    tab[(size_t)t * max_chunks + blockIdx.x] = make_uint2(s_base, n);
+  }
+  __syncthreads();
+  uint2 *cl = list + (size_t)t * kListCap;
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int64_t p = lo + (int64_t)r * kRound + kPer * threadIdx.x;
+    uint32_t o = s_base + (r == 0 ? (pre & 0xffffu) : tot0 + (pre >> 16));
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      if ((m[r] >> e) & 1u) {
+        if (o < (uint32_t)kListCap) cl[o] = make_uint2(v[r][e], (uint32_t)(p + e));
+        ++o;
+      }
+  }
+
+  // publish this CTA's run; the last CTA of the row resolves it
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const uint32_t nch = (uint32_t)((L + chunk - 1) / chunk);
-    s_last = atomicAdd(c_done, 1u) == nch - 1;
+    s_last = atomicAdd(&cnt[4 * t + 2], 1u) == nch - 1;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  resolve_row(t, S, scores, ld, row_len, k, index_base, hist, cnt, gt_list, cand, idx, lens,
-              err_flag);
+  resolve_row(t, S, b1, n_gt, scores, ld, L, k, chunk, max_chunks, index_base, cnt, list, tab, idx,
+              lens, err_flag);
 }
 
+// Positions per collect CTA: the smallest power of two in [kMinChunk,
+// kMaxChunk] whose grid fits in one wave (two CTAs per SM); kMaxChunk when
+// none does.
 int collect_chunk(int T, int64_t max_len) {
-  // enough CTAs to cover the GPU about twice, 2k..16k positions each
-  int64_t target = 2LL * num_sms();
-  int64_t chunk = 16384;
-  while (chunk > 2048 && (int64_t)T * ((max_len + chunk - 1) / chunk) < target) chunk >>= 1;
+  const int64_t wave = 2LL * num_sms();
+  int64_t chunk = kMinChunk;
+  while (chunk < kMaxChunk && (int64_t)T * ((max_len + chunk - 1) / chunk) > wave) chunk <<= 1;
   return (int)chunk;
 }
 
 }  // namespace
 
-size_t topk_ws_layout(int T, int k, void *ws, TopkWs *out) {
+size_t topk_ws_layout(int T, int64_t max_len, int k, void *ws, TopkWs *out) {
+  (void)k;
   WsCarver c(ws);
   TopkWs w;
+  w.max_chunks = (int)std::max<int64_t>(1, (max_len + kMinChunk - 1) / kMinChunk);
   w.hist = c.take<uint32_t>((size_t)T * kHistBins);
-  w.cnt = c.take<uint32_t>((size_t)T * 4);   // gt, eq, CTAs done, pad
-  w.gt_list = c.take<int32_t>((size_t)T * k);
-  w.cand = c.take<uint2>((size_t)T * kCandCap);
+  w.cnt = c.take<uint32_t>((size_t)T * 4);   // list entries, -, CTAs done, -
+  w.list = c.take<uint2>((size_t)T * kListCap);
+  w.tab = c.take<uint2>((size_t)T * w.max_chunks);
   if (out) *out = w;
   return c.bytes();
 }
@@ -454,10 +546,11 @@ cudaError_t topk_select(const float *scores, int64_t ld, const int32_t *row_len,
                         int32_t *lens, const TopkWs &w, int32_t *err_flag, cudaStream_t s) {
   const int chunk = collect_chunk(T, max_len);
   const int64_t nch = max_len > k ? (max_len + chunk - 1) / chunk : 1;
+  if (nch > w.max_chunks) return cudaErrorInvalidValue;
   dim3 grid((unsigned)nch, (unsigned)T);
-  topk_collect_kernel<<<grid, kCollectThreads, 0, s>>>(scores, ld, row_len, k, chunk, index_base,
-                                                        w.hist, w.cnt, w.gt_list, w.cand, idx,
-                                                        lens, err_flag);
+  topk_collect_kernel<<<grid, kThreads, 0, s>>>(scores, ld, row_len, k, chunk, w.max_chunks,
+                                                index_base, w.hist, w.cnt, w.list, w.tab, idx,
+                                                lens, err_flag);
   return cudaGetLastError();
 }
 

@@ -61,14 +61,14 @@ extern "C" int dsa_topk_noalloc(const float *scores, int64_t ld_scores, const in
   if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
   if (T == 0) return DSA_OK;
   if (!scores || !row_len || !idx) return DSA_ERR_INVALID_ARG;
-  if (topk_ws_layout(T, k, nullptr, nullptr) > kTopkNoAllocScratchBytes)
+  if (topk_ws_layout(T, max_len, k, nullptr, nullptr) > kTopkNoAllocScratchBytes)
     return DSA_ERR_UNSUPPORTED;  // more rows than the static scratch holds
   cudaError_t e;
   void *scratch = scratch_address(&e);
   if (!scratch) return DSA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   TopkWs w;
-  topk_ws_layout(T, k, scratch, &w);
+  topk_ws_layout(T, max_len, k, scratch, &w);
   e = topk_clear(w, T, s);  // the histogram and counters must start at zero
   if (e == cudaSuccess) e = topk_hist(scores, ld_scores, row_len, T, max_len, k, w, s);
   if (e == cudaSuccess)

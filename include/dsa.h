@@ -164,8 +164,8 @@ int dsa_topk(const float *scores, int64_t ld_scores, const int32_t *row_len, int
  * scratch memory is a static device array of DSA_TOPK_NOALLOC_SCRATCH_BYTES
  * (4 MiB) that every GPU loading the library holds until the process exits.
  * Limit: the scratch of T rows must fit, i.e. dsa_topk_workspace_size(T,
- * max_len, k) <= 4 MiB (up to 46 rows at k = 2048); larger calls return
- * DSA_ERR_UNSUPPORTED without launching anything.
+ * max_len, k) <= 4 MiB (about 80 KiB a row: up to 50 rows of 128K scores);
+ * larger calls return DSA_ERR_UNSUPPORTED without launching anything.
  * The first call on a device looks up the array's device address (with that
  * device current), so make that first call before any stream capture.  All
  * calls share the array and it keeps the last call's contents; each call

@@ -141,6 +141,21 @@ def test_topk_random_fp32_many_rows():
         assert np.array_equal(idx[t, :n], np.sort(ref[:n]))
 
 
+@pytest.mark.parametrize("k", [100, 2048])
+def test_topk_long_rows_many_chunks(k):
+    # rows of 8.4M-9M scores: more than 512 collect chunks each, so the ordered
+    # compaction walks the chunk table in several groups; scores on a 1/64 grid
+    # tie at the threshold, so the position radix runs too
+    rng = np.random.default_rng(100 + k)
+    rows = [(np.round(rng.standard_normal(L) * 64) / 64).astype(np.float32)
+            for L in (9_000_001, 8_400_000)]
+    idx, lens = _run_topk(rows, k)
+    for t, r in enumerate(rows):
+        ref = O.topk_row(r.astype(np.float64), k)
+        assert lens[t] == k
+        assert np.array_equal(idx[t], np.sort(ref[:k])), t
+
+
 # ---------------------------------------------------------------- sparse MLA
 
 def _mla_case(fmt, T, H, k, neg=0.1, seed=0, rows=4096, all_neg_row=True):
