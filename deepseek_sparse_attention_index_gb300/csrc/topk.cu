@@ -41,6 +41,8 @@ constexpr int kRound = kPer * kThreads;     // 8192 positions per round
 constexpr int kRounds = 2;                  // a chunk is one or two rounds
 constexpr int kMaxChunk = kRound * kRounds; // 16384
 constexpr int kGather = 8;                  // entries per thread per compaction round
+constexpr int kBatch = 8;                   // list entries a thread loads at once
+constexpr int kEqCache = 3072;              // bin-b1 entries the resolve keeps in shared memory (static smem < 48 KB)
 constexpr int kHistThreads = 512;
 static_assert(kHistBins == 8 * kThreads, "threshold_bin gives each thread 8 bins");
 
@@ -77,45 +79,90 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_sums, uint32_t *t
 // Over a histogram h[0..nbins) in shared memory, find the bin where the
 // cumulative count first reaches `need`, walking from the highest bin down
 // (descending = true) or from bin 0 up.  *bin_out / *before_out (shared)
-// receive that bin and the count strictly before it in walk order.
-// nbins must be a multiple of blockDim.x.
+// receive that bin and the count strictly before it in walk order; they are
+// left alone when the total stays below `need`.  Warp w owns the walk
+// positions [w * seg, (w + 1) * seg), seg = nbins / warps (a multiple of 32);
+// consecutive lanes read consecutive bins (no bank conflicts), a scan over
+// the warp totals picks the crossing warp, and that warp alone walks its
+// segment 32 bins at a time.
 __device__ void find_bin(const uint32_t *h, int nbins, uint32_t need, bool descending,
                          uint32_t *warp_sums, int *bin_out, uint32_t *before_out) {
-  const int per = nbins / blockDim.x;
-  // thread i owns walk positions [i*per, (i+1)*per)
-  uint32_t sum = 0;
-  for (int j = 0; j < per; ++j) {
-    int wpos = threadIdx.x * per + j;
-    int b = descending ? nbins - 1 - wpos : wpos;
-    sum += h[b];
+  const int nw = blockDim.x >> 5;
+  const int w = threadIdx.x >> 5;
+  const unsigned lane = lane_id();
+  const int seg = nbins / nw;
+  uint32_t s = 0;
+  for (int j = lane; j < seg; j += 32) {
+    const int wpos = w * seg + j;
+    s += h[descending ? nbins - 1 - wpos : wpos];
   }
-  uint32_t tot;
-  uint32_t cum = block_excl_scan(sum, warp_sums, &tot);
-  for (int j = 0; j < per; ++j) {
-    int wpos = threadIdx.x * per + j;
-    int b = descending ? nbins - 1 - wpos : wpos;
-    uint32_t c = h[b];
-    if (cum < need && cum + c >= need) {
-      *bin_out = b;
-      *before_out = cum;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) warp_sums[w] = s;
+  __syncthreads();
+  if (w == 0) {
+    const uint32_t v = lane < (unsigned)nw ? warp_sums[lane] : 0u;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= (unsigned)o) incl += y;
     }
-    cum += c;
+    const uint32_t excl = incl - v;
+    const unsigned ball = __ballot_sync(0xffffffffu, excl < need && incl >= need);
+    const int cw = ball ? __ffs(ball) - 1 : -1;
+    const uint32_t cb = __shfl_sync(0xffffffffu, excl, cw < 0 ? 0 : cw);
+    __syncwarp();
+    if (lane == 0) {
+      warp_sums[0] = (uint32_t)cw;
+      warp_sums[1] = cb;
+    }
+  }
+  __syncthreads();
+  const int cw = (int)warp_sums[0];
+  if (w == cw) {
+    uint32_t before = warp_sums[1];
+    for (int j0 = 0; j0 < seg; j0 += 32) {
+      const int wpos = w * seg + j0 + (int)lane;
+      const int b = descending ? nbins - 1 - wpos : wpos;
+      const uint32_t c = h[b];
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= (unsigned)o) incl += y;
+      }
+      const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+      if (before + tot >= need) {
+        const unsigned ball = __ballot_sync(0xffffffffu, before + incl >= need);
+        if (lane == (unsigned)(__ffs(ball) - 1)) {
+          *bin_out = b;
+          *before_out = before + incl - c;
+        }
+        break;
+      }
+      before += tot;
+    }
   }
   __syncthreads();
 }
 
-
-
 // The first-level threshold straight from a row's histogram in global
 // memory: the bin where the count from the top first reaches `need`, and the
 // count above it.  Thread i owns bins [4088 - 8i, 4096 - 8i) (descending
-// walk positions 8i .. 8i + 7), read with two 16-byte loads.  blockDim.x must
-// be kThreads; the histogram must be 16-byte aligned.
-__device__ void threshold_bin(const uint32_t *gh, uint32_t need, uint32_t *warp_sums,
-                              int *bin_out, uint32_t *before_out) {
+// walk positions 8i .. 8i + 7), read with two 16-byte loads that the caller
+// issues early (hist_load) and hands to the scan (threshold_bin).
+// blockDim.x must be kThreads; the histogram must be 16-byte aligned.
+struct HistSlice {
+  uint4 lo, hi;
+};
+__device__ __forceinline__ HistSlice hist_load(const uint32_t *gh) {
   const uint4 *p = reinterpret_cast<const uint4 *>(gh + (kHistBins - 8) - 8 * threadIdx.x);
-  const uint4 lo = __ldcg(p), hi = __ldcg(p + 1);
-  const uint32_t h[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};
+  return HistSlice{__ldcg(p), __ldcg(p + 1)};
+}
+__device__ void threshold_bin(const HistSlice &hs, uint32_t need, uint32_t *warp_sums,
+                              int *bin_out, uint32_t *before_out) {
+  const uint32_t h[8] = {hs.hi.w, hs.hi.z, hs.hi.y, hs.hi.x, hs.lo.w, hs.lo.z, hs.lo.y, hs.lo.x};
   uint32_t sum = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) sum += h[j];
@@ -207,6 +254,8 @@ struct ResolveSmem {
   uint32_t sh[kHistBins];
   uint32_t run_pre[kThreads];    // ordered start of each run of a group of chunks
   uint32_t run_at[kThreads];     // where that run sits in the list
+  uint2 eq[kEqCache];            // the bin-b1 (key, position) pairs, when they fit
+  uint32_t n_eq;
   uint32_t warp_sums[32];
   int s_bin;
   uint32_t s_before;
@@ -244,15 +293,65 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
   src.n = src.from_row ? L : (int64_t)n_list;
   const uint32_t r1 = (uint32_t)k - n_gt;  // to take from bin b1
 
-  // level 2: bits 19..8 of the bin-b1 keys
+  // level 2: bits 19..8 of the bin-b1 keys.  The same pass keeps the bin-b1
+  // pairs in shared memory (a warp reserves its slots with one atomic), so
+  // the later passes read the list again only when they do not fit.
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
+  if (threadIdx.x == 0) S.n_eq = 0;
   __syncthreads();
-  for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
-    uint32_t key; int32_t pos;
-    src.get(i, key, pos);
-    if ((key >> 20) == b1) atomicAdd(&sh[(key >> 8) & 0xFFFu], 1u);
+  const unsigned lane = lane_id();
+  for (int64_t i0 = 0; i0 < src.n; i0 += (int64_t)kBatch * kThreads) {
+    uint32_t key[kBatch];
+    int32_t pos[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t i = i0 + (int64_t)j * kThreads + threadIdx.x;
+      key[j] = 0;
+      pos[j] = -1;                       // -1: past the end
+      if (i < src.n) src.get(i, key[j], pos[j]);
+    }
+    unsigned ball[kBatch];
+    uint32_t n_warp = 0;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const bool in = pos[j] >= 0 && (key[j] >> 20) == b1;
+      if (in) atomicAdd(&sh[(key[j] >> 8) & 0xFFFu], 1u);
+      ball[j] = __ballot_sync(0xffffffffu, in);
+      n_warp += (uint32_t)__popc(ball[j]);
+    }
+    if (n_warp) {
+      uint32_t slot = 0;
+      if (lane == 0) slot = atomicAdd(&S.n_eq, n_warp);
+      slot = __shfl_sync(0xffffffffu, slot, 0);
+      const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if ((ball[j] >> lane) & 1u) {
+          const uint32_t at = slot + (uint32_t)__popc(ball[j] & lt);
+          if (at < (uint32_t)kEqCache) S.eq[at] = make_uint2(key[j], (uint32_t)pos[j]);
+        }
+        slot += (uint32_t)__popc(ball[j]);
+      }
+    }
   }
   __syncthreads();
+  const uint32_t n_eq = S.n_eq;
+  const bool cached = n_eq <= (uint32_t)kEqCache;
+  // calls f(key, pos) for every bin-b1 pair, from shared memory when cached
+  auto for_each_eq = [&](auto f) {
+    if (cached) {
+      for (uint32_t i = threadIdx.x; i < n_eq; i += blockDim.x) {
+        const uint2 e = S.eq[i];
+        f(e.x, (int32_t)e.y);
+      }
+    } else {
+      for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
+        uint32_t key; int32_t pos;
+        src.get(i, key, pos);
+        if ((key >> 20) == b1) f(key, pos);
+      }
+    }
+  };
   find_bin(sh, kHistBins, r1, true, S.warp_sums, &S.s_bin, &S.s_before);
   const uint32_t b2 = (uint32_t)S.s_bin;
   const uint32_t r2 = r1 - S.s_before;
@@ -261,11 +360,9 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
   // level 3: bits 7..0 among keys whose bits 31..8 are hi20
   for (int i = threadIdx.x; i < kThreads; i += blockDim.x) sh[i] = 0;
   __syncthreads();
-  for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
-    uint32_t key; int32_t pos;
-    src.get(i, key, pos);
+  for_each_eq([&](uint32_t key, int32_t) {
     if ((key >> 8) == hi20) atomicAdd(&sh[key & 0xFFu], 1u);
-  }
+  });
   __syncthreads();
   // 256 bins padded with zero bins to the block size; walking down from the
   // top passes the zero bins first
@@ -288,15 +385,13 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
       __syncthreads();
       for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
       __syncthreads();
-      for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
-        uint32_t key; int32_t pos;
-        src.get(i, key, pos);
+      for_each_eq([&](uint32_t key, int32_t pos) {
         if (key == kstar) {
           const uint32_t p = (uint32_t)pos;
           const uint32_t hi_bits = lvl == 0 ? 0u : (p >> (sft + widths[lvl]));
           if (hi_bits == prefix) atomicAdd(&sh[(p >> sft) & (nb - 1)], 1u);
         }
-      }
+      });
       __syncthreads();
       // ascending walk over max(nb, blockDim) bins (extra bins are zero)
       const int nbins = (int)max(nb, (uint32_t)blockDim.x);
@@ -348,8 +443,9 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
       __syncthreads();
       for (uint32_t r0 = 0; r0 < n_group; r0 += (uint32_t)kGather * kThreads) {
         const uint32_t l0 = r0 + (uint32_t)kGather * threadIdx.x;
-        uint32_t m = 0;
-        int32_t posv[kGather];
+        // list slots of this thread's entries (shared memory only), then all
+        // loads at once, then the tests
+        uint32_t at[kGather];
         if (l0 < n_group) {
           // the last run starting at or before l0 (runs are non-empty there)
           int lo = 0, hi = ng;
@@ -361,14 +457,27 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
 #pragma unroll
           for (int j = 0; j < kGather; ++j) {
             const uint32_t l = l0 + j;
-            posv[j] = 0;
+            at[j] = 0xffffffffu;
             if (l < n_group) {
               while (c + 1 < ng && S.run_pre[c + 1] <= l) ++c;
-              const uint2 e = __ldcg(src.list + S.run_at[c] + (l - S.run_pre[c]));
-              posv[j] = (int32_t)e.y;
-              if (e.x > kstar || (e.x == kstar && (int32_t)e.y <= pstar)) m |= 1u << j;
+              at[j] = S.run_at[c] + (l - S.run_pre[c]);
             }
           }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kGather; ++j) at[j] = 0xffffffffu;
+        }
+        uint2 e[kGather];
+#pragma unroll
+        for (int j = 0; j < kGather; ++j)
+          e[j] = at[j] != 0xffffffffu ? __ldcg(src.list + at[j]) : make_uint2(0u, 0u);
+        uint32_t m = 0;
+        int32_t posv[kGather];
+#pragma unroll
+        for (int j = 0; j < kGather; ++j) {
+          posv[j] = (int32_t)e[j].y;
+          if (at[j] != 0xffffffffu && (e[j].x > kstar || (e[j].x == kstar && (int32_t)e[j].y <= pstar)))
+            m |= 1u << j;
         }
         uint32_t tot;
         uint32_t o = written + block_excl_scan((uint32_t)__popc(m), S.warp_sums, &tot);
@@ -423,7 +532,9 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
   const float *row = scores + (int64_t)t * ld;
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
 
-  // this thread's scores, loads in flight while the threshold is found
+  // this row's histogram slice, then this thread's scores: all loads in
+  // flight while the threshold is found
+  const HistSlice hs = hist_load(hist + (size_t)t * kHistBins);
   uint32_t v[kRounds][kPer];
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
@@ -445,7 +556,7 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
   }
   if (threadIdx.x == 0) { S.s_bin = 0; S.s_before = 0; }
   __syncthreads();
-  threshold_bin(hist + (size_t)t * kHistBins, (uint32_t)k, S.warp_sums, &S.s_bin, &S.s_before);
+  threshold_bin(hs, (uint32_t)k, S.warp_sums, &S.s_bin, &S.s_before);
   const uint32_t b1 = (uint32_t)S.s_bin;
   const uint32_t n_gt = S.s_before;
 
