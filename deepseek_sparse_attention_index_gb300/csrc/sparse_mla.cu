@@ -304,7 +304,7 @@ cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s) {
                       sizeof(__nv_bfloat16) * kHeadsPerCta * kQStride;
   dim3 grid((unsigned)a.T, (unsigned)a.n_splits, (unsigned)((a.H + kHeadsPerCta - 1) / kHeadsPerCta));
   cudaError_t e;
-  if (a.kv.format == DSA_KV_BF16 && (a.k2 == 0 || a.kv2.format == DSA_KV_BF16)) {
+  if (sparse_mla_tc_bf16_ok(a)) {
     e = sparse_mla_tc_bf16_launch(a, s);
   } else if (a.Dv == 512) {
     e = cudaFuncSetAttribute(sparse_mla_simt_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,

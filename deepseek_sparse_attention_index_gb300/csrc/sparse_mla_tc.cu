@@ -26,9 +26,22 @@
 // math warps, one TMEM lane quadrant each) and the sums are rescaled.
 // Otherwise p <= 256, exact in fp32 and representable in bf16.
 //
-// Warps: 0-3 math, 4 MMA issue, 5-6 gather (cp.async 16-byte copies into the
-// 128-byte-swizzled operand layout, 32 rows each per tile, zero-filled for
-// masked rows so that a -1 entry is never read).
+// Two gather warps copy each tile's rows with 16-byte cp.async into the
+// 128-byte-swizzled operand layout (a masked entry -- -1, out of range, or
+// past the list's end -- is zero-filled and never read); Q arrives by TMA.
+// Only two 72 KB stages fit beside Q, so each lane first pulls its rows into
+// L2 a few tiles ahead: HBM streams ahead of the stages and the copies into
+// shared memory see L2 latency.
+// (A TMA row gather moves 512 bytes per instruction at a few tens of cycles
+// of issue each; one warp of cp.async moves as much per instruction at a
+// fraction of that.)
+//
+// S and PV are issued by two warps: small MMAs have a per-instruction issue
+// floor (~55 cycles for any N <= 64 from one thread), and a second issuing
+// thread roughly doubles the rate for the 64 x 64 S products.  The S warp
+// runs ahead as soon as a tile has landed; the PV warp follows the softmax.
+//
+// Warps: 0-3 math, 4 S issue, 5 PV issue (and the Q load), 6-7 gather.
 #include <math.h>
 
 #include "common.cuh"
@@ -39,7 +52,7 @@ namespace dsa {
 
 namespace {
 
-constexpr int kThreads = 224;      // 7 warps (<= 2 per SM sub-partition: no register cap)
+constexpr int kThreads = 256;      // 8 warps (<= 2 per SM sub-partition: no register cap)
 constexpr int kTileRows = 64;
 constexpr int kKBlocks = 9;        // 576 bf16 = 9 x 128 bytes
 constexpr int kKBlockBytes = kTileRows * 128;               // 8 KB
@@ -48,6 +61,22 @@ constexpr int kQBytes = kKBlocks * 64 * 128;                // Q padded to 64 he
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.0f;      // log2 of the largest tolerated p
+constexpr int kPrefetchTiles = 4;  // rows are pulled into L2 this many tiles ahead
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
 
 struct MlaSmem {
   uint32_t q, k, p, alpha, inv_l, flag, bars, total;
@@ -66,23 +95,10 @@ __host__ __device__ inline MlaSmem mla_smem_layout() {
   return L;
 }
 
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-// Row address of list entry e (of the concatenated main + extra list) of
-// token t, or nullptr when the entry is masked.  An entry other than -1
-// outside [0, rows) is reported through err_flag (when `report`) and masked
-// like -1.
-__device__ __forceinline__ const uint8_t *entry_row(const MlaArgs &a, int t, int e, bool report) {
+// Pool slot of list entry e (of the concatenated main + extra list) of token
+// t, or -1 when the entry is masked.  An entry other than -1 outside [0,
+// rows) is reported through err_flag (when `report`) and masked like -1.
+__device__ __forceinline__ int64_t entry_slot(const MlaArgs &a, int t, int e, bool report) {
   const PoolDev *pool;
   int64_t slot;
   if (e < a.k) {
@@ -92,13 +108,14 @@ __device__ __forceinline__ const uint8_t *entry_row(const MlaArgs &a, int t, int
     pool = &a.kv2;
     slot = a.idx2[(size_t)t * a.k2 + (e - a.k)];
   }
-  if (slot >= 0 && slot < pool->rows) return pool->data + slot * (int64_t)1152;
+  if (slot >= 0 && slot < pool->rows) return slot;
   if (report && slot != -1) raise_flag(a.err_flag, DSA_DEVERR_INDEX_RANGE);
-  return nullptr;
+  return -1;
 }
 
 template <int N>   // heads of the PV product (16, 32 or 64)
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int per) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const MlaSmem L = mla_smem_layout();
   unsigned char *q_s = smem + L.q;
@@ -114,9 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
   uint64_t *sempty = bars + 6;   // [2]
   uint64_t *pfull = bars + 8;
   uint64_t *pempty = bars + 9;
-  uint64_t *done = bars + 10;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 12);
+  uint64_t *done = bars + 10;     // [2]: S warp, PV warp
+  uint64_t *qfull = bars + 12;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 14);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -125,8 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
   const int h0 = blockIdx.z * 64;
   const int nh = min(64, a.H - h0);
   const int total = a.k + a.k2;
-  const int per = (total + a.n_splits - 1) / a.n_splits;
-  const int j0 = min(total, split * per);
+  const int j0 = min(total, split * per);   // per: a multiple of the tile
   const int je = min(total, j0 + per);
   const int nt = (je - j0 + kTileRows - 1) / kTileRows;
   // TMEM: S[2] at columns [0, 128), O^T blocks at [128, 128 + 4N)
@@ -146,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
     }
     tc::mbar_init(pfull, 4);
     tc::mbar_init(pempty, 1);
-    tc::mbar_init(done, 1);
+    tc::mbar_init(&done[0], 1);
+    tc::mbar_init(&done[1], 1);
+    tc::mbar_init(qfull, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -154,73 +173,112 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
-  // Q of this head group, K-major 128B-swizzled: K-block kb holds 64 rows of
-  // 128 bytes; rows >= nh are zero.  Asynchronous copies, no load round trips.
-  {
-    const uint16_t *qg = static_cast<const uint16_t *>(a.q) + ((size_t)t * a.H + h0) * 576;
-    const uint32_t q_addr0 = tc::smem_u32(q_s);
-    for (int i = threadIdx.x; i < 64 * 72; i += blockDim.x) {
-      const int h = i / 72, c = i % 72;   // c: 16-byte chunk of the 1152-byte row
-      const int kb = c >> 3, cc = c & 7;
-      const bool real = h < nh;
-      cp_async_16(q_addr0 + kb * kKBlockBytes + h * 128 + ((cc ^ (h & 7)) << 4),
-                  real ? static_cast<const void *>(qg + (size_t)h * 576 + c * 8) : a.q,
-                  real ? 16u : 0u);
-    }
-    cp_async_commit();
-    cp_async_wait_all();
-  }
-  tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 5) {
+  if (warp >= 6) {
     // -------------------------------------------------------------- gather
-    const int half = warp - 5;          // rows [32*half, 32*half + 32) of every tile
+    const int half = warp - 6;          // rows [32*half, 32*half + 32) of every tile
+    // this lane's row of tile i (row 32*half + lane), or nullptr when masked
+    auto row_of = [&](int i) -> const uint8_t * {
+      const int e = j0 + i * kTileRows + 32 * half + lane;
+      if (e >= je) return nullptr;
+      const int64_t slot = entry_slot(a, t, e, false);
+      if (slot < 0) return nullptr;
+      return (e < a.k ? a.kv.data : a.kv2.data) + slot * (int64_t)1152;
+    };
+    // each lane pulls its rows into L2 kPrefetchTiles tiles ahead of the copy
+    // into shared memory, so the copy meets L2 latency instead of HBM's
+    auto prefetch_row = [&](int i) {
+      const uint8_t *row = row_of(i);
+      if (row) {
+#pragma unroll
+        for (int c = 0; c < 9; ++c) prefetch_l2(row + 128 * c);
+      }
+    };
+    for (int i = 0; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);
+    const uint8_t *next = nt > 0 ? row_of(0) : nullptr;
     for (int i = 0; i < nt; ++i) {
       const int st = i & 1;
+      const uint8_t *my_row = next;
       if (!tc::mbar_wait(&kempty[st], ((i >> 1) & 1) ^ 1, abort_flag)) break;
       const uint32_t sbase = tc::smem_u32(k_s + st * kStageBytes);
-      const int e = j0 + i * kTileRows + 32 * half + lane;
-      const uint8_t *my_row = e < je ? entry_row(a, t, e, false) : nullptr;
-#pragma unroll 4
-      for (int rr = 0; rr < 32; ++rr) {
-        const int r = 32 * half + rr;
-        const uint8_t *row = reinterpret_cast<const uint8_t *>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(my_row), rr));
-        const uint8_t *src = row ? row : a.kv.data;
-        const uint32_t nbytes = row ? 16u : 0u;
+#pragma unroll 1
+      for (int r0 = 32 * half; r0 < 32 * half + 32; r0 += 8) {
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          const int c = lane + 32 * q;          // 16-byte chunk of the row, 0..71
-          if (c < 72) {
-            const int kb = c >> 3, cc = c & 7;
-            cp_async_16(sbase + kb * kKBlockBytes + r * 128 + ((cc ^ (r & 7)) << 4),
-                        src + (row ? c * 16 : 0), nbytes);
+        for (int j = 0; j < 8; ++j) {       // row r0 + j: swizzle phase j
+          const uint8_t *row = reinterpret_cast<const uint8_t *>(__shfl_sync(
+              0xffffffffu, reinterpret_cast<unsigned long long>(my_row), (r0 & 31) + j));
+          const uint8_t *src = row ? row : static_cast<const uint8_t *>(a.q);   // not read when masked
+          const uint32_t nbytes = row ? 16u : 0u;
+          const uint32_t rdst = sbase + (r0 + j) * 128;
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const int c = lane + 32 * q;          // 16-byte chunk of the row, 0..71
+            if (c < 72)
+              cp_async_16(rdst + (c >> 3) * kKBlockBytes + (((c & 7) ^ j) << 4),
+                          src + (row ? c * 16 : 0), nbytes);
           }
         }
       }
       cp_async_commit();
+      if (i + kPrefetchTiles < nt) prefetch_row(i + kPrefetchTiles);
+      if (i + 1 < nt) next = row_of(i + 1);   // index loads overlap the copies
       cp_async_wait_all();
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&kfull[st]);
     }
     cp_async_wait_all();
+    __syncwarp();
   } else if (warp == 4) {
-    // -------------------------------------------------------------- MMA issue
+    // -------------------------------------------------------------- S issue
     if (lane == 0) {
       // S = Q K^T: A = Q (K-major, M = 64), B = K tile (K-major, N = 64)
       constexpr uint32_t idesc_s = tc::idesc_f32acc(1, 1, 0, 0, 64, 64);
+      const uint32_t q_addr = tc::smem_u32(q_s);
+      bool ok = nt == 0 || tc::mbar_wait(qfull, 0, abort_flag);
+      for (int i = 0; i < nt && ok; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!tc::mbar_wait(&kfull[st], ph, abort_flag)) break;
+        if (!tc::mbar_wait(&sempty[st], ph ^ 1, abort_flag)) break;
+        tc::fence_after_sync();
+        const uint32_t k_addr = tc::smem_u32(k_s + st * kStageBytes);
+#pragma unroll 1
+        for (int kb = 0; kb < kKBlocks; ++kb) {
+          const uint64_t ad0 = tc::sdesc_sw128(q_addr + kb * kKBlockBytes, 16, 1024);
+          const uint64_t bd0 = tc::sdesc_sw128(k_addr + kb * kKBlockBytes, 16, 1024);
+#pragma unroll
+          for (int ko = 0; ko < 4; ++ko)   // 32 bytes (16 bf16) of K per instruction
+            tc::mma_f16(tmem + kSCol + st * 64, ad0 + 2 * ko, bd0 + 2 * ko, idesc_s,
+                        (kb > 0 || ko > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&sfull[st]);
+      }
+      if (nt > 0) {
+        // this warp's MMAs retired before TMEM is released
+        tc::mma_commit(&done[0]);
+        tc::mbar_wait_drain(&done[0], 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // -------------------------------------------------------------- PV issue
+    if (lane == 0) {
+      tc::prefetch_tmap(&qmap);
+      // Q of this head group: nine 64-column boxes of 64 heads (heads past H
+      // lie outside the map and read as zeros)
+      tc::mbar_arrive_expect_tx(qfull, kQBytes);
+      for (int kb = 0; kb < kKBlocks; ++kb)
+        tc::tma_load_3d(&qmap, qfull, q_s + kb * kKBlockBytes, kb * 64, h0, t);
       // O^T += V^T P^T: A = V^T (MN-major, M = 128), B = P (K-major, N heads)
       constexpr uint32_t idesc_pv = tc::idesc_f32acc(1, 1, 1, 0, N, 128);
-      const uint32_t q_addr = tc::smem_u32(q_s);
       const uint32_t p_addr = tc::smem_u32(p_s);
-      bool ok = true;
-      auto issue_pv = [&](int i) -> bool {
+      for (int i = 0; i < nt; ++i) {
         const int st = i & 1;
-        if (!tc::mbar_wait(pfull, i & 1, abort_flag)) return false;
+        if (!tc::mbar_wait(pfull, i & 1, abort_flag)) break;
         tc::fence_after_sync();
         const uint32_t k_addr = tc::smem_u32(k_s + st * kStageBytes);
         const uint32_t plo_addr = k_addr + 8 * kKBlockBytes;   // P_lo: the RoPE block
@@ -237,34 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
         }
         tc::mma_commit(&kempty[st]);
         tc::mma_commit(pempty);
-        return true;
-      };
-      for (int i = 0; i < nt && ok; ++i) {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!tc::mbar_wait(&kfull[st], ph, abort_flag)) { ok = false; break; }
-        if (!tc::mbar_wait(&sempty[st], ph ^ 1, abort_flag)) { ok = false; break; }
-        tc::fence_after_sync();
-        const uint32_t k_addr = tc::smem_u32(k_s + st * kStageBytes);
-#pragma unroll 1
-        for (int kb = 0; kb < kKBlocks; ++kb) {
-          const uint64_t ad0 = tc::sdesc_sw128(q_addr + kb * kKBlockBytes, 16, 1024);
-          const uint64_t bd0 = tc::sdesc_sw128(k_addr + kb * kKBlockBytes, 16, 1024);
-#pragma unroll
-          for (int ko = 0; ko < 4; ++ko)   // 32 bytes (16 bf16) of K per instruction
-            tc::mma_f16(tmem + kSCol + st * 64, ad0 + 2 * ko, bd0 + 2 * ko, idesc_s,
-                        (kb > 0 || ko > 0) ? 1u : 0u);
-        }
-        tc::mma_commit(&sfull[st]);
-        // PV(i) right after S(i): the stage of tile i is then freed as early as
-        // possible, so the gather of tile i + 2 overlaps S(i+1), softmax(i+1)
-        // and PV(i+1)
-        if (!issue_pv(i)) { ok = false; break; }
       }
       if (nt > 0) {
-        tc::mma_commit(done);
-        tc::mbar_wait_drain(done, 0);
+        tc::mma_commit(&done[1]);
+        tc::mbar_wait_drain(&done[1], 0);
       }
+      tc::mbar_wait_drain(qfull, 0);   // the Q load landed before the CTA exits
     }
     __syncwarp();
   } else {
@@ -281,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
       const int b = i & 1;                  // S buffer and K stage of tile i
       // validity of the 64 entries of this tile as a bit mask (2 loads per lane)
       const int e = j0 + i * kTileRows + lane;
-      const bool v_lo = e < je && entry_row(a, t, e, quad == 0) != nullptr;
-      const bool v_hi = e + 32 < je && entry_row(a, t, e + 32, quad == 0) != nullptr;
+      const bool v_lo = e < je && entry_slot(a, t, e, quad == 0) >= 0;
+      const bool v_hi = e + 32 < je && entry_slot(a, t, e + 32, quad == 0) >= 0;
       const uint32_t vm_lo = __ballot_sync(0xffffffffu, v_lo);
       const uint32_t vm_hi = __ballot_sync(0xffffffffu, v_hi);
       if (!tc::mbar_wait(&sfull[b], (i >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -368,12 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
     }
     tc::named_bar_sync(1, 128);
     const bool have_o = ok && nt > 0;
-    const int Dv = a.Dv;
+    // this CTA's records: [nh heads][kDv] bf16 (one piece) or fp32 partials
+    constexpr int kDv = 512;
+    const size_t rec0 = a.n_splits == 1 ? (size_t)t * a.H + h0
+                                        : ((size_t)t * a.n_splits + split) * a.H + h0;
 #pragma unroll 1
     for (int j = 0; j < 4; ++j) {
       const int dv = 128 * j + 32 * quad + lane;
 #pragma unroll 1
-      for (int c0 = 0; c0 < N; c0 += 16) {
+      for (int c0 = 0; c0 < N && c0 < nh; c0 += 16) {
         float o[16];
         if (have_o) {
           tc::tmem_ld_cols<16>(tmem + lane_base + kOCol + j * N + c0, o);
@@ -381,18 +420,32 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
 #pragma unroll
           for (int h = 0; h < 16; ++h) o[h] = 0.f;
         }
-        if (dv >= Dv) continue;
+        float inv[16];
 #pragma unroll
-        for (int hq = 0; hq < 16; ++hq) {
-          const int h = c0 + hq;
-          if (h < nh) {
-            const size_t rec = a.n_splits == 1 ? (size_t)t * a.H + h0 + h
-                                               : ((size_t)t * a.n_splits + split) * a.H + h0 + h;
-            const float v = o[hq] * inv_l[h];
-            if (a.n_splits == 1)
-              static_cast<__nv_bfloat16 *>(a.out)[rec * Dv + dv] = __float2bfloat16_rn(v);
-            else
-              a.part_o[rec * Dv + dv] = v;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 v = *reinterpret_cast<const float4 *>(inv_l + c0 + 4 * q4);
+          inv[4 * q4] = v.x; inv[4 * q4 + 1] = v.y; inv[4 * q4 + 2] = v.z; inv[4 * q4 + 3] = v.w;
+        }
+        const int nq = min(16, nh - c0);   // heads of this chunk that exist
+        if (a.n_splits == 1) {
+          __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + (rec0 + c0) * kDv + dv;
+          if (nq == 16) {
+#pragma unroll
+            for (int hq = 0; hq < 16; ++hq) dst[hq * kDv] = __float2bfloat16_rn(o[hq] * inv[hq]);
+          } else {
+#pragma unroll
+            for (int hq = 0; hq < 16; ++hq)
+              if (hq < nq) dst[hq * kDv] = __float2bfloat16_rn(o[hq] * inv[hq]);
+          }
+        } else {
+          float *dst = a.part_o + (rec0 + c0) * kDv + dv;
+          if (nq == 16) {
+#pragma unroll
+            for (int hq = 0; hq < 16; ++hq) dst[hq * kDv] = o[hq] * inv[hq];
+          } else {
+#pragma unroll
+            for (int hq = 0; hq < 16; ++hq)
+              if (hq < nq) dst[hq * kDv] = o[hq] * inv[hq];
           }
         }
       }
@@ -417,17 +470,32 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaArgs a) {
 
 template <int N>
 cudaError_t launch_n(const MlaArgs &a, cudaStream_t s) {
+  CUtensorMap qmap;
+  // Q [T][H][576] bf16 in boxes of 64 columns x 64 heads
+  if (!make_tmap_3d(&qmap, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 576, (uint64_t)a.H,
+                    (uint64_t)a.T, 64, 64, 1))
+    return cudaErrorInvalidValue;
+  const int total = a.k + a.k2;
+  int per = (total + a.n_splits - 1) / a.n_splits;
+  per = (per + kTileRows - 1) / kTileRows * kTileRows;
   const MlaSmem L = mla_smem_layout();
   auto kern = sparse_mla_tc_kernel<N>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)a.T, (unsigned)a.n_splits, (unsigned)((a.H + 63) / 64));
-  kern<<<grid, kThreads, L.total, s>>>(a);
+  kern<<<grid, kThreads, L.total, s>>>(a, qmap, per);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+bool sparse_mla_tc_bf16_ok(const MlaArgs &a) {
+  // bf16 rows of 576 (V = the leading 512); Q read by TMA needs a 16-byte
+  // aligned base
+  return a.D == 576 && a.Dv == 512 && a.kv.format == DSA_KV_BF16 &&
+         (a.k2 == 0 || a.kv2.format == DSA_KV_BF16) && (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
+}
 
 cudaError_t sparse_mla_tc_bf16_launch(const MlaArgs &a, cudaStream_t s) {
   const int hg = a.H >= 64 ? 64 : a.H;

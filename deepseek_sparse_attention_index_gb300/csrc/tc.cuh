@@ -103,6 +103,28 @@ DSA_DEVINLINE void tma_load_2d(const CUtensorMap *map, uint64_t *bar, void *dst,
       : "memory");
 }
 
+DSA_DEVINLINE void tma_load_3d(const CUtensorMap *map, uint64_t *bar, void *dst, int x, int y,
+                              int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Row gather: rows y0..y3 (each in [0, rows) of the map), columns [x, x +
+// box width), into four consecutive box-sized rows at dst.  The map's box
+// must be one row high.
+DSA_DEVINLINE void tma_gather4(const CUtensorMap *map, uint64_t *bar, void *dst, int x, int y0,
+                               int y1, int y2, int y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1),
+      "r"(y2), "r"(y3)
+      : "memory");
+}
+
 // Tile load of `box` elements starting at element x of a map made by
 // make_tmap_1d.  The caller keeps x * element size a multiple of 16 bytes.
 DSA_DEVINLINE void tma_load_1d(const CUtensorMap *map, uint64_t *bar, void *dst, int x) {
@@ -312,5 +334,10 @@ bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
 // `box` elements, no swizzle, zero fill out of bounds.
 bool make_tmap_1d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
                   uint64_t n, uint32_t box);
+// 3-D tiled map over a dense [d2][d1][d0] array (d0 contiguous), 128-byte
+// swizzle; out-of-range boxes read zeros.
+bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                  uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1,
+                  uint32_t box2);
 
 }  // namespace dsa

@@ -50,4 +50,19 @@ bool make_tmap_1d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                  uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1,
+                  uint32_t box2) {
+  std::call_once(g_once, resolve);
+  if (!g_encode) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * (cuuint64_t)elem_bytes, d0 * d1 * (cuuint64_t)elem_bytes};
+  cuuint32_t box[3] = {box0, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace dsa
