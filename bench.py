@@ -282,6 +282,145 @@ def run_ours(args, rank, world):
     return res
 
 
+# ---------------------------------------------------------------- other workloads
+
+def _timed(fn, steps, warmup, flush_fn):
+    """Device µs of fn() per call: W warm-up calls, then K calls each between
+    CUDA events on the current stream, the L2 flushed before each (outside the
+    events); all launches queued behind a GPU-side sleep."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = []
+    torch.cuda._sleep(50_000_000)
+    for i in range(steps):
+        flush_fn(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return [1000.0 * a.elapsed_time(b) for a, b in ev]
+
+
+def run_workload(args):
+    """Secondary measurements (one JSON line each): the other configurations
+    of the scope table, timed like the default line.  Not the default line."""
+    import torch
+    from deepseek_sparse_attention_index_gb300 import build as B
+    from deepseek_sparse_attention_index_gb300 import inputs as I
+    from deepseek_sparse_attention_index_gb300 import ops
+    B.build()
+    ops.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm_gbs, bf16_tflops, peak_kind = measured_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def l2_flush(i):
+        flush.fill_(i & 0xff)
+        flush_rd.sum()
+
+    clocks = ClockSampler(0)
+    res = {"metric": METRIC, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
+           "vs_baseline": None, "data": "synthetic", "e2e": None, "gpu_launches": None}
+    w = args.workload
+    if w in ("tiny", "packed_1m"):
+        case = I.tiny_decode(device=dev) if w == "tiny" else I.packed_long_decode(device=dev)
+        k_swa = 0 if case.idx_swa is None else case.idx_swa.shape[1]
+        ws = ops.workspace(ops.dsa_decode_workspace_size(case.B, case.max_seq_len, case.k,
+                                                         case.H, case.Dv, k_swa), dev)
+        fn = lambda: ops.decode_case(case, ws=ws)
+        clocks.start()
+        us = _timed(fn, args.steps, args.warmup, l2_flush)
+        clk = clocks.stop()
+        N = case.max_seq_len
+        if w == "tiny":
+            nbytes = N * 64 * 2 + min(N, case.k) * 1152 + case.H * (576 * 2 + 512 * 2 + 4)
+            dtype = "bf16 indexer + bf16 attention"
+        else:
+            nbytes = N * (128 + 4 + 4) + (case.k + k_swa) * 584 + case.H * (512 * 2 + 448 * 2 + 4)
+            dtype = "fp8_e4m3 indexer + fp8_ds_mla attention (fp32 accumulate)"
+        v = statistics.median(us)
+        res.update({"value": round(v, 3), "ms_per_step": round(v / 1000, 6), "dtype": dtype,
+                    "config": {"workload": case.name, "batch": case.B, "context": N,
+                               "topk": case.k, "swa": k_swa, "heads": case.H},
+                    "step_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": nbytes,
+                                      "achieved_gbs": round(nbytes / (v * 1e-6) / 1e9, 1),
+                                      "frac": round(nbytes / (v * 1e-6) / 1e9 / hbm_gbs, 4),
+                                      "peak": hbm_gbs, "peak_kind": peak_kind},
+                    "clocks": clk})
+    elif w == "uniform_fp8":
+        case = I.uniform_fp8_swa_topk_case(device=dev)
+        n = case.idx.shape[1]
+        ws = ops.workspace(ops.dsa_sparse_mla_workspace_size(case.T, case.H, case.Dv, n, 0), dev)
+        fn = lambda: ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, case.idx, ws=ws)
+        clocks.start()
+        us = _timed(fn, args.steps, args.warmup, l2_flush)
+        clk = clocks.stop()
+        valid = int((case.idx >= 0).sum())
+        nbytes = valid * (512 + 32) + case.T * case.H * (512 * 2 + 448 * 2 + 4) + case.idx.numel() * 4
+        v = statistics.median(us)
+        res.update({"value": round(v, 3), "ms_per_step": round(v / 1000, 6),
+                    "dtype": "fp8_e4m3 pool (1x64 fp32 scales) + bf16 q, fp32 accumulate",
+                    "config": {"workload": case.name, "batch": case.T, "entries": n,
+                               "heads": case.H, "D": case.D, "Dv": case.Dv},
+                    "step_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": nbytes,
+                                      "achieved_gbs": round(nbytes / (v * 1e-6) / 1e9, 1),
+                                      "frac": round(nbytes / (v * 1e-6) / 1e9 / hbm_gbs, 4),
+                                      "peak": hbm_gbs, "peak_kind": peak_kind},
+                    "clocks": clk})
+    elif w == "prefill":
+        T, H = args.context, args.heads
+        case = I.prefill_case([T], k=2048, H=H, device=dev)
+        ind = case.indexer
+        maxL = T
+        ld = (maxL + 3) // 4 * 4
+        scores = torch.empty((T, ld), dtype=torch.float32, device=dev)
+        rl = (case.row_end - case.row_start).contiguous()
+        tws = ops.workspace(ops.dsa_topk_workspace_size(T, maxL, case.k), dev)
+        mws = ops.workspace(ops.dsa_sparse_mla_workspace_size(T, H, 512, case.k, 0), dev)
+        idx = torch.empty((T, case.k), dtype=torch.int32, device=dev)
+        f_idx = lambda: ops.dsa_index_score(ind["q_idx"], 1, ind["q_scale"], ind["k_idx"],
+                                            ind["k_scale"], ind["w"], case.row_start,
+                                            case.row_end, maxL, scores=scores)
+        f_topk = lambda: ops.dsa_topk(scores, rl, case.k, maxL, index_base=case.row_start,
+                                      idx=idx, ws=tws)
+        f_mla = lambda: ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, idx, ws=mws)
+        clocks.start()
+        st = {"index_score": statistics.median(_timed(f_idx, args.steps, args.warmup, l2_flush)),
+              "topk": statistics.median(_timed(f_topk, args.steps, args.warmup, l2_flush)),
+              "sparse_mla": statistics.median(_timed(f_mla, args.steps, args.warmup, l2_flush))}
+        clk = clocks.stop()
+        R = sum(min(t + 1, case.k) for t in range(T))
+        mla_flop = 2.0 * H * R * 1088
+        idx_flop = 2.0 * 64 * 128 * T * (T + 1) / 2
+        v = sum(st.values())
+        fp8_tflops = 2.0 * bf16_tflops   # the fp8 dense rate is twice bf16's
+        res.update({"value": round(v, 3), "ms_per_step": round(v / 1000, 6),
+                    "dtype": "fp8_e4m3 indexer + bf16 attention (fp32 accumulate)",
+                    "config": {"workload": "prefill_T%d_H%d" % (T, H), "tokens": T, "heads": H,
+                               "topk": case.k},
+                    "stages_us": {k: round(x, 2) for k, x in st.items()},
+                    "roofline": {"sparse_mla": {"bound": "tensor", "unit": "TFLOP/s",
+                                                "achieved": round(mla_flop / (st["sparse_mla"] * 1e-6) / 1e12, 1),
+                                                "peak": bf16_tflops, "peak_kind": peak_kind + " bf16 dense",
+                                                "frac": round(mla_flop / (st["sparse_mla"] * 1e-6) / 1e12 / bf16_tflops, 4),
+                                                "flop": mla_flop},
+                                 "index_score": {"bound": "tensor", "unit": "TFLOP/s",
+                                                 "achieved": round(idx_flop / (st["index_score"] * 1e-6) / 1e12, 1),
+                                                 "peak": fp8_tflops, "peak_kind": peak_kind + " bf16 x 2 (fp8 dense)",
+                                                 "frac": round(idx_flop / (st["index_score"] * 1e-6) / 1e12 / fp8_tflops, 4),
+                                                 "flop": idx_flop}},
+                    "clocks": clk})
+    print(json.dumps(res), flush=True)
+
+
 # ---------------------------------------------------------------- oracle (CPU)
 
 def oracle_sample(B, N, n_req, seed=1):
@@ -351,6 +490,11 @@ def main():
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--context", type=int, default=131072)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "tiny", "uniform_fp8", "packed_1m", "prefill"],
+                    help="decode (default): the driver's line; the others are secondary "
+                         "measurements of the remaining configurations")
+    ap.add_argument("--heads", type=int, default=64, help="prefill: attention heads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", 0))
@@ -359,6 +503,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
+        return
+    if args.workload != "decode":
+        if rank == 0:
+            run_workload(args)
         return
 
     if world > 1:
