@@ -212,8 +212,14 @@ def run_ours(args, rank, world):
     traffic = None
     tfile = os.path.join(ROOT, "profiles", "index_score_traffic.json")
     if os.path.exists(tfile):
+        # the ncu counters hold only for the kernel source they were taken on
+        import hashlib
         with open(tfile) as f:
-            traffic = json.load(f).get("bytes_per_launch_full_size")
+            tr = json.load(f)
+        h = hashlib.sha256(b"".join(open(os.path.join(ROOT, p), "rb").read()
+                                    for p in tr["source_files"])).hexdigest()[:16]
+        if h == tr.get("source_sha256_16"):
+            traffic = tr.get("bytes_per_launch_full_size")
 
     # ---- e2e: host buffers, per-step inputs copied in and results copied out
     pin = lambda t: t.detach().cpu().pin_memory()
@@ -418,6 +424,43 @@ def run_workload(args):
                                                  "frac": round(idx_flop / (st["index_score"] * 1e-6) / 1e12 / fp8_tflops, 4),
                                                  "flop": idx_flop}},
                     "clocks": clk})
+    elif w in ("index", "topk", "mla"):
+        # one stage of the decode step on decode_sweep(batch, context) inputs
+        Bsz, N, k = args.batch, args.context, 2048
+        case = I.decode_sweep(Bsz, N, device=dev)
+        ind = case.indexer
+        rs = case.slot_base
+        re = (case.slot_base + case.seq_lens).contiguous()
+        ld = (N + 3) // 4 * 4
+        scores = torch.empty((Bsz, ld), dtype=torch.float32, device=dev)
+        idx = torch.empty((Bsz, k), dtype=torch.int32, device=dev)
+        f_idx = lambda: ops.dsa_index_score(ind["q_idx"], ind["idx_dtype"], ind["q_scale"],
+                                            ind["k_idx"], ind["k_scale"], ind["w"], rs, re, N,
+                                            scores=scores)
+        tws = ops.workspace(ops.dsa_topk_workspace_size(Bsz, N, k), dev)
+        f_topk = lambda: ops.dsa_topk(scores, case.seq_lens, k, N, index_base=case.slot_base,
+                                      idx=idx, ws=tws)
+        mws = ops.workspace(ops.dsa_sparse_mla_workspace_size(Bsz, case.H, case.Dv, k, 0), dev)
+        f_mla = lambda: ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, idx, ws=mws)
+        f_idx()
+        f_topk()
+        torch.cuda.synchronize()
+        fn = {"index": f_idx, "topk": f_topk, "mla": f_mla}[w]
+        clocks.start()
+        v = statistics.median(_timed(fn, args.steps, args.warmup, l2_flush))
+        clk = clocks.stop()
+        nbytes = {"index": Bsz * N * (128 + 4 + 4) + Bsz * 64 * (128 + 8),
+                  "topk": Bsz * N * 4 + Bsz * k * 4,
+                  "mla": Bsz * min(N, k) * (1152 + 4) + Bsz * case.H * (576 * 2 + 512 * 2 + 4)}[w]
+        res.update({"value": round(v, 3), "ms_per_step": round(v / 1000, 6),
+                    "dtype": "fp8_e4m3 indexer + bf16 attention (fp32 accumulate)",
+                    "config": {"workload": "%s_b%d_n%d" % (w, Bsz, N), "batch": Bsz, "context": N,
+                               "topk": k},
+                    "step_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": nbytes,
+                                      "achieved_gbs": round(nbytes / (v * 1e-6) / 1e9, 1),
+                                      "frac": round(nbytes / (v * 1e-6) / 1e9 / hbm_gbs, 4),
+                                      "peak": hbm_gbs, "peak_kind": peak_kind},
+                    "clocks": clk})
     print(json.dumps(res), flush=True)
 
 
@@ -491,7 +534,8 @@ def main():
     ap.add_argument("--context", type=int, default=131072)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "tiny", "uniform_fp8", "packed_1m", "prefill"],
+                    choices=["decode", "tiny", "uniform_fp8", "packed_1m", "prefill",
+                             "index", "topk", "mla"],
                     help="decode (default): the driver's line; the others are secondary "
                          "measurements of the remaining configurations")
     ap.add_argument("--heads", type=int, default=64, help="prefill: attention heads")

@@ -84,9 +84,10 @@ int mla_num_splits(int T, int H, int k_total);
 size_t mla_ws_bytes(int T, int H, int Dv, int k_total);
 void mla_ws_layout(int T, int H, int Dv, int k_total, void *ws, float **part_o, float **part_lse);
 cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s);
-// tcgen05 kernel for the bf16 pool (D = 576, Dv = 512), sparse_mla_tc.cu; the
-// launch needs sparse_mla_tc_bf16_ok(a)
-bool sparse_mla_tc_bf16_ok(const MlaArgs &a);
-cudaError_t sparse_mla_tc_bf16_launch(const MlaArgs &a, cudaStream_t s);
+// tcgen05 kernels (sparse_mla_tc.cu): the format code of a call they serve
+// (bf16 pool, D = 576; uniform or packed fp8 pools, D = 512), or -1 for a call
+// the SIMT kernel takes; then the launch for that code.
+int sparse_mla_tc_format(const MlaArgs &a);
+cudaError_t sparse_mla_tc_launch(const MlaArgs &a, int fmt, cudaStream_t s);
 
 }  // namespace dsa

@@ -304,8 +304,9 @@ cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s) {
                       sizeof(__nv_bfloat16) * kHeadsPerCta * kQStride;
   dim3 grid((unsigned)a.T, (unsigned)a.n_splits, (unsigned)((a.H + kHeadsPerCta - 1) / kHeadsPerCta));
   cudaError_t e;
-  if (sparse_mla_tc_bf16_ok(a)) {
-    e = sparse_mla_tc_bf16_launch(a, s);
+  const int fmt = sparse_mla_tc_format(a);
+  if (fmt >= 0) {
+    e = sparse_mla_tc_launch(a, fmt, s);
   } else if (a.Dv == 512) {
     e = cudaFuncSetAttribute(sparse_mla_simt_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);

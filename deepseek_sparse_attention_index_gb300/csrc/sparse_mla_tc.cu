@@ -1,5 +1,18 @@
-// Absorbed-MLA sparse attention on the 5th-generation tensor cores, bf16
-// latent pool (576 = 512 NoPE + 64 RoPE per row, V = the leading 512).
+// Absorbed-MLA sparse attention on the 5th-generation tensor cores.
+//   bf16 pool: rows of 576 = 512 NoPE + 64 RoPE, V = the leading 512; the
+//     products run in bf16.
+//   fp8 pools (uniform e4m3 with 1 x 64 fp32 scales, or packed fp8_ds_mla
+//     pages with UE8M0 exponents and a bf16 RoPE tail): rows of 512 = 448
+//     NoPE + 64 RoPE, V = the leading 448.  The gather warps dequantise each
+//     row to fp16 in shared memory (an e4m3 value times a power of two is
+//     exact in fp16; times an fp32 scale it rounds once, to 2^-11 relative),
+//     Q is converted bf16 -> fp16 in shared memory, and the products run in
+//     fp16 -- whose 11-bit significand also carries p exactly enough that P
+//     needs one term.  With an fp32 scale (uniform pool) K also keeps its
+//     fp16 residual plane, S = Q K_hi^T + Q K_lo^T, because the scores are
+//     large enough (|s| ~ 20) that 2^-11 in K would move the lse by ~1e-3;
+//     that second plane fits only one stage.  A value beyond fp16's range (|x| > 65504) raises
+//     DSA_DEVERR_FP16_RANGE.
 // (The "sparse attn" stage of tokenspeed PR #627 "Add gluon kernel for DSA";
 // semantics of miles PR #3608: natural-log lse, -1 entries masked.)
 //
@@ -42,6 +55,7 @@
 // runs ahead as soon as a tile has landed; the PV warp follows the softmax.
 //
 // Warps: 0-3 math, 4 S issue, 5 PV issue (and the Q load), 6-7 gather.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -54,10 +68,26 @@ namespace {
 
 constexpr int kThreads = 256;      // 8 warps (<= 2 per SM sub-partition: no register cap)
 constexpr int kTileRows = 64;
-constexpr int kKBlocks = 9;        // 576 bf16 = 9 x 128 bytes
-constexpr int kKBlockBytes = kTileRows * 128;               // 8 KB
-constexpr int kStageBytes = kKBlocks * kKBlockBytes;        // 72 KB
-constexpr int kQBytes = kKBlocks * 64 * 128;                // Q padded to 64 heads
+constexpr int kKBlockBytes = kTileRows * 128;               // 8 KB: 64 rows x 64 16-bit values
+
+enum { kFmtBf16 = 0, kFmtUniform = 1, kFmtPacked = 2 };
+// Per pool format: K-blocks of 64 columns per row, stored V width, PV
+// K-steps per 128-row block of dv (P_hi + P_lo for bf16, one fp16 term
+// otherwise), and the operand type code of the instruction descriptor
+// (1 = bf16, 0 = fp16).
+template <int FMT> struct FmtTraits {
+  static constexpr int kKBlocks = FMT == kFmtBf16 ? 9 : 8;
+  static constexpr int kDv = FMT == kFmtBf16 ? 512 : 448;
+  static constexpr int kPvSteps = FMT == kFmtBf16 ? 8 : 4;
+  static constexpr uint32_t kOpType = FMT == kFmtBf16 ? 1u : 0u;
+  // uniform pool: K = K_hi + K_lo (two fp16 planes) for the S product, so an
+  // e4m3 value times an arbitrary fp32 scale keeps ~22 significant bits;
+  // the second plane leaves room for one stage only
+  static constexpr int kLoBlocks = FMT == kFmtUniform ? kKBlocks : 0;
+  static constexpr int kStages = FMT == kFmtUniform ? 1 : 2;
+  static constexpr int kStageBytes = (kKBlocks + kLoBlocks) * kKBlockBytes;   // 72, 64 or 128 KB
+  static constexpr int kQBytes = kKBlocks * 64 * 128;           // Q padded to 64 heads
+};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.0f;      // log2 of the largest tolerated p
@@ -82,11 +112,13 @@ struct MlaSmem {
   uint32_t q, k, p, alpha, inv_l, flag, bars, total;
 };
 
+template <int FMT>
 __host__ __device__ inline MlaSmem mla_smem_layout() {
+  using F = FmtTraits<FMT>;
   MlaSmem L;
   L.q = 0;
-  L.k = L.q + kQBytes;
-  L.p = L.k + 2 * kStageBytes;
+  L.k = L.q + F::kQBytes;
+  L.p = L.k + F::kStages * F::kStageBytes;
   L.alpha = L.p + 64 * 128;          // [2][64] rescale factors, by tile parity
   L.inv_l = L.alpha + 2 * 64 * 4;    // [64] 1 / final sums
   L.flag = L.inv_l + 64 * 4;         // [2][4] ints, by tile parity
@@ -113,11 +145,102 @@ __device__ __forceinline__ int64_t entry_slot(const MlaArgs &a, int t, int e, bo
   return -1;
 }
 
-template <int N>   // heads of the PV product (16, 32 or 64)
+// Pool addresses of an fp8 row (slot >= 0): its 512 (uniform) or 576
+// (packed: 448 e4m3 + 64 bf16) payload bytes and its scales (8 fp32 |
+// 7 UE8M0 bytes + pad).
+struct Fp8Row {
+  const uint8_t *data;
+  const uint8_t *scale;
+};
+template <int FMT>
+__device__ __forceinline__ Fp8Row fp8_row(const PoolDev &p, int64_t slot) {
+  if (FMT == kFmtUniform)
+    return {p.data + slot * 512, reinterpret_cast<const uint8_t *>(p.scales + slot * 8)};
+  const int64_t page = slot / p.block, pos = slot - page * p.block;
+  const uint8_t *pg = p.data + page * (int64_t)p.block * 584;
+  return {pg + pos * 576, pg + (int64_t)p.block * 576 + pos * 8};
+}
+
+// 2^(e - 127) of a UE8M0 byte (e = 255 -> inf, which the range check reports)
+__device__ __forceinline__ float ue8m0_scale(uint32_t e) {
+  if (e == 0) return __int_as_float(0x00400000);
+  if (e == 255) return INFINITY;
+  return __int_as_float((int)(e << 23));
+}
+
+// Round a pair of fp32 values to an fp16 pair; *bad is set when either is
+// not a finite fp16 value.
+__device__ __forceinline__ uint32_t to_f16x2(float a, float b, bool &bad) {
+  bad |= !(fabsf(a) <= 65504.f) || !(fabsf(b) <= 65504.f);
+  const __half2 r = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// 16 e4m3 values (16 bytes, lowest address first) times s -> 16 fp16 in two
+// 16-byte words, same order.
+__device__ __forceinline__ void deq16_e4m3(const uint4 v, float s, uint4 &o0, uint4 &o1,
+                                           bool &bad) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
+          (__nv_fp8x2_storage_t)((w[i] >> (16 * hh)) & 0xffffu), __NV_E4M3);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r));
+      h[2 * i + hh] = to_f16x2(f.x * s, f.y * s, bad);
+    }
+  }
+  o0 = make_uint4(h[0], h[1], h[2], h[3]);
+  o1 = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// As deq16_e4m3, and the fp16 residuals x - hi(x) as a second plane.
+__device__ __forceinline__ void deq16_e4m3_hilo(const uint4 v, float s, uint4 (&hi)[2],
+                                                uint4 (&lo)[2], bool &bad) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t h[8], r[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const __half2_raw raw = __nv_cvt_fp8x2_to_halfraw2(
+          (__nv_fp8x2_storage_t)((w[i] >> (16 * hh)) & 0xffffu), __NV_E4M3);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&raw));
+      const float x0 = f.x * s, x1 = f.y * s;
+      const uint32_t hv = to_f16x2(x0, x1, bad);
+      const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hv));
+      bool unused = false;
+      h[2 * i + hh] = hv;
+      r[2 * i + hh] = to_f16x2(x0 - hf.x, x1 - hf.y, unused);
+    }
+  }
+  hi[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  hi[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  lo[0] = make_uint4(r[0], r[1], r[2], r[3]);
+  lo[1] = make_uint4(r[4], r[5], r[6], r[7]);
+}
+
+// 8 bf16 values (one 16-byte word) -> 8 fp16, same order.
+__device__ __forceinline__ uint4 bf16x8_to_f16(const uint4 v, bool &bad) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    h[i] = to_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u), bad);
+  return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+template <int FMT, int N>   // pool format; heads of the PV product (16, 32 or 64)
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int per) {
+  using F = FmtTraits<FMT>;
+  constexpr int kKBlocks = F::kKBlocks;
+  constexpr int kStageBytes = F::kStageBytes;
+  constexpr int NS = F::kStages;   // tile i uses stage i % NS, phase (i / NS) & 1
   extern __shared__ __align__(1024) unsigned char smem[];
-  const MlaSmem L = mla_smem_layout();
+  const MlaSmem L = mla_smem_layout<FMT>();
   unsigned char *q_s = smem + L.q;
   unsigned char *k_s = smem + L.k;
   unsigned char *p_s = smem + L.p;
@@ -135,6 +258,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   uint64_t *qfull = bars + 12;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 14);
+  uint64_t *qready = bars + 15;   // fp8 pools: Q converted to fp16 by the math warps
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -166,6 +290,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     tc::mbar_init(&done[0], 1);
     tc::mbar_init(&done[1], 1);
     tc::mbar_init(qfull, 1);
+    tc::mbar_init(qready, 4);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -178,8 +303,8 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 6) {
-    // -------------------------------------------------------------- gather
+  if (warp >= 6 && FMT == kFmtBf16) {
+    // -------------------------------------------------------------- gather (bf16)
     const int half = warp - 6;          // rows [32*half, 32*half + 32) of every tile
     // this lane's row of tile i (row 32*half + lane), or nullptr when masked
     auto row_of = [&](int i) -> const uint8_t * {
@@ -201,9 +326,9 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     for (int i = 0; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);
     const uint8_t *next = nt > 0 ? row_of(0) : nullptr;
     for (int i = 0; i < nt; ++i) {
-      const int st = i & 1;
+      const int st = i % NS;
       const uint8_t *my_row = next;
-      if (!tc::mbar_wait(&kempty[st], ((i >> 1) & 1) ^ 1, abort_flag)) break;
+      if (!tc::mbar_wait(&kempty[st], ((i / NS) & 1) ^ 1, abort_flag)) break;
       const uint32_t sbase = tc::smem_u32(k_s + st * kStageBytes);
 #pragma unroll 1
       for (int r0 = 32 * half; r0 < 32 * half + 32; r0 += 8) {
@@ -232,18 +357,119 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     }
     cp_async_wait_all();
     __syncwarp();
+  } else if (warp >= 6) {
+    // -------------------------------------------------------------- gather (fp8)
+    // Lane l dequantises columns [16 l, 16 l + 16) of each row: an e4m3 word
+    // of 16 values times the scale of its 64-column group (uniform: fp32;
+    // packed: UE8M0), or -- packed, lanes 28..31 -- 16 bf16 RoPE values.
+    // Column 16 l lands in K-block l / 4, 16-byte chunks 2 (l % 4) and
+    // 2 (l % 4) + 1 of the row, swizzled by the row's phase.
+    const int half = warp - 6;
+    auto row_of = [&](int i) -> Fp8Row {
+      const int e = j0 + i * kTileRows + 32 * half + lane;
+      Fp8Row r{nullptr, nullptr};
+      if (e < je) {
+        const int64_t slot = entry_slot(a, t, e, false);
+        if (slot >= 0) r = fp8_row<FMT>(e < a.k ? a.kv : a.kv2, slot);
+      }
+      return r;
+    };
+    auto prefetch_row = [&](int i) {
+      const Fp8Row r = row_of(i);
+      if (r.data) {
+        // the 128-byte lines of the row's payload (4 or 5), then its scales
+        constexpr uintptr_t kBytes = FMT == kFmtUniform ? 512 : 576;
+        const uintptr_t first = reinterpret_cast<uintptr_t>(r.data) >> 7;
+        const uintptr_t last = (reinterpret_cast<uintptr_t>(r.data) + kBytes - 1) >> 7;
+        for (uintptr_t ln = first; ln <= last; ++ln)
+          prefetch_l2(reinterpret_cast<const void *>(ln << 7));
+        prefetch_l2(r.scale);
+      }
+    };
+    for (int i = 0; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);
+    const int kb = lane >> 2;
+    const uint32_t cc0 = 2u * (lane & 3);
+    bool bad = false;
+    Fp8Row next = nt > 0 ? row_of(0) : Fp8Row{nullptr, nullptr};
+    for (int i = 0; i < nt; ++i) {
+      const int st = i % NS;
+      const Fp8Row mine = next;
+      if (!tc::mbar_wait(&kempty[st], ((i / NS) & 1) ^ 1, abort_flag)) break;
+      unsigned char *stage = k_s + st * kStageBytes;
+#pragma unroll 1
+      for (int r0 = 0; r0 < 32; r0 += 8) {
+        uint4 v0[8], v1[8];
+        float sc[8];
+        bool has[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {        // loads of 8 rows in flight
+          const uint8_t *d = reinterpret_cast<const uint8_t *>(__shfl_sync(
+              0xffffffffu, reinterpret_cast<unsigned long long>(mine.data), r0 + b));
+          const uint8_t *sp = reinterpret_cast<const uint8_t *>(__shfl_sync(
+              0xffffffffu, reinterpret_cast<unsigned long long>(mine.scale), r0 + b));
+          has[b] = d != nullptr;
+          v0[b] = make_uint4(0u, 0u, 0u, 0u);
+          v1[b] = make_uint4(0u, 0u, 0u, 0u);
+          sc[b] = 0.f;
+          if (has[b]) {
+            if (FMT == kFmtUniform) {
+              v0[b] = __ldg(reinterpret_cast<const uint4 *>(d) + lane);
+              sc[b] = __ldg(reinterpret_cast<const float *>(sp) + kb);
+            } else if (lane < 28) {
+              v0[b] = __ldg(reinterpret_cast<const uint4 *>(d) + lane);
+              sc[b] = ue8m0_scale(__ldg(sp + kb));
+            } else {
+              const uint4 *rp = reinterpret_cast<const uint4 *>(d + 448) + 2 * (lane - 28);
+              v0[b] = __ldg(rp);
+              v1[b] = __ldg(rp + 1);
+            }
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const int r = 32 * half + r0 + b;
+          uint4 o[2], ol[2];
+          o[0] = o[1] = ol[0] = ol[1] = make_uint4(0u, 0u, 0u, 0u);
+          if (has[b]) {
+            if (FMT == kFmtUniform) {
+              deq16_e4m3_hilo(v0[b], sc[b], o, ol, bad);
+            } else if (lane < 28) {
+              deq16_e4m3(v0[b], sc[b], o[0], o[1], bad);
+            } else {
+              o[0] = bf16x8_to_f16(v0[b], bad);
+              o[1] = bf16x8_to_f16(v1[b], bad);
+            }
+          }
+          const uint32_t c0 = (cc0 ^ (uint32_t)(r & 7)) << 4, c1 = ((cc0 + 1) ^ (uint32_t)(r & 7)) << 4;
+          unsigned char *rowp = stage + kb * kKBlockBytes + r * 128;
+          *reinterpret_cast<uint4 *>(rowp + c0) = o[0];
+          *reinterpret_cast<uint4 *>(rowp + c1) = o[1];
+          if (FMT == kFmtUniform) {
+            unsigned char *lowp = rowp + kKBlocks * kKBlockBytes;
+            *reinterpret_cast<uint4 *>(lowp + c0) = ol[0];
+            *reinterpret_cast<uint4 *>(lowp + c1) = ol[1];
+          }
+        }
+      }
+      if (i + kPrefetchTiles < nt) prefetch_row(i + kPrefetchTiles);
+      if (i + 1 < nt) next = row_of(i + 1);
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&kfull[st]);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.err_flag, DSA_DEVERR_FP16_RANGE);
+    __syncwarp();
   } else if (warp == 4) {
     // -------------------------------------------------------------- S issue
     if (lane == 0) {
       // S = Q K^T: A = Q (K-major, M = 64), B = K tile (K-major, N = 64)
-      constexpr uint32_t idesc_s = tc::idesc_f32acc(1, 1, 0, 0, 64, 64);
+      constexpr uint32_t idesc_s = tc::idesc_f32acc(F::kOpType, F::kOpType, 0, 0, 64, 64);
       const uint32_t q_addr = tc::smem_u32(q_s);
-      bool ok = nt == 0 || tc::mbar_wait(qfull, 0, abort_flag);
+      bool ok = nt == 0 || tc::mbar_wait(FMT == kFmtBf16 ? qfull : qready, 0, abort_flag);
       for (int i = 0; i < nt && ok; ++i) {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!tc::mbar_wait(&kfull[st], ph, abort_flag)) break;
-        if (!tc::mbar_wait(&sempty[st], ph ^ 1, abort_flag)) break;
+        const int st = i % NS;              // K stage
+        const int sb = i & 1;               // S buffer in TMEM
+        if (!tc::mbar_wait(&kfull[st], (i / NS) & 1, abort_flag)) break;
+        if (!tc::mbar_wait(&sempty[sb], ((i >> 1) & 1) ^ 1, abort_flag)) break;
         tc::fence_after_sync();
         const uint32_t k_addr = tc::smem_u32(k_s + st * kStageBytes);
 #pragma unroll 1
@@ -251,11 +477,18 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
           const uint64_t ad0 = tc::sdesc_sw128(q_addr + kb * kKBlockBytes, 16, 1024);
           const uint64_t bd0 = tc::sdesc_sw128(k_addr + kb * kKBlockBytes, 16, 1024);
 #pragma unroll
-          for (int ko = 0; ko < 4; ++ko)   // 32 bytes (16 bf16) of K per instruction
-            tc::mma_f16(tmem + kSCol + st * 64, ad0 + 2 * ko, bd0 + 2 * ko, idesc_s,
+          for (int ko = 0; ko < 4; ++ko)   // 32 bytes (16 values) of K per instruction
+            tc::mma_f16(tmem + kSCol + sb * 64, ad0 + 2 * ko, bd0 + 2 * ko, idesc_s,
                         (kb > 0 || ko > 0) ? 1u : 0u);
+          if (F::kLoBlocks > 0) {          // the low plane of the same K-block
+            const uint64_t bl0 =
+                tc::sdesc_sw128(k_addr + (kKBlocks + kb) * kKBlockBytes, 16, 1024);
+#pragma unroll
+            for (int ko = 0; ko < 4; ++ko)
+              tc::mma_f16(tmem + kSCol + sb * 64, ad0 + 2 * ko, bl0 + 2 * ko, idesc_s, 1u);
+          }
         }
-        tc::mma_commit(&sfull[st]);
+        tc::mma_commit(&sfull[sb]);
       }
       if (nt > 0) {
         // this warp's MMAs retired before TMEM is released
@@ -268,24 +501,24 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     // -------------------------------------------------------------- PV issue
     if (lane == 0) {
       tc::prefetch_tmap(&qmap);
-      // Q of this head group: nine 64-column boxes of 64 heads (heads past H
-      // lie outside the map and read as zeros)
-      tc::mbar_arrive_expect_tx(qfull, kQBytes);
+      // Q of this head group: 64-column boxes of 64 heads (heads past H lie
+      // outside the map and read as zeros)
+      tc::mbar_arrive_expect_tx(qfull, F::kQBytes);
       for (int kb = 0; kb < kKBlocks; ++kb)
         tc::tma_load_3d(&qmap, qfull, q_s + kb * kKBlockBytes, kb * 64, h0, t);
       // O^T += V^T P^T: A = V^T (MN-major, M = 128), B = P (K-major, N heads)
-      constexpr uint32_t idesc_pv = tc::idesc_f32acc(1, 1, 1, 0, N, 128);
+      constexpr uint32_t idesc_pv = tc::idesc_f32acc(F::kOpType, F::kOpType, 1, 0, N, 128);
       const uint32_t p_addr = tc::smem_u32(p_s);
       for (int i = 0; i < nt; ++i) {
-        const int st = i & 1;
+        const int st = i % NS;
         if (!tc::mbar_wait(pfull, i & 1, abort_flag)) break;
         tc::fence_after_sync();
         const uint32_t k_addr = tc::smem_u32(k_s + st * kStageBytes);
-        const uint32_t plo_addr = k_addr + 8 * kKBlockBytes;   // P_lo: the RoPE block
+        const uint32_t plo_addr = k_addr + 8 * kKBlockBytes;   // bf16: P_lo in the RoPE block
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < F::kPvSteps; ++kk) {
             const uint32_t kr = kk & 3;   // 16 kv rows per instruction
             const uint64_t ad = tc::sdesc_sw128(k_addr + (2 * j) * kKBlockBytes + kr * 2048,
                                                 kKBlockBytes, 1024);
@@ -313,8 +546,23 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     float m = -INFINITY;                    // reference maximum (exp2 units)
     float l = 0.f;                          // running sum of p
     bool ok = true;
-    for (int i = 0; i < nt; ++i) {
-      const int b = i & 1;                  // S buffer and K stage of tile i
+    if (FMT != kFmtBf16) {
+      // Q (bf16 from the TMA load) -> fp16 in place, elementwise, so the
+      // swizzled layout is unchanged
+      if (nt > 0 && !tc::mbar_wait(qfull, 0, abort_flag)) ok = false;
+      bool bad = false;
+      if (ok) {
+        uint4 *qw = reinterpret_cast<uint4 *>(q_s);
+        for (int i2 = threadIdx.x; i2 < F::kQBytes / 16; i2 += 128)
+          qw[i2] = bf16x8_to_f16(qw[i2], bad);
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.err_flag, DSA_DEVERR_FP16_RANGE);
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(qready);
+    }
+    for (int i = 0; i < nt && ok; ++i) {
+      const int b = i & 1;                  // S buffer of tile i (= its K stage with two stages)
       // validity of the 64 entries of this tile as a bit mask (2 loads per lane)
       const int e = j0 + i * kTileRows + lane;
       const bool v_lo = e < je && entry_slot(a, t, e, quad == 0) >= 0;
@@ -364,10 +612,16 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         const float p0 = exp2f(x0 - msafe);      // -inf -> 0
         const float p1 = exp2f(x1 - msafe);
         ps += p0 + p1;
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
-        const float2 hf = __bfloat1622float2(hi);
-        phi[j / 2] = *reinterpret_cast<const uint32_t *>(&hi);
-        plo[j / 2] = pack_bf16x2(p0 - hf.x, p1 - hf.y);
+        if (FMT == kFmtBf16) {
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+          const float2 hf = __bfloat1622float2(hi);
+          phi[j / 2] = *reinterpret_cast<const uint32_t *>(&hi);
+          plo[j / 2] = pack_bf16x2(p0 - hf.x, p1 - hf.y);
+        } else {
+          const __half2 ph = __floats2half2_rn(p0, p1);   // p <= 256: 2^-11 relative
+          phi[j / 2] = *reinterpret_cast<const uint32_t *>(&ph);
+          plo[j / 2] = 0u;
+        }
       }
       l = l * al + ps;
       // P and O^T may be touched only after PV(i-1) retired
@@ -380,15 +634,16 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         for (int j = 0; j < 4; ++j) tc::tmem_scale_cols<N>(tmem + lane_base + kOCol + j * N, alpha);
       }
       if (head_lane && hl < N) {
-        // row hl of P (K-major B operand): 64 kv bf16 = 128 bytes, swizzled
-        unsigned char *plo_s = k_s + b * kStageBytes + 8 * kKBlockBytes;
+        // row hl of P (K-major B operand): 64 kv 16-bit values = 128 bytes, swizzled
+        unsigned char *plo_s = k_s + (i % NS) * kStageBytes + 8 * kKBlockBytes;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           const uint32_t off = hl * 128 + ((ch ^ (hl & 7)) << 4);
           *reinterpret_cast<uint4 *>(p_s + off) =
               make_uint4(phi[4 * ch], phi[4 * ch + 1], phi[4 * ch + 2], phi[4 * ch + 3]);
-          *reinterpret_cast<uint4 *>(plo_s + off) =
-              make_uint4(plo[4 * ch], plo[4 * ch + 1], plo[4 * ch + 2], plo[4 * ch + 3]);
+          if (FMT == kFmtBf16)
+            *reinterpret_cast<uint4 *>(plo_s + off) =
+                make_uint4(plo[4 * ch], plo[4 * ch + 1], plo[4 * ch + 2], plo[4 * ch + 3]);
         }
       }
       tc::fence_proxy_async_smem();
@@ -405,12 +660,13 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     tc::named_bar_sync(1, 128);
     const bool have_o = ok && nt > 0;
     // this CTA's records: [nh heads][kDv] bf16 (one piece) or fp32 partials
-    constexpr int kDv = 512;
+    constexpr int kDv = F::kDv;
     const size_t rec0 = a.n_splits == 1 ? (size_t)t * a.H + h0
                                         : ((size_t)t * a.n_splits + split) * a.H + h0;
 #pragma unroll 1
     for (int j = 0; j < 4; ++j) {
       const int dv = 128 * j + 32 * quad + lane;
+      if (128 * j + 32 * quad >= kDv) break;   // warp-uniform: the RoPE columns of fp8 rows
 #pragma unroll 1
       for (int c0 = 0; c0 < N && c0 < nh; c0 += 16) {
         float o[16];
@@ -468,18 +724,19 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   }
 }
 
-template <int N>
+template <int FMT, int N>
 cudaError_t launch_n(const MlaArgs &a, cudaStream_t s) {
+  using F = FmtTraits<FMT>;
   CUtensorMap qmap;
-  // Q [T][H][576] bf16 in boxes of 64 columns x 64 heads
-  if (!make_tmap_3d(&qmap, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 576, (uint64_t)a.H,
-                    (uint64_t)a.T, 64, 64, 1))
+  // Q [T][H][D] bf16 in boxes of 64 columns x 64 heads
+  if (!make_tmap_3d(&qmap, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)F::kKBlocks * 64,
+                    (uint64_t)a.H, (uint64_t)a.T, 64, 64, 1))
     return cudaErrorInvalidValue;
   const int total = a.k + a.k2;
   int per = (total + a.n_splits - 1) / a.n_splits;
   per = (per + kTileRows - 1) / kTileRows * kTileRows;
-  const MlaSmem L = mla_smem_layout();
-  auto kern = sparse_mla_tc_kernel<N>;
+  const MlaSmem L = mla_smem_layout<FMT>();
+  auto kern = sparse_mla_tc_kernel<FMT, N>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
   if (e != cudaSuccess) return e;
@@ -488,20 +745,38 @@ cudaError_t launch_n(const MlaArgs &a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-}  // namespace
-
-bool sparse_mla_tc_bf16_ok(const MlaArgs &a) {
-  // bf16 rows of 576 (V = the leading 512); Q read by TMA needs a 16-byte
-  // aligned base
-  return a.D == 576 && a.Dv == 512 && a.kv.format == DSA_KV_BF16 &&
-         (a.k2 == 0 || a.kv2.format == DSA_KV_BF16) && (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
+template <int FMT>
+cudaError_t launch_fmt(const MlaArgs &a, cudaStream_t s) {
+  const int hg = a.H >= 64 ? 64 : a.H;
+  if (hg <= 16) return launch_n<FMT, 16>(a, s);
+  if (hg <= 32) return launch_n<FMT, 32>(a, s);
+  return launch_n<FMT, 64>(a, s);
 }
 
-cudaError_t sparse_mla_tc_bf16_launch(const MlaArgs &a, cudaStream_t s) {
-  const int hg = a.H >= 64 ? 64 : a.H;
-  if (hg <= 16) return launch_n<16>(a, s);
-  if (hg <= 32) return launch_n<32>(a, s);
-  return launch_n<64>(a, s);
+}  // namespace
+
+int sparse_mla_tc_format(const MlaArgs &a) {
+  // Q is read by TMA (16-byte aligned base); fp8 rows are read as 16-byte
+  // words (16-byte aligned pool data; packed pages of an even token count)
+  if ((reinterpret_cast<uintptr_t>(a.q) & 15) != 0) return -1;
+  if (a.D == 576 && a.Dv == 512 && a.kv.format == DSA_KV_BF16 &&
+      (a.k2 == 0 || a.kv2.format == DSA_KV_BF16))
+    return kFmtBf16;
+  auto fp8_ok = [](const PoolDev &p) {
+    if ((reinterpret_cast<uintptr_t>(p.data) & 15) != 0) return false;
+    if (p.format == DSA_KV_FP8_UNIFORM) return p.scales != nullptr;
+    return p.format == DSA_KV_FP8_DS_MLA && p.block >= 2 && p.block % 2 == 0;
+  };
+  if (a.D == 512 && a.Dv == 448 && fp8_ok(a.kv) &&
+      (a.k2 == 0 || (a.kv2.format == a.kv.format && fp8_ok(a.kv2))))
+    return a.kv.format == DSA_KV_FP8_UNIFORM ? kFmtUniform : kFmtPacked;
+  return -1;
+}
+
+cudaError_t sparse_mla_tc_launch(const MlaArgs &a, int fmt, cudaStream_t s) {
+  if (fmt == kFmtBf16) return launch_fmt<kFmtBf16>(a, s);
+  if (fmt == kFmtUniform) return launch_fmt<kFmtUniform>(a, s);
+  return launch_fmt<kFmtPacked>(a, s);
 }
 
 }  // namespace dsa

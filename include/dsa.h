@@ -56,7 +56,11 @@ enum {
 enum {
   DSA_DEVERR_INDEX_RANGE = 1, /* an index list entry < -1 or >= the pool's rows,
                                  or a key range outside the index-k cache     */
-  DSA_DEVERR_TIMEOUT = 2      /* an internal bounded wait gave up             */
+  DSA_DEVERR_TIMEOUT = 2,     /* an internal bounded wait gave up             */
+  DSA_DEVERR_FP16_RANGE = 4   /* sparse MLA over an fp8 pool: a dequantised
+                                 value or a q element beyond fp16's finite
+                                 range (|x| > 65504); that token's output is
+                                 not valid                                     */
 };
 
 /* Indexer operand types. */
