@@ -234,25 +234,34 @@ sparse_mla_simt_kernel(MlaArgs a) {
 }
 
 // Merge split partials: one CTA per (token, head), 128 threads x 4 values.
+// The splits' lse values are staged in shared memory first, so every
+// partial-row load below is independent of the others and all are in flight
+// together (a split with no valid entry has lse = -inf and weight 0; its
+// partial row holds zeros).
+constexpr int kMaxSplits = 256;
+
 __global__ void __launch_bounds__(128)
 mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
                    int H, int Dv, int n_splits, __nv_bfloat16 *__restrict__ out,
                    float *__restrict__ lse) {
+  __shared__ float lse_s[kMaxSplits];
   const int t = blockIdx.x, h = blockIdx.y;
+  for (int i = threadIdx.x; i < n_splits; i += blockDim.x)
+    lse_s[i] = __ldcg(part_lse + ((size_t)t * n_splits + i) * H + h);
+  __syncthreads();
   float mx = -INFINITY;
-  for (int i = 0; i < n_splits; ++i)
-    mx = fmaxf(mx, part_lse[((size_t)t * n_splits + i) * H + h]);
+  for (int i = 0; i < n_splits; ++i) mx = fmaxf(mx, lse_s[i]);
   float tot = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int dv = 4 * threadIdx.x;
+#pragma unroll 8
   for (int i = 0; i < n_splits; ++i) {
-    const size_t rec = ((size_t)t * n_splits + i) * H + h;
-    const float li = part_lse[rec];
-    if (li == -INFINITY) continue;
-    const float wgt = __expf(li - mx);
+    const float li = lse_s[i];
+    const float wgt = li == -INFINITY ? 0.f : __expf(li - mx);
     tot += wgt;
     if (dv < Dv) {
-      const float4 v = *reinterpret_cast<const float4 *>(part_o + rec * Dv + dv);
+      const size_t rec = ((size_t)t * n_splits + i) * H + h;
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(part_o + rec * Dv + dv));
       acc.x = fmaf(wgt, v.x, acc.x);
       acc.y = fmaf(wgt, v.y, acc.y);
       acc.z = fmaf(wgt, v.z, acc.z);
@@ -278,6 +287,7 @@ int mla_num_splits(int T, int H, int k_total) {
   const int ctas_per_split = T * hgroups;
   int s = num_sms() / max(ctas_per_split, 1);
   s = min(s, (k_total + 63) / 64);
+  s = min(s, kMaxSplits);
   return max(s, 1);
 }
 

@@ -66,7 +66,8 @@ namespace dsa {
 
 namespace {
 
-constexpr int kThreads = 256;      // 8 warps (<= 2 per SM sub-partition: no register cap)
+// Warps 0-3 math, 4 S issue, 5 PV issue, 6.. gather: 8 warps (bf16, <= 2 per
+// SM sub-partition: no register cap) or 10 (fp8: <= 168 registers a thread).
 constexpr int kTileRows = 64;
 constexpr int kKBlockBytes = kTileRows * 128;               // 8 KB: 64 rows x 64 16-bit values
 
@@ -86,6 +87,13 @@ template <int FMT> struct FmtTraits {
   static constexpr int kLoBlocks = FMT == kFmtUniform ? kKBlocks : 0;
   static constexpr int kStages = FMT == kFmtUniform ? 1 : 2;
   static constexpr int kStageBytes = (kKBlocks + kLoBlocks) * kKBlockBytes;   // 72, 64 or 128 KB
+  // gather warps: two cp.async warps (bf16); four load-and-dequantise warps
+  // (fp8), so that every 16-byte load of a tile is in flight at once
+  static constexpr int kGatherWarps = FMT == kFmtBf16 ? 2 : 4;
+  static constexpr int kThreads = 32 * (6 + kGatherWarps);
+  // register bound: with 10 warps three share an SM sub-partition (16K
+  // registers), so at most 168 a thread -- declared as a 384-thread bound
+  static constexpr int kBoundThreads = FMT == kFmtBf16 ? 256 : 384;
   static constexpr int kQBytes = kKBlocks * 64 * 128;           // Q padded to 64 heads
 };
 constexpr float kLog2e = 1.4426950408889634f;
@@ -109,7 +117,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 struct MlaSmem {
-  uint32_t q, k, p, alpha, inv_l, flag, bars, total;
+  uint32_t q, k, p, alpha, rows, inv_l, flag, bars, total;
 };
 
 template <int FMT>
@@ -120,7 +128,8 @@ __host__ __device__ inline MlaSmem mla_smem_layout() {
   L.k = L.q + F::kQBytes;
   L.p = L.k + F::kStages * F::kStageBytes;
   L.alpha = L.p + 64 * 128;          // [2][64] rescale factors, by tile parity
-  L.inv_l = L.alpha + 2 * 64 * 4;    // [64] 1 / final sums
+  L.rows = L.alpha + 2 * 64 * 4;     // [2][64] fp8 row descriptors, by tile parity
+  L.inv_l = L.rows + (FMT == kFmtBf16 ? 0 : 2 * 64 * 16);   // [64] 1 / final sums
   L.flag = L.inv_l + 64 * 4;         // [2][4] ints, by tile parity
   L.bars = L.flag + 32;              // 8-byte aligned
   L.total = L.bars + 16 * 8;
@@ -196,6 +205,35 @@ __device__ __forceinline__ void deq16_e4m3(const uint4 v, float s, uint4 &o0, ui
   o1 = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
+// 16 e4m3 values times 2^k (a UE8M0 scale).  For k in [-15, 7] an fp16
+// product is exact and cannot overflow (|e4m3| <= 448; 2^-9 * 2^-15 = 2^-24 is
+// fp16's least subnormal), so it runs as packed half2 multiplies; other k
+// take the fp32 path with the range check.
+__device__ __forceinline__ void deq16_e4m3_pow2(const uint4 v, uint32_t e, uint4 &o0, uint4 &o1,
+                                                bool &bad) {
+  const int k = (int)e - 127;
+  if (k < -15 || k > 7) {
+    deq16_e4m3(v, ue8m0_scale(e), o0, o1, bad);
+    return;
+  }
+  const unsigned short sb = k >= -14 ? (unsigned short)((k + 15) << 10) : (unsigned short)0x0200;
+  const __half2 s2 = __half2half2(__ushort_as_half(sb));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
+          (__nv_fp8x2_storage_t)((w[i] >> (16 * hh)) & 0xffffu), __NV_E4M3);
+      const __half2 x = __hmul2(*reinterpret_cast<const __half2 *>(&r), s2);
+      h[2 * i + hh] = *reinterpret_cast<const uint32_t *>(&x);
+    }
+  }
+  o0 = make_uint4(h[0], h[1], h[2], h[3]);
+  o1 = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
 // As deq16_e4m3, and the fp16 residuals x - hi(x) as a second plane.
 __device__ __forceinline__ void deq16_e4m3_hilo(const uint4 v, float s, uint4 (&hi)[2],
                                                 uint4 (&lo)[2], bool &bad) {
@@ -233,7 +271,7 @@ __device__ __forceinline__ uint4 bf16x8_to_f16(const uint4 v, bool &bad) {
 }
 
 template <int FMT, int N>   // pool format; heads of the PV product (16, 32 or 64)
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FmtTraits<FMT>::kBoundThreads, 1)
 sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int per) {
   using F = FmtTraits<FMT>;
   constexpr int kKBlocks = F::kKBlocks;
@@ -280,7 +318,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&kfull[i], 64);
+      tc::mbar_init(&kfull[i], 32 * F::kGatherWarps);
       tc::mbar_init(&kempty[i], 1);
       tc::mbar_init(&sfull[i], 1);
       tc::mbar_init(&sempty[i], 4);
@@ -359,16 +397,21 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     __syncwarp();
   } else if (warp >= 6) {
     // -------------------------------------------------------------- gather (fp8)
-    // Lane l dequantises columns [16 l, 16 l + 16) of each row: an e4m3 word
-    // of 16 values times the scale of its 64-column group (uniform: fp32;
-    // packed: UE8M0), or -- packed, lanes 28..31 -- 16 bf16 RoPE values.
-    // Column 16 l lands in K-block l / 4, 16-byte chunks 2 (l % 4) and
-    // 2 (l % 4) + 1 of the row, swizzled by the row's phase.
-    const int half = warp - 6;
+    // A tile is a flat list of 16-byte chunks, CPR per row (uniform: 32 e4m3
+    // chunks; packed: 28 e4m3 NoPE chunks + 8 bf16 RoPE chunks); gather lane
+    // gl takes chunks gl + 128 j, issues all its loads, then dequantises them
+    // to fp16 and stores them swizzled: chunk cc of a row covers columns
+    // [16 cc, 16 cc + 16) (K-block cc / 4, 16-byte slots 2 (cc % 4) and +1),
+    // a RoPE chunk the 8 columns 448 + 8 (cc - 28) (K-block 7, slot cc - 28).
+    // Lanes 0..63 publish the tile's row addresses in shared memory first.
+    constexpr int CPR = FMT == kFmtUniform ? 32 : 36;
+    constexpr int CPL = 64 * CPR / 128;            // chunks per lane per tile
+    const int gl = threadIdx.x - 192;              // 0..127
+    Fp8Row *rtab = reinterpret_cast<Fp8Row *>(smem + L.rows);
     auto row_of = [&](int i) -> Fp8Row {
-      const int e = j0 + i * kTileRows + 32 * half + lane;
       Fp8Row r{nullptr, nullptr};
-      if (e < je) {
+      const int e = j0 + i * kTileRows + gl;
+      if (gl < 64 && e < je) {
         const int64_t slot = entry_slot(a, t, e, false);
         if (slot >= 0) r = fp8_row<FMT>(e < a.k ? a.kv : a.kv2, slot);
       }
@@ -386,69 +429,67 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         prefetch_l2(r.scale);
       }
     };
-    for (int i = 0; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);
-    const int kb = lane >> 2;
-    const uint32_t cc0 = 2u * (lane & 3);
+    for (int i = 1; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);
     bool bad = false;
     Fp8Row next = nt > 0 ? row_of(0) : Fp8Row{nullptr, nullptr};
     for (int i = 0; i < nt; ++i) {
       const int st = i % NS;
-      const Fp8Row mine = next;
       if (!tc::mbar_wait(&kempty[st], ((i / NS) & 1) ^ 1, abort_flag)) break;
+      Fp8Row *rt = rtab + (i & 1) * 64;   // by tile parity: a lane still on tile i-1 reads the other half
+      if (gl < 64) rt[gl] = next;
+      tc::named_bar_sync(2, 128);
       unsigned char *stage = k_s + st * kStageBytes;
-#pragma unroll 1
-      for (int r0 = 0; r0 < 32; r0 += 8) {
-        uint4 v0[8], v1[8];
-        float sc[8];
-        bool has[8];
+      uint4 v[CPL];
+      uint32_t sc[CPL];                   // fp32 scale bits (uniform) or UE8M0 byte (packed)
+      uint32_t has = 0;
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {        // loads of 8 rows in flight
-          const uint8_t *d = reinterpret_cast<const uint8_t *>(__shfl_sync(
-              0xffffffffu, reinterpret_cast<unsigned long long>(mine.data), r0 + b));
-          const uint8_t *sp = reinterpret_cast<const uint8_t *>(__shfl_sync(
-              0xffffffffu, reinterpret_cast<unsigned long long>(mine.scale), r0 + b));
-          has[b] = d != nullptr;
-          v0[b] = make_uint4(0u, 0u, 0u, 0u);
-          v1[b] = make_uint4(0u, 0u, 0u, 0u);
-          sc[b] = 0.f;
-          if (has[b]) {
-            if (FMT == kFmtUniform) {
-              v0[b] = __ldg(reinterpret_cast<const uint4 *>(d) + lane);
-              sc[b] = __ldg(reinterpret_cast<const float *>(sp) + kb);
-            } else if (lane < 28) {
-              v0[b] = __ldg(reinterpret_cast<const uint4 *>(d) + lane);
-              sc[b] = ue8m0_scale(__ldg(sp + kb));
-            } else {
-              const uint4 *rp = reinterpret_cast<const uint4 *>(d + 448) + 2 * (lane - 28);
-              v0[b] = __ldg(rp);
-              v1[b] = __ldg(rp + 1);
-            }
+      for (int j = 0; j < CPL; ++j) {     // every load of the tile in flight
+        const int c = gl + 128 * j;
+        const int r = c / CPR, cc = c - r * CPR;
+        const Fp8Row R = rt[r];
+        v[j] = make_uint4(0u, 0u, 0u, 0u);
+        sc[j] = 0u;
+        if (R.data) {
+          has |= 1u << j;
+          if (FMT == kFmtUniform) {
+            v[j] = __ldg(reinterpret_cast<const uint4 *>(R.data) + cc);
+            sc[j] = __ldg(reinterpret_cast<const uint32_t *>(R.scale) + (cc >> 2));
+          } else if (cc < 28) {
+            v[j] = __ldg(reinterpret_cast<const uint4 *>(R.data) + cc);
+            sc[j] = __ldg(R.scale + (cc >> 2));
+          } else {
+            v[j] = __ldg(reinterpret_cast<const uint4 *>(R.data + 448) + (cc - 28));
           }
         }
+      }
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const int r = 32 * half + r0 + b;
-          uint4 o[2], ol[2];
-          o[0] = o[1] = ol[0] = ol[1] = make_uint4(0u, 0u, 0u, 0u);
-          if (has[b]) {
-            if (FMT == kFmtUniform) {
-              deq16_e4m3_hilo(v0[b], sc[b], o, ol, bad);
-            } else if (lane < 28) {
-              deq16_e4m3(v0[b], sc[b], o[0], o[1], bad);
-            } else {
-              o[0] = bf16x8_to_f16(v0[b], bad);
-              o[1] = bf16x8_to_f16(v1[b], bad);
-            }
-          }
-          const uint32_t c0 = (cc0 ^ (uint32_t)(r & 7)) << 4, c1 = ((cc0 + 1) ^ (uint32_t)(r & 7)) << 4;
-          unsigned char *rowp = stage + kb * kKBlockBytes + r * 128;
-          *reinterpret_cast<uint4 *>(rowp + c0) = o[0];
-          *reinterpret_cast<uint4 *>(rowp + c1) = o[1];
-          if (FMT == kFmtUniform) {
-            unsigned char *lowp = rowp + kKBlocks * kKBlockBytes;
-            *reinterpret_cast<uint4 *>(lowp + c0) = ol[0];
-            *reinterpret_cast<uint4 *>(lowp + c1) = ol[1];
-          }
+      for (int j = 0; j < CPL; ++j) {
+        const int c = gl + 128 * j;
+        const int r = c / CPR, cc = c - r * CPR;
+        const uint32_t ph = (uint32_t)(r & 7);
+        const bool hv = (has >> j) & 1u;
+        if (FMT == kFmtPacked && cc >= 28) {
+          const uint4 o = hv ? bf16x8_to_f16(v[j], bad) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(stage + 7 * kKBlockBytes + r * 128 +
+                                     (((uint32_t)(cc - 28) ^ ph) << 4)) = o;
+          continue;
+        }
+        uint4 o[2], ol[2];
+        o[0] = o[1] = ol[0] = ol[1] = make_uint4(0u, 0u, 0u, 0u);
+        if (hv) {
+          if (FMT == kFmtUniform)
+            deq16_e4m3_hilo(v[j], __uint_as_float(sc[j]), o, ol, bad);
+          else
+            deq16_e4m3_pow2(v[j], sc[j], o[0], o[1], bad);
+        }
+        const uint32_t s0 = 2u * (uint32_t)(cc & 3);
+        unsigned char *rowp = stage + (cc >> 2) * kKBlockBytes + r * 128;
+        *reinterpret_cast<uint4 *>(rowp + ((s0 ^ ph) << 4)) = o[0];
+        *reinterpret_cast<uint4 *>(rowp + (((s0 + 1) ^ ph) << 4)) = o[1];
+        if (FMT == kFmtUniform) {
+          unsigned char *lowp = rowp + kKBlocks * kKBlockBytes;
+          *reinterpret_cast<uint4 *>(lowp + ((s0 ^ ph) << 4)) = ol[0];
+          *reinterpret_cast<uint4 *>(lowp + (((s0 + 1) ^ ph) << 4)) = ol[1];
         }
       }
       if (i + kPrefetchTiles < nt) prefetch_row(i + kPrefetchTiles);
@@ -741,7 +782,7 @@ cudaError_t launch_n(const MlaArgs &a, cudaStream_t s) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)a.T, (unsigned)a.n_splits, (unsigned)((a.H + 63) / 64));
-  kern<<<grid, kThreads, L.total, s>>>(a, qmap, per);
+  kern<<<grid, F::kThreads, L.total, s>>>(a, qmap, per);
   return cudaGetLastError();
 }
 
