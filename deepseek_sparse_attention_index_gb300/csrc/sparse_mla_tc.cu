@@ -66,8 +66,8 @@ namespace dsa {
 
 namespace {
 
-// Warps 0-3 math, 4 S issue, 5 PV issue, 6.. gather: 8 warps (bf16, <= 2 per
-// SM sub-partition: no register cap) or 10 (fp8: <= 168 registers a thread).
+// Warps 0-3 math, 4 S issue, 5 PV issue, 6-9 gather: 10 warps, so at most
+// 168 registers a thread (three warps share an SM sub-partition).
 constexpr int kTileRows = 64;
 constexpr int kKBlockBytes = kTileRows * 128;               // 8 KB: 64 rows x 64 16-bit values
 
@@ -87,13 +87,13 @@ template <int FMT> struct FmtTraits {
   static constexpr int kLoBlocks = FMT == kFmtUniform ? kKBlocks : 0;
   static constexpr int kStages = FMT == kFmtUniform ? 1 : 2;
   static constexpr int kStageBytes = (kKBlocks + kLoBlocks) * kKBlockBytes;   // 72, 64 or 128 KB
-  // gather warps: two cp.async warps (bf16); four load-and-dequantise warps
-  // (fp8), so that every 16-byte load of a tile is in flight at once
-  static constexpr int kGatherWarps = FMT == kFmtBf16 ? 2 : 4;
+  // gather warps: four, 16 rows each per tile (bf16: cp.async issue split
+  // four ways; fp8: every 16-byte load of a tile in flight at once)
+  static constexpr int kGatherWarps = 4;
   static constexpr int kThreads = 32 * (6 + kGatherWarps);
   // register bound: with 10 warps three share an SM sub-partition (16K
   // registers), so at most 168 a thread -- declared as a 384-thread bound
-  static constexpr int kBoundThreads = FMT == kFmtBf16 ? 256 : 384;
+  static constexpr int kBoundThreads = 384;
   static constexpr int kQBytes = kKBlocks * 64 * 128;           // Q padded to 64 heads
 };
 constexpr float kLog2e = 1.4426950408889634f;
@@ -343,11 +343,11 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
 
   if (warp >= 6 && FMT == kFmtBf16) {
     // -------------------------------------------------------------- gather (bf16)
-    const int half = warp - 6;          // rows [32*half, 32*half + 32) of every tile
-    // this lane's row of tile i (row 32*half + lane), or nullptr when masked
+    const int gw = warp - 6;            // rows [16*gw, 16*gw + 16) of every tile
+    // this lane's row of tile i (row 16*gw + lane, lanes < 16), or nullptr
     auto row_of = [&](int i) -> const uint8_t * {
-      const int e = j0 + i * kTileRows + 32 * half + lane;
-      if (e >= je) return nullptr;
+      const int e = j0 + i * kTileRows + 16 * gw + lane;
+      if (lane >= 16 || e >= je) return nullptr;
       const int64_t slot = entry_slot(a, t, e, false);
       if (slot < 0) return nullptr;
       return (e < a.k ? a.kv.data : a.kv2.data) + slot * (int64_t)1152;
@@ -361,19 +361,19 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         for (int c = 0; c < 9; ++c) prefetch_l2(row + 128 * c);
       }
     };
-    for (int i = 0; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);
+    for (int i = 1; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);   // tile 0 is copied at once
     const uint8_t *next = nt > 0 ? row_of(0) : nullptr;
     for (int i = 0; i < nt; ++i) {
       const int st = i % NS;
       const uint8_t *my_row = next;
       if (!tc::mbar_wait(&kempty[st], ((i / NS) & 1) ^ 1, abort_flag)) break;
       const uint32_t sbase = tc::smem_u32(k_s + st * kStageBytes);
-#pragma unroll 1
-      for (int r0 = 32 * half; r0 < 32 * half + 32; r0 += 8) {
+#pragma unroll
+      for (int r0 = 16 * gw; r0 < 16 * gw + 16; r0 += 8) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {       // row r0 + j: swizzle phase j
           const uint8_t *row = reinterpret_cast<const uint8_t *>(__shfl_sync(
-              0xffffffffu, reinterpret_cast<unsigned long long>(my_row), (r0 & 31) + j));
+              0xffffffffu, reinterpret_cast<unsigned long long>(my_row), (r0 & 15) + j));
           const uint8_t *src = row ? row : static_cast<const uint8_t *>(a.q);   // not read when masked
           const uint32_t nbytes = row ? 16u : 0u;
           const uint32_t rdst = sbase + (r0 + j) * 128;
@@ -429,7 +429,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         prefetch_l2(r.scale);
       }
     };
-    for (int i = 1; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);
+    for (int i = 1; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);   // tile 0 is loaded at once
     bool bad = false;
     Fp8Row next = nt > 0 ? row_of(0) : Fp8Row{nullptr, nullptr};
     for (int i = 0; i < nt; ++i) {
@@ -504,7 +504,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     if (lane == 0) {
       // S = Q K^T: A = Q (K-major, M = 64), B = K tile (K-major, N = 64)
       constexpr uint32_t idesc_s = tc::idesc_f32acc(F::kOpType, F::kOpType, 0, 0, 64, 64);
-      const uint32_t q_addr = tc::smem_u32(q_s);
+      const uint64_t adq = tc::sdesc_sw128(tc::smem_u32(q_s), 16, 1024);
       bool ok = nt == 0 || tc::mbar_wait(FMT == kFmtBf16 ? qfull : qready, 0, abort_flag);
       for (int i = 0; i < nt && ok; ++i) {
         const int st = i % NS;              // K stage
@@ -512,21 +512,21 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         if (!tc::mbar_wait(&kfull[st], (i / NS) & 1, abort_flag)) break;
         if (!tc::mbar_wait(&sempty[sb], ((i >> 1) & 1) ^ 1, abort_flag)) break;
         tc::fence_after_sync();
-        const uint32_t k_addr = tc::smem_u32(k_s + st * kStageBytes);
-#pragma unroll 1
+        // descriptors: the start-address field is the byte address / 16, so
+        // a K-block (8192 B) adds 512 and 32 bytes of K add 2
+        const uint64_t bdk = tc::sdesc_sw128(tc::smem_u32(k_s + st * kStageBytes), 16, 1024);
+        const uint32_t dcol = tmem + kSCol + sb * 64;
+#pragma unroll
         for (int kb = 0; kb < kKBlocks; ++kb) {
-          const uint64_t ad0 = tc::sdesc_sw128(q_addr + kb * kKBlockBytes, 16, 1024);
-          const uint64_t bd0 = tc::sdesc_sw128(k_addr + kb * kKBlockBytes, 16, 1024);
 #pragma unroll
           for (int ko = 0; ko < 4; ++ko)   // 32 bytes (16 values) of K per instruction
-            tc::mma_f16(tmem + kSCol + sb * 64, ad0 + 2 * ko, bd0 + 2 * ko, idesc_s,
+            tc::mma_f16(dcol, adq + kb * 512 + 2 * ko, bdk + kb * 512 + 2 * ko, idesc_s,
                         (kb > 0 || ko > 0) ? 1u : 0u);
           if (F::kLoBlocks > 0) {          // the low plane of the same K-block
-            const uint64_t bl0 =
-                tc::sdesc_sw128(k_addr + (kKBlocks + kb) * kKBlockBytes, 16, 1024);
 #pragma unroll
             for (int ko = 0; ko < 4; ++ko)
-              tc::mma_f16(tmem + kSCol + sb * 64, ad0 + 2 * ko, bl0 + 2 * ko, idesc_s, 1u);
+              tc::mma_f16(dcol, adq + kb * 512 + 2 * ko,
+                          bdk + (kKBlocks + kb) * 512 + 2 * ko, idesc_s, 1u);
           }
         }
         tc::mma_commit(&sfull[sb]);
@@ -555,16 +555,19 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         if (!tc::mbar_wait(pfull, i & 1, abort_flag)) break;
         tc::fence_after_sync();
         const uint32_t k_addr = tc::smem_u32(k_s + st * kStageBytes);
-        const uint32_t plo_addr = k_addr + 8 * kKBlockBytes;   // bf16: P_lo in the RoPE block
-#pragma unroll 1
+        // A = V^T: dv block j is K-blocks 2j, 2j+1 (+1024 in the descriptor),
+        // 16 kv rows = 2048 B (+128); B = P (or P_lo, bf16: the RoPE block),
+        // 16 kv = 32 B (+2)
+        const uint64_t adv = tc::sdesc_sw128(k_addr, kKBlockBytes, 1024);
+        const uint64_t bdp = tc::sdesc_sw128(p_addr, 16, 1024);
+        const uint64_t bdl = tc::sdesc_sw128(k_addr + 8 * kKBlockBytes, 16, 1024);
+#pragma unroll
         for (int j = 0; j < 4; ++j) {
 #pragma unroll
           for (int kk = 0; kk < F::kPvSteps; ++kk) {
             const uint32_t kr = kk & 3;   // 16 kv rows per instruction
-            const uint64_t ad = tc::sdesc_sw128(k_addr + (2 * j) * kKBlockBytes + kr * 2048,
-                                                kKBlockBytes, 1024);
-            const uint64_t bd = tc::sdesc_sw128((kk < 4 ? p_addr : plo_addr) + kr * 32, 16, 1024);
-            tc::mma_f16(tmem + kOCol + j * N, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_f16(tmem + kOCol + j * N, adv + j * 1024 + kr * 128,
+                        (kk < 4 ? bdp : bdl) + kr * 2, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
           }
         }
         tc::mma_commit(&kempty[st]);
@@ -645,7 +648,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       // p = exp2(x - m), its sum, and the P row in two bf16 terms
       const float msafe = m == -INFINITY ? 0.f : m;   // all masked so far: p = 0
       float ps = 0.f;
-      uint32_t phi[32], plo[32];
+      uint32_t phi[32], plo[4];
 #pragma unroll
       for (int j = 0; j < 64; j += 2) {
         const float x0 = j < 32 ? xa[j] : xb[j - 32];
@@ -657,11 +660,18 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
           const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
           const float2 hf = __bfloat1622float2(hi);
           phi[j / 2] = *reinterpret_cast<const uint32_t *>(&hi);
-          plo[j / 2] = pack_bf16x2(p0 - hf.x, p1 - hf.y);
+          plo[(j / 2) & 3] = pack_bf16x2(p0 - hf.x, p1 - hf.y);
+          if ((j & 7) == 6 && head_lane && hl < N) {
+            // P_lo goes straight into this tile's RoPE block (free once S(i)
+            // has read it; PV(i-1) never reads it): 8 kv = one 16-byte chunk
+            const int ch = j >> 3;
+            *reinterpret_cast<uint4 *>(k_s + (i % NS) * kStageBytes + 8 * kKBlockBytes + hl * 128 +
+                                       ((ch ^ (hl & 7)) << 4)) =
+                make_uint4(plo[0], plo[1], plo[2], plo[3]);
+          }
         } else {
           const __half2 ph = __floats2half2_rn(p0, p1);   // p <= 256: 2^-11 relative
           phi[j / 2] = *reinterpret_cast<const uint32_t *>(&ph);
-          plo[j / 2] = 0u;
         }
       }
       l = l * al + ps;
@@ -676,15 +686,11 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       }
       if (head_lane && hl < N) {
         // row hl of P (K-major B operand): 64 kv 16-bit values = 128 bytes, swizzled
-        unsigned char *plo_s = k_s + (i % NS) * kStageBytes + 8 * kKBlockBytes;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           const uint32_t off = hl * 128 + ((ch ^ (hl & 7)) << 4);
           *reinterpret_cast<uint4 *>(p_s + off) =
               make_uint4(phi[4 * ch], phi[4 * ch + 1], phi[4 * ch + 2], phi[4 * ch + 3]);
-          if (FMT == kFmtBf16)
-            *reinterpret_cast<uint4 *>(plo_s + off) =
-                make_uint4(plo[4 * ch], plo[4 * ch + 1], plo[4 * ch + 2], plo[4 * ch + 3]);
         }
       }
       tc::fence_proxy_async_smem();
