@@ -53,6 +53,15 @@ DSA_DEVINLINE uint32_t score_key(float x) {
 
 DSA_DEVINLINE unsigned lane_id() { return threadIdx.x & 31; }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start
+// while the previous kernel on the stream is still running; pdl_wait() blocks
+// until that kernel has completed and its writes are visible, so everything
+// that reads its results comes after pdl_wait().  pdl_trigger() lets this
+// kernel's own dependent launch early (it still waits for us to finish).
+// Both are no-ops for a kernel launched without the attribute.
+DSA_DEVINLINE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DSA_DEVINLINE void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Pack two floats to a bf16x2 word (round to nearest even), low half = a.
 DSA_DEVINLINE uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -81,6 +90,23 @@ struct WsCarver {
   }
   size_t bytes() const { return align_up(off, 256); }
 };
+
+// Launch with the programmatic-stream-serialization attribute (see pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 inline int num_sms() {
   static int n = 0;

@@ -241,6 +241,7 @@ int dsa_decode(const void *q_idx, int idx_dtype, const float *q_scale, const voi
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   MlaArgs a{};
   a.q = q; a.T = B; a.H = H; a.D = D; a.Dv = Dv; a.softmax_scale = softmax_scale;
+  a.q_ready = 1;   // q precedes the whole fused call on the stream
   a.kv = to_dev(kv); a.idx = idx; a.k = k;
   a.kv2 = to_dev(k_swa > 0 ? kv_swa : nullptr); a.idx2 = k_swa > 0 ? idx_swa : nullptr;
   a.k2 = k_swa;

@@ -147,6 +147,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();   // the next kernel may be placed as SMs free up; it waits for us
 
   const int64_t total = (int64_t)a.T * tiles_per_row;
   const int64_t v0 = (int64_t)blockIdx.x * tiles_per_cta;

@@ -15,7 +15,7 @@ constexpr int kMinChunk = 2048;   // smallest run of positions one collect CTA c
 
 struct TopkWs {
   uint32_t *hist;    // [T][kHistBins]        zeroed before the histogram pass
-  uint32_t *cnt;     // [T][4] (list entries, -, CTAs done, -), zeroed before the collect pass
+  uint32_t *cnt;     // [T][4]: list entries, -, then one u64 (entries | CTAs done << 32); zeroed before the collect pass
   uint2 *list;       // [T][kListCap]  (key, position): the row's runs, one per collect CTA
   uint2 *tab;        // [T][max_chunks] (run start, run length) by chunk
   int max_chunks;    // ceil(max_len / kMinChunk)
@@ -79,6 +79,8 @@ struct MlaArgs {
   float *part_lse;
   int n_splits;
   int32_t *err_flag;
+  int q_ready;               // q was complete before the previous kernel on the stream
+                             // began (fused decode): the kernel may load it before pdl_wait
 };
 int mla_num_splits(int T, int H, int k_total);
 size_t mla_ws_bytes(int T, int H, int Dv, int k_total);

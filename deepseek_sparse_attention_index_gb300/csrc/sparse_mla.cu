@@ -245,6 +245,7 @@ mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ p
                    int H, int Dv, int n_splits, __nv_bfloat16 *__restrict__ out,
                    float *__restrict__ lse) {
   __shared__ float lse_s[kMaxSplits];
+  pdl_wait();      // the partials come from the previous kernel
   const int t = blockIdx.x, h = blockIdx.y;
   for (int i = threadIdx.x; i < n_splits; i += blockDim.x)
     lse_s[i] = __ldcg(part_lse + ((size_t)t * n_splits + i) * H + h);
@@ -330,9 +331,9 @@ cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_splits == 1) return e;
-  mla_combine_kernel<<<dim3((unsigned)a.T, (unsigned)a.H), 128, 0, s>>>(
-      a.part_o, a.part_lse, a.H, a.Dv, a.n_splits, static_cast<__nv_bfloat16 *>(a.out), a.lse);
-  return cudaGetLastError();
+  return launch_pdl(mla_combine_kernel, dim3((unsigned)a.T, (unsigned)a.H), dim3(128), 0, s,
+                    (const float *)a.part_o, (const float *)a.part_lse, a.H, a.Dv, a.n_splits,
+                    static_cast<__nv_bfloat16 *>(a.out), a.lse);
 }
 
 }  // namespace dsa

@@ -340,6 +340,19 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // Q of this head group: 64-column boxes of 64 heads (heads past H lie
+  // outside the map and read as zeros).  In the fused decode q precedes the
+  // whole call, so it is loaded before waiting for the top-k kernel.
+  auto load_q = [&]() {
+    tc::prefetch_tmap(&qmap);
+    tc::mbar_arrive_expect_tx(qfull, F::kQBytes);
+    for (int kb = 0; kb < kKBlocks; ++kb)
+      tc::tma_load_3d(&qmap, qfull, q_s + kb * kKBlockBytes, kb * 64, h0, t);
+  };
+  if (warp == 5 && lane == 0 && a.q_ready) load_q();
+  pdl_wait();      // the index lists come from the previous kernel
+  pdl_trigger();
+  if (warp == 5 && lane == 0 && !a.q_ready) load_q();
 
   if (warp >= 6 && FMT == kFmtBf16) {
     // -------------------------------------------------------------- gather (bf16)
@@ -541,12 +554,6 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   } else if (warp == 5) {
     // -------------------------------------------------------------- PV issue
     if (lane == 0) {
-      tc::prefetch_tmap(&qmap);
-      // Q of this head group: 64-column boxes of 64 heads (heads past H lie
-      // outside the map and read as zeros)
-      tc::mbar_arrive_expect_tx(qfull, F::kQBytes);
-      for (int kb = 0; kb < kKBlocks; ++kb)
-        tc::tma_load_3d(&qmap, qfull, q_s + kb * kKBlockBytes, kb * 64, h0, t);
       // O^T += V^T P^T: A = V^T (MN-major, M = 128), B = P (K-major, N heads)
       constexpr uint32_t idesc_pv = tc::idesc_f32acc(F::kOpType, F::kOpType, 1, 0, N, 128);
       const uint32_t p_addr = tc::smem_u32(p_s);
@@ -788,8 +795,7 @@ cudaError_t launch_n(const MlaArgs &a, cudaStream_t s) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)a.T, (unsigned)a.n_splits, (unsigned)((a.H + 63) / 64));
-  kern<<<grid, F::kThreads, L.total, s>>>(a, qmap, per);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(F::kThreads), L.total, s, a, qmap, per);
 }
 
 template <int FMT>

@@ -42,7 +42,7 @@ constexpr int kRounds = 2;                  // a chunk is one or two rounds
 constexpr int kMaxChunk = kRound * kRounds; // 16384
 constexpr int kGather = 8;                  // entries per thread per compaction round
 constexpr int kBatch = 8;                   // list entries a thread loads at once
-constexpr int kEqCache = 3072;              // bin-b1 entries the resolve keeps in shared memory (static smem < 48 KB)
+constexpr int kListCache = 6144;            // list entries the resolve copies into (dynamic) shared memory
 constexpr int kHistThreads = 512;
 static_assert(kHistBins == 8 * kThreads, "threshold_bin gives each thread 8 bins");
 
@@ -230,16 +230,22 @@ topk_hist_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__
 }
 
 
-// Where the resolve pass reads a row's (key, position) pairs: the list (the
-// entries at or above bin b1, in runs by chunk) or -- after an overflow --
-// the row itself.  Other CTAs wrote the list, so it is read through L2.
+// Where the resolve pass reads a row's (key, position) pairs: the list in
+// shared memory (copied by the first pass when it fits), the list in global
+// memory (written by other CTAs, so read through L2), or -- after an
+// overflow -- the row itself.
 struct Source {
+  const uint2 *cache;   // shared copy of the list, or nullptr
   const uint2 *list;
   const float *row;
-  int64_t n;        // list length, or the row length when reading the row
+  int64_t n;            // list length, or the row length when reading the row
   bool from_row;
   __device__ __forceinline__ void get(int64_t i, uint32_t &key, int32_t &pos) const {
-    if (!from_row) {
+    if (cache) {
+      const uint2 c = cache[i];
+      key = c.x;
+      pos = (int32_t)c.y;
+    } else if (!from_row) {
       const uint2 c = __ldcg(list + i);
       key = c.x;
       pos = (int32_t)c.y;
@@ -254,31 +260,30 @@ struct ResolveSmem {
   uint32_t sh[kHistBins];
   uint32_t run_pre[kThreads];    // ordered start of each run of a group of chunks
   uint32_t run_at[kThreads];     // where that run sits in the list
-  uint2 eq[kEqCache];            // the bin-b1 (key, position) pairs, when they fit
-  uint32_t n_eq;
   uint32_t warp_sums[32];
   int s_bin;
   uint32_t s_before;
 };
 
-// Resolves row t once its collect pass is complete (b1 and n_gt = the count
-// above bin b1 come from the caller's threshold_bin): two more radix levels
-// over the bin-b1 entries give the exact k-th key K*, a radix select over
-// positions breaks ties toward lower positions, and an ordered compaction
-// writes the k survivors in ascending position order.  Run by one whole CTA
-// of kThreads threads.
-__device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uint32_t n_gt,
+// Resolves row t once its collect pass is complete.  b1 and n_gt (the count
+// above bin b1) come from the caller's threshold_bin, n_list (entries at or
+// above bin b1) from the done counter.  Two more radix levels over the
+// bin-b1 entries give the exact k-th key K*, a radix select over positions
+// breaks ties toward lower positions, and an ordered compaction writes the k
+// survivors in ascending position order.  The first pass copies the list
+// into `lc` (kListCache entries of dynamic shared memory) when it fits, so
+// the later passes read shared memory.  Run by one whole CTA of kThreads.
+__device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint32_t b1,
+                                         uint32_t n_gt, uint32_t n_list,
                                          const float *__restrict__ scores, int64_t ld, int64_t L,
                                          int k, int chunk, int max_chunks,
                                          const int32_t *__restrict__ index_base,
-                                         const uint32_t *__restrict__ cnt,
                                          const uint2 *__restrict__ list,
                                          const uint2 *__restrict__ tab, int32_t *__restrict__ idx,
                                          int32_t *__restrict__ lens, int32_t *err_flag) {
   uint32_t *sh = S.sh;
   const int32_t base = index_base ? index_base[t] : 0;
   int32_t *out = idx + (size_t)t * k;
-  const uint32_t n_list = __ldcg(cnt + 4 * t);   // entries at or above bin b1
   if (n_gt >= (uint32_t)k || n_list < (uint32_t)k) {
     // histogram and scores disagree (a histogram of other scores, or NaNs)
     if (threadIdx.x == 0) raise_flag(err_flag, DSA_DEVERR_INDEX_RANGE);
@@ -287,19 +292,22 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
     return;
   }
   Source src;
+  src.cache = nullptr;
   src.list = list + (size_t)t * kListCap;
   src.row = scores + (int64_t)t * ld;
   src.from_row = n_list > (uint32_t)kListCap;
   src.n = src.from_row ? L : (int64_t)n_list;
+  const bool to_cache = !src.from_row && n_list <= (uint32_t)kListCache;
   const uint32_t r1 = (uint32_t)k - n_gt;  // to take from bin b1
+  const int nch = (int)((L + chunk - 1) / chunk);
+  const uint2 *rt = tab + (size_t)t * max_chunks;
+  // the first group of the chunk table, loaded now, used by the compaction
+  uint2 run0 = make_uint2(0u, 0u);
+  if (!src.from_row && (int)threadIdx.x < min(nch, kThreads)) run0 = __ldcg(rt + threadIdx.x);
 
-  // level 2: bits 19..8 of the bin-b1 keys.  The same pass keeps the bin-b1
-  // pairs in shared memory (a warp reserves its slots with one atomic), so
-  // the later passes read the list again only when they do not fit.
+  // level 2: bits 19..8 of the bin-b1 keys; the same pass copies the list
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
-  if (threadIdx.x == 0) S.n_eq = 0;
   __syncthreads();
-  const unsigned lane = lane_id();
   for (int64_t i0 = 0; i0 < src.n; i0 += (int64_t)kBatch * kThreads) {
     uint32_t key[kBatch];
     int32_t pos[kBatch];
@@ -310,48 +318,17 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
       pos[j] = -1;                       // -1: past the end
       if (i < src.n) src.get(i, key[j], pos[j]);
     }
-    unsigned ball[kBatch];
-    uint32_t n_warp = 0;
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      const bool in = pos[j] >= 0 && (key[j] >> 20) == b1;
-      if (in) atomicAdd(&sh[(key[j] >> 8) & 0xFFFu], 1u);
-      ball[j] = __ballot_sync(0xffffffffu, in);
-      n_warp += (uint32_t)__popc(ball[j]);
-    }
-    if (n_warp) {
-      uint32_t slot = 0;
-      if (lane == 0) slot = atomicAdd(&S.n_eq, n_warp);
-      slot = __shfl_sync(0xffffffffu, slot, 0);
-      const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        if ((ball[j] >> lane) & 1u) {
-          const uint32_t at = slot + (uint32_t)__popc(ball[j] & lt);
-          if (at < (uint32_t)kEqCache) S.eq[at] = make_uint2(key[j], (uint32_t)pos[j]);
-        }
-        slot += (uint32_t)__popc(ball[j]);
+      const int64_t i = i0 + (int64_t)j * kThreads + threadIdx.x;
+      if (pos[j] >= 0) {
+        if (to_cache) lc[i] = make_uint2(key[j], (uint32_t)pos[j]);
+        if ((key[j] >> 20) == b1) atomicAdd(&sh[(key[j] >> 8) & 0xFFFu], 1u);
       }
     }
   }
   __syncthreads();
-  const uint32_t n_eq = S.n_eq;
-  const bool cached = n_eq <= (uint32_t)kEqCache;
-  // calls f(key, pos) for every bin-b1 pair, from shared memory when cached
-  auto for_each_eq = [&](auto f) {
-    if (cached) {
-      for (uint32_t i = threadIdx.x; i < n_eq; i += blockDim.x) {
-        const uint2 e = S.eq[i];
-        f(e.x, (int32_t)e.y);
-      }
-    } else {
-      for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
-        uint32_t key; int32_t pos;
-        src.get(i, key, pos);
-        if ((key >> 20) == b1) f(key, pos);
-      }
-    }
-  };
+  if (to_cache) src.cache = lc;
   find_bin(sh, kHistBins, r1, true, S.warp_sums, &S.s_bin, &S.s_before);
   const uint32_t b2 = (uint32_t)S.s_bin;
   const uint32_t r2 = r1 - S.s_before;
@@ -360,9 +337,11 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
   // level 3: bits 7..0 among keys whose bits 31..8 are hi20
   for (int i = threadIdx.x; i < kThreads; i += blockDim.x) sh[i] = 0;
   __syncthreads();
-  for_each_eq([&](uint32_t key, int32_t) {
+  for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
+    uint32_t key; int32_t pos;
+    src.get(i, key, pos);
     if ((key >> 8) == hi20) atomicAdd(&sh[key & 0xFFu], 1u);
-  });
+  }
   __syncthreads();
   // 256 bins padded with zero bins to the block size; walking down from the
   // top passes the zero bins first
@@ -385,13 +364,15 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
       __syncthreads();
       for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
       __syncthreads();
-      for_each_eq([&](uint32_t key, int32_t pos) {
+      for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
+        uint32_t key; int32_t pos;
+        src.get(i, key, pos);
         if (key == kstar) {
           const uint32_t p = (uint32_t)pos;
           const uint32_t hi_bits = lvl == 0 ? 0u : (p >> (sft + widths[lvl]));
           if (hi_bits == prefix) atomicAdd(&sh[(p >> sft) & (nb - 1)], 1u);
         }
-      });
+      }
       __syncthreads();
       // ascending walk over max(nb, blockDim) bins (extra bins are zero)
       const int nbins = (int)max(nb, (uint32_t)blockDim.x);
@@ -429,13 +410,11 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
       written += tot;
     }
   } else {
-    const int nch = (int)((L + chunk - 1) / chunk);
-    const uint2 *rt = tab + (size_t)t * max_chunks;
     for (int g0 = 0; g0 < nch; g0 += kThreads) {
       // the runs of chunks g0 .. g0 + ng - 1, their ordered starts by a block scan
       const int ng = min(kThreads, nch - g0);
-      uint2 run = make_uint2(0u, 0u);
-      if ((int)threadIdx.x < ng) run = __ldcg(rt + g0 + threadIdx.x);
+      uint2 run = g0 == 0 ? run0 : make_uint2(0u, 0u);
+      if (g0 > 0 && (int)threadIdx.x < ng) run = __ldcg(rt + g0 + threadIdx.x);
       uint32_t n_group;
       const uint32_t pre = block_excl_scan(run.y, S.warp_sums, &n_group);
       S.run_pre[threadIdx.x] = pre;
@@ -470,7 +449,9 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint32_t b1, uin
         uint2 e[kGather];
 #pragma unroll
         for (int j = 0; j < kGather; ++j)
-          e[j] = at[j] != 0xffffffffu ? __ldcg(src.list + at[j]) : make_uint2(0u, 0u);
+          e[j] = at[j] == 0xffffffffu ? make_uint2(0u, 0u)
+                 : src.cache    ? src.cache[at[j]]
+                                : __ldcg(src.list + at[j]);
         uint32_t m = 0;
         int32_t posv[kGather];
 #pragma unroll
@@ -515,6 +496,10 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
   __shared__ ResolveSmem S;
   __shared__ uint32_t s_base;
   __shared__ int s_last;
+  __shared__ uint32_t s_total;
+  extern __shared__ uint2 list_cache[];   // kListCache entries, used by the resolving CTA
+  pdl_wait();      // scores and histogram come from the previous kernel
+  pdl_trigger();
   const int t = blockIdx.y;
   const int64_t L = max(row_len[t], 0);
   if (L <= k) {                     // every position is selected: no search
@@ -579,10 +564,10 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
   uint32_t tot;
   const uint32_t pre = block_excl_scan(packed, S.warp_sums, &tot);
   const uint32_t tot0 = tot & 0xffffu;
+  const uint32_t n_cta = tot0 + (tot >> 16);
   if (threadIdx.x == 0) {
-    const uint32_t n = tot0 + (tot >> 16);
-    s_base = n ? atomicAdd(&cnt[4 * t], n) : 0u;
-    tab[(size_t)t * max_chunks + blockIdx.x] = make_uint2(s_base, n);
+    s_base = n_cta ? atomicAdd(&cnt[4 * t], n_cta) : 0u;
+    tab[(size_t)t * max_chunks + blockIdx.x] = make_uint2(s_base, n_cta);
   }
   __syncthreads();
   uint2 *cl = list + (size_t)t * kListCap;
@@ -602,14 +587,19 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    // one 64-bit word per row: CTAs done (high half) and entries appended
+    // (low half), so the last CTA learns the row's total from its own atomic
     const uint32_t nch = (uint32_t)((L + chunk - 1) / chunk);
-    s_last = atomicAdd(&cnt[4 * t + 2], 1u) == nch - 1;
+    const unsigned long long old = atomicAdd(
+        reinterpret_cast<unsigned long long *>(cnt + 4 * t + 2), (1ull << 32) | n_cta);
+    s_last = (uint32_t)(old >> 32) == nch - 1;
+    s_total = (uint32_t)old + n_cta;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  resolve_row(t, S, b1, n_gt, scores, ld, L, k, chunk, max_chunks, index_base, cnt, list, tab, idx,
-              lens, err_flag);
+  resolve_row(t, S, list_cache, b1, n_gt, s_total, scores, ld, L, k, chunk, max_chunks,
+              index_base, list, tab, idx, lens, err_flag);
 }
 
 // Positions per collect CTA: the smallest power of two in [kMinChunk,
@@ -629,8 +619,8 @@ size_t topk_ws_layout(int T, int64_t max_len, int k, void *ws, TopkWs *out) {
   WsCarver c(ws);
   TopkWs w;
   w.max_chunks = (int)std::max<int64_t>(1, (max_len + kMinChunk - 1) / kMinChunk);
-  w.hist = c.take<uint32_t>((size_t)T * kHistBins);
-  w.cnt = c.take<uint32_t>((size_t)T * 4);   // list entries, -, CTAs done, -
+  w.hist = c.take<uint32_t>((size_t)T * kHistBins);   // hist then cnt, adjacent (one memset clears both)
+  w.cnt = c.take<uint32_t>((size_t)T * 4);   // list entries, -, (entries | CTAs done << 32) as u64
   w.list = c.take<uint2>((size_t)T * kListCap);
   w.tab = c.take<uint2>((size_t)T * w.max_chunks);
   if (out) *out = w;
@@ -638,9 +628,9 @@ size_t topk_ws_layout(int T, int64_t max_len, int k, void *ws, TopkWs *out) {
 }
 
 cudaError_t topk_clear(const TopkWs &w, int T, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(w.hist, 0, sizeof(uint32_t) * (size_t)T * kHistBins, s);
-  if (e != cudaSuccess) return e;
-  return cudaMemsetAsync(w.cnt, 0, sizeof(uint32_t) * (size_t)T * 4, s);
+  // hist and cnt are adjacent in the workspace (topk_ws_layout): one memset
+  const char *end = reinterpret_cast<const char *>(w.cnt + (size_t)T * 4);
+  return cudaMemsetAsync(w.hist, 0, (size_t)(end - reinterpret_cast<const char *>(w.hist)), s);
 }
 
 cudaError_t topk_hist(const float *scores, int64_t ld, const int32_t *row_len, int T,
@@ -659,10 +649,13 @@ cudaError_t topk_select(const float *scores, int64_t ld, const int32_t *row_len,
   const int64_t nch = max_len > k ? (max_len + chunk - 1) / chunk : 1;
   if (nch > w.max_chunks) return cudaErrorInvalidValue;
   dim3 grid((unsigned)nch, (unsigned)T);
-  topk_collect_kernel<<<grid, kThreads, 0, s>>>(scores, ld, row_len, k, chunk, w.max_chunks,
-                                                index_base, w.hist, w.cnt, w.list, w.tab, idx,
-                                                lens, err_flag);
-  return cudaGetLastError();
+  const size_t dyn = sizeof(uint2) * kListCache;
+  cudaError_t e = cudaFuncSetAttribute(topk_collect_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(topk_collect_kernel, grid, dim3(kThreads), dyn, s, scores, ld, row_len, k,
+                    chunk, w.max_chunks, index_base, (const uint32_t *)w.hist, w.cnt, w.list,
+                    w.tab, idx, lens, err_flag);
 }
 
 }  // namespace dsa
