@@ -205,11 +205,13 @@ __device__ __forceinline__ void load16(const float *row, int64_t base, int64_t h
 
 __global__ void __launch_bounds__(kHistThreads)
 topk_hist_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restrict__ row_len,
-                 int k, int chunk, uint32_t *__restrict__ hist) {
+                 int k, int chunk, int nch, uint32_t *__restrict__ hist) {
   __shared__ uint32_t sh[kHistBins];
-  const int t = blockIdx.y;
+  // 1-D grid of rows x chunks (a 2-D grid would cap the rows at 65535)
+  const int t = (int)(blockIdx.x / (unsigned)nch);
+  const int c = (int)(blockIdx.x - (unsigned)t * (unsigned)nch);
   const int64_t L = max(row_len[t], 0);
-  const int64_t lo = (int64_t)blockIdx.x * chunk;
+  const int64_t lo = (int64_t)c * chunk;
   if (L <= k || lo >= L) return;
   const int64_t hi = min(L, lo + chunk);
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
@@ -488,7 +490,7 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
 // packed two-round block scan places every entry of the CTA's run.
 __global__ void __launch_bounds__(kThreads, 2)
 topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
-                    const int32_t *__restrict__ row_len, int k, int chunk, int max_chunks,
+                    const int32_t *__restrict__ row_len, int k, int chunk, int nch, int max_chunks,
                     const int32_t *__restrict__ index_base, const uint32_t *__restrict__ hist,
                     uint32_t *__restrict__ cnt, uint2 *__restrict__ list,
                     uint2 *__restrict__ tab, int32_t *__restrict__ idx,
@@ -500,10 +502,12 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
   extern __shared__ uint2 list_cache[];   // kListCache entries, used by the resolving CTA
   pdl_wait();      // scores and histogram come from the previous kernel
   pdl_trigger();
-  const int t = blockIdx.y;
+  // 1-D grid of rows x chunks (a 2-D grid would cap the rows at 65535)
+  const int t = (int)(blockIdx.x / (unsigned)nch);
+  const int c = (int)(blockIdx.x - (unsigned)t * (unsigned)nch);
   const int64_t L = max(row_len[t], 0);
   if (L <= k) {                     // every position is selected: no search
-    if (blockIdx.x == 0) {
+    if (c == 0) {
       const int32_t base = index_base ? index_base[t] : 0;
       int32_t *out = idx + (size_t)t * k;
       for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < L ? (int32_t)j + base : -1;
@@ -511,7 +515,7 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
     }
     return;
   }
-  const int64_t lo = (int64_t)blockIdx.x * chunk;
+  const int64_t lo = (int64_t)c * chunk;
   if (lo >= L) return;
   const int64_t hi = min(L, lo + chunk);
   const float *row = scores + (int64_t)t * ld;
@@ -567,7 +571,7 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
   const uint32_t n_cta = tot0 + (tot >> 16);
   if (threadIdx.x == 0) {
     s_base = n_cta ? atomicAdd(&cnt[4 * t], n_cta) : 0u;
-    tab[(size_t)t * max_chunks + blockIdx.x] = make_uint2(s_base, n_cta);
+    tab[(size_t)t * max_chunks + c] = make_uint2(s_base, n_cta);
   }
   __syncthreads();
   uint2 *cl = list + (size_t)t * kListCap;
@@ -637,8 +641,10 @@ cudaError_t topk_hist(const float *scores, int64_t ld, const int32_t *row_len, i
                       int64_t max_len, int k, const TopkWs &w, cudaStream_t s) {
   if (max_len <= k) return cudaSuccess;
   const int chunk = collect_chunk(T, max_len);
-  dim3 grid((unsigned)((max_len + chunk - 1) / chunk), (unsigned)T);
-  topk_hist_kernel<<<grid, kHistThreads, 0, s>>>(scores, ld, row_len, k, chunk, w.hist);
+  const int64_t nch = (max_len + chunk - 1) / chunk;
+  if (nch * T >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
+  topk_hist_kernel<<<(unsigned)(nch * T), kHistThreads, 0, s>>>(scores, ld, row_len, k, chunk,
+                                                                  (int)nch, w.hist);
   return cudaGetLastError();
 }
 
@@ -648,13 +654,14 @@ cudaError_t topk_select(const float *scores, int64_t ld, const int32_t *row_len,
   const int chunk = collect_chunk(T, max_len);
   const int64_t nch = max_len > k ? (max_len + chunk - 1) / chunk : 1;
   if (nch > w.max_chunks) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)nch, (unsigned)T);
+  if (nch * T >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
+  const dim3 grid((unsigned)(nch * T));
   const size_t dyn = sizeof(uint2) * kListCache;
   cudaError_t e = cudaFuncSetAttribute(topk_collect_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
   return launch_pdl(topk_collect_kernel, grid, dim3(kThreads), dyn, s, scores, ld, row_len, k,
-                    chunk, w.max_chunks, index_base, (const uint32_t *)w.hist, w.cnt, w.list,
+                    chunk, (int)nch, w.max_chunks, index_base, (const uint32_t *)w.hist, w.cnt, w.list,
                     w.tab, idx, lens, err_flag);
 }
 

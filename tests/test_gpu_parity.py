@@ -141,6 +141,22 @@ def test_topk_random_fp32_many_rows():
         assert np.array_equal(idx[t, :n], np.sort(ref[:n]))
 
 
+def test_topk_more_rows_than_a_grid_dimension():
+    # 65537 rows (prefill at 64K tokens has as many): rows and chunks share
+    # one grid dimension, so the row count is not capped at 65535
+    rng = np.random.default_rng(7)
+    T, k = 65537, 8
+    lens = rng.integers(0, 40, T)
+    rows = [(np.round(rng.standard_normal(int(L)) * 4) / 4).astype(np.float32) for L in lens]
+    idx, out_lens = _run_topk(rows, k)
+    for t in list(range(0, T, 997)) + [T - 1]:
+        ref = O.topk_row(rows[t].astype(np.float64), k)
+        n = min(len(rows[t]), k)
+        assert out_lens[t] == n
+        assert (idx[t, n:] == -1).all()
+        assert np.array_equal(idx[t, :n], np.sort(ref[:n])), t
+
+
 @pytest.mark.parametrize("k", [100, 2048])
 def test_topk_long_rows_many_chunks(k):
     # rows of 8.4M-9M scores: more than 512 collect chunks each, so the ordered
