@@ -590,8 +590,11 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   } else {
     // -------------------------------------------------------------- math
     const int quad = warp;                  // TMEM lane quadrant
-    const int hl = 16 * quad + lane;        // head of this lane (lanes < 16)
-    const bool head_lane = lane < 16;
+    // lanes l and l+16 share head 16q + l % 16: lane l < 16 holds its scores
+    // of kv 0..31, lane l+16 those of kv 32..63 (one 16x32bx2 TMEM load)
+    const int hl = 16 * quad + (lane & 15);
+    const int half = lane >> 4;
+    const bool head_lane = half == 0;       // the lane that writes per-head results
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const float c = a.softmax_scale * kLog2e;
     float m = -INFINITY;                    // reference maximum (exp2 units)
@@ -622,22 +625,22 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       const uint32_t vm_hi = __ballot_sync(0xffffffffu, v_hi);
       if (!tc::mbar_wait(&sfull[b], (i >> 1) & 1, abort_flag)) { ok = false; break; }
       tc::fence_after_sync();
-      float xa[32], xb[32];                 // scores of kv 0..31 and 32..63
-      tc::tmem_ld_cols<32>(tmem + lane_base + kSCol + b * 64, xa);
-      tc::tmem_ld_cols<32>(tmem + lane_base + kSCol + b * 64 + 32, xb);
+      float x[32];                          // this lane's half of its head's 64 scores
+      tc::tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kSCol + b * 64, x);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sempty[b]);
+      const uint32_t vm = half ? vm_hi : vm_lo;
       float tmax = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        xa[j] = ((vm_lo >> j) & 1u) ? xa[j] * c : -INFINITY;
-        xb[j] = ((vm_hi >> j) & 1u) ? xb[j] * c : -INFINITY;
-        tmax = fmaxf(tmax, fmaxf(xa[j], xb[j]));
+        x[j] = ((vm >> j) & 1u) ? x[j] * c : -INFINITY;
+        tmax = fmaxf(tmax, x[j]);
       }
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));   // the head's maximum
       float al = 1.f;
       int need = 0;
-      if (head_lane && tmax > m + kLazy) {
+      if (tmax > m + kLazy) {               // both lanes of the pair decide alike
         al = (m == -INFINITY) ? 0.f : exp2f(m - tmax);
         m = tmax;
         need = 1;
@@ -652,26 +655,25 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       if (head_lane) alpha[hl] = al;
       tc::named_bar_sync(1, 128);
       const int rescale = flag[0] | flag[1] | flag[2] | flag[3];
-      // p = exp2(x - m), its sum, and the P row in two bf16 terms
+      // p = exp2(x - m), its sum, and this lane's half of the P row (bf16:
+      // P_hi + P_lo; fp8 pools: one fp16 term)
       const float msafe = m == -INFINITY ? 0.f : m;   // all masked so far: p = 0
       float ps = 0.f;
-      uint32_t phi[32], plo[4];
+      uint32_t phi[16], plo[4];
 #pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const float x0 = j < 32 ? xa[j] : xb[j - 32];
-        const float x1 = j < 32 ? xa[j + 1] : xb[j - 31];
-        const float p0 = exp2f(x0 - msafe);      // -inf -> 0
-        const float p1 = exp2f(x1 - msafe);
+      for (int j = 0; j < 32; j += 2) {
+        const float p0 = exp2f(x[j] - msafe);      // -inf -> 0
+        const float p1 = exp2f(x[j + 1] - msafe);
         ps += p0 + p1;
         if (FMT == kFmtBf16) {
           const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
           const float2 hf = __bfloat1622float2(hi);
           phi[j / 2] = *reinterpret_cast<const uint32_t *>(&hi);
           plo[(j / 2) & 3] = pack_bf16x2(p0 - hf.x, p1 - hf.y);
-          if ((j & 7) == 6 && head_lane && hl < N) {
+          if ((j & 7) == 6 && hl < N) {
             // P_lo goes straight into this tile's RoPE block (free once S(i)
             // has read it; PV(i-1) never reads it): 8 kv = one 16-byte chunk
-            const int ch = j >> 3;
+            const int ch = 4 * half + (j >> 3);
             *reinterpret_cast<uint4 *>(k_s + (i % NS) * kStageBytes + 8 * kKBlockBytes + hl * 128 +
                                        ((ch ^ (hl & 7)) << 4)) =
                 make_uint4(plo[0], plo[1], plo[2], plo[3]);
@@ -681,6 +683,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
           phi[j / 2] = *reinterpret_cast<const uint32_t *>(&ph);
         }
       }
+      ps += __shfl_xor_sync(0xffffffffu, ps, 16);   // the head's sum, alike in both lanes
       l = l * al + ps;
       // P and O^T may be touched only after PV(i-1) retired
       if (i >= 1) {
@@ -691,13 +694,15 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) tc::tmem_scale_cols<N>(tmem + lane_base + kOCol + j * N, alpha);
       }
-      if (head_lane && hl < N) {
-        // row hl of P (K-major B operand): 64 kv 16-bit values = 128 bytes, swizzled
+      if (hl < N) {
+        // row hl of P (K-major B operand): 64 kv 16-bit values = 128 bytes,
+        // swizzled; this lane's half is chunks 4 half .. 4 half + 3
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int cc = 0; cc < 4; ++cc) {
+          const int ch = 4 * half + cc;
           const uint32_t off = hl * 128 + ((ch ^ (hl & 7)) << 4);
           *reinterpret_cast<uint4 *>(p_s + off) =
-              make_uint4(phi[4 * ch], phi[4 * ch + 1], phi[4 * ch + 2], phi[4 * ch + 3]);
+              make_uint4(phi[4 * cc], phi[4 * cc + 1], phi[4 * cc + 2], phi[4 * cc + 3]);
         }
       }
       tc::fence_proxy_async_smem();

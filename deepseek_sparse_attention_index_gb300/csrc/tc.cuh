@@ -231,6 +231,29 @@ DSA_DEVINLINE void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
   for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16x32bx2 load, 32 columns: threads 0-15 read TMEM lanes base .. base+15
+// (base = the lane field of taddr) at columns [c, c+32); threads 16-31 read
+// the same 16 lanes at columns [c+OFF, c+OFF+32) (OFF an immediate).  For an
+// M = 64 accumulator (rows in lanes 32q + 0..15) lanes l and l+16 of warp q
+// then hold the two halves of row 16q + (l % 16).
+template <int OFF>
+DSA_DEVINLINE void tmem_ld_16x32bx2_x32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], %33;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr), "n"(OFF));
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 32 lanes x 32 bits stores, 16 / 32 / 64 consecutive columns of this lane.
 DSA_DEVINLINE void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
