@@ -85,13 +85,16 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_sums, uint32_t *t
 // consecutive lanes read consecutive bins (no bank conflicts), a scan over
 // the warp totals picks the crossing warp, and that warp alone walks its
 // segment 32 bins at a time.
-__device__ void find_bin(const uint32_t *h, int nbins, uint32_t need, bool descending,
-                         uint32_t *warp_sums, int *bin_out, uint32_t *before_out) {
-  const int nw = blockDim.x >> 5;
+template <int nbins, bool descending>
+__device__ __forceinline__ void find_bin(const uint32_t *h, uint32_t need, uint32_t *warp_sums,
+                                         int *bin_out, uint32_t *before_out) {
+  constexpr int nw = kThreads / 32;   // blockDim.x == kThreads
   const int w = threadIdx.x >> 5;
   const unsigned lane = lane_id();
-  const int seg = nbins / nw;
+  constexpr int seg = nbins / nw;
+  static_assert(seg % 32 == 0, "each warp walks whole 32-bin rows");
   uint32_t s = 0;
+#pragma unroll
   for (int j = lane; j < seg; j += 32) {
     const int wpos = w * seg + j;
     s += h[descending ? nbins - 1 - wpos : wpos];
@@ -331,7 +334,7 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
   }
   __syncthreads();
   if (to_cache) src.cache = lc;
-  find_bin(sh, kHistBins, r1, true, S.warp_sums, &S.s_bin, &S.s_before);
+  find_bin<kHistBins, true>(sh, r1, S.warp_sums, &S.s_bin, &S.s_before);
   const uint32_t b2 = (uint32_t)S.s_bin;
   const uint32_t r2 = r1 - S.s_before;
   const uint32_t hi20 = (b1 << 12) | b2;   // bits 31..8 of K*
@@ -339,15 +342,28 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
   // level 3: bits 7..0 among keys whose bits 31..8 are hi20
   for (int i = threadIdx.x; i < kThreads; i += blockDim.x) sh[i] = 0;
   __syncthreads();
-  for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
-    uint32_t key; int32_t pos;
-    src.get(i, key, pos);
+  auto for_each = [&](auto f) {   // every (key, position): the shared copy, else via src
+    if (src.cache) {
+      const int n = (int)src.n;
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint2 e = src.cache[i];
+        f(e.x, (int32_t)e.y);
+      }
+    } else {
+      for (int64_t i = threadIdx.x; i < src.n; i += kThreads) {
+        uint32_t key; int32_t pos;
+        src.get(i, key, pos);
+        f(key, pos);
+      }
+    }
+  };
+  for_each([&](uint32_t key, int32_t) {
     if ((key >> 8) == hi20) atomicAdd(&sh[key & 0xFFu], 1u);
-  }
+  });
   __syncthreads();
   // 256 bins padded with zero bins to the block size; walking down from the
   // top passes the zero bins first
-  find_bin(sh, kThreads, r2, true, S.warp_sums, &S.s_bin, &S.s_before);
+  find_bin<kThreads, true>(sh, r2, S.warp_sums, &S.s_bin, &S.s_before);
   const uint32_t b3 = (uint32_t)S.s_bin;
   const uint32_t r3 = r2 - S.s_before;   // how many elements equal to K* to keep
   const uint32_t m_eq = sh[b3];          // how many elements equal K*
@@ -366,19 +382,17 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
       __syncthreads();
       for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
       __syncthreads();
-      for (int64_t i = threadIdx.x; i < src.n; i += blockDim.x) {
-        uint32_t key; int32_t pos;
-        src.get(i, key, pos);
+      for_each([&](uint32_t key, int32_t pos) {
         if (key == kstar) {
           const uint32_t p = (uint32_t)pos;
           const uint32_t hi_bits = lvl == 0 ? 0u : (p >> (sft + widths[lvl]));
           if (hi_bits == prefix) atomicAdd(&sh[(p >> sft) & (nb - 1)], 1u);
         }
-      }
+      });
       __syncthreads();
       // ascending walk over max(nb, blockDim) bins (extra bins are zero)
-      const int nbins = (int)max(nb, (uint32_t)blockDim.x);
-      find_bin(sh, nbins, need, false, S.warp_sums, &S.s_bin, &S.s_before);
+      if (nb == 2048) find_bin<2048, false>(sh, need, S.warp_sums, &S.s_bin, &S.s_before);
+      else find_bin<1024, false>(sh, need, S.warp_sums, &S.s_bin, &S.s_before);
       need -= S.s_before;
       prefix = (prefix << widths[lvl]) | (uint32_t)S.s_bin;
     }
