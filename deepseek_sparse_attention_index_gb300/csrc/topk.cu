@@ -265,6 +265,8 @@ struct ResolveSmem {
   uint32_t sh[kHistBins];
   uint32_t run_pre[kThreads];    // ordered start of each run of a group of chunks
   uint32_t run_at[kThreads];     // where that run sits in the list
+  uint32_t ph_at[kThreads];      // the runs sorted by where they sit in the list:
+  uint32_t ph_pre[kThreads];     //   list start and ordered (position-order) start
   uint32_t warp_sums[32];
   int s_bin;
   uint32_t s_before;
@@ -309,6 +311,31 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
   // the first group of the chunk table, loaded now, used by the compaction
   uint2 run0 = make_uint2(0u, 0u);
   if (!src.from_row && (int)threadIdx.x < min(nch, kThreads)) run0 = __ldcg(rt + threadIdx.x);
+  // With the list copied and at most kThreads chunks, the copy is made in
+  // position order: run c (chunk c) starts at the ordered offset pre(c), and
+  // a list slot i finds its run by a binary search over the runs sorted by
+  // list start (an empty run sorts last and is never found).
+  const bool ordered = to_cache && nch <= kThreads;
+  int n_runs = 0;
+  if (ordered) {
+    uint32_t tot_runs;
+    const uint32_t pre = block_excl_scan(run0.y, S.warp_sums, &tot_runs);
+    const uint32_t at = ((int)threadIdx.x < nch && run0.y > 0) ? run0.x : 0xffffffffu;
+    S.run_at[threadIdx.x] = at;
+    S.run_pre[threadIdx.x] = pre;
+    __syncthreads();
+    if ((int)threadIdx.x < nch) {
+      int rank = 0;   // position of this run among the runs sorted by (list start, chunk)
+      for (int c2 = 0; c2 < nch; ++c2) {
+        const uint32_t a2 = S.run_at[c2];
+        rank += (a2 < at || (a2 == at && c2 < (int)threadIdx.x)) ? 1 : 0;
+      }
+      S.ph_at[rank] = at;
+      S.ph_pre[rank] = pre;
+    }
+    for (int c2 = 0; c2 < nch; ++c2) n_runs += S.run_at[c2] != 0xffffffffu ? 1 : 0;
+    __syncthreads();
+  }
 
   // level 2: bits 19..8 of the bin-b1 keys; the same pass copies the list
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
@@ -327,7 +354,17 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
     for (int j = 0; j < kBatch; ++j) {
       const int64_t i = i0 + (int64_t)j * kThreads + threadIdx.x;
       if (pos[j] >= 0) {
-        if (to_cache) lc[i] = make_uint2(key[j], (uint32_t)pos[j]);
+        if (ordered) {
+          // the run holding list slot i: the last one starting at or before i
+          int lo = 0, hi = n_runs;
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (S.ph_at[mid] <= (uint32_t)i) lo = mid; else hi = mid;
+          }
+          lc[S.ph_pre[lo] + ((uint32_t)i - S.ph_at[lo])] = make_uint2(key[j], (uint32_t)pos[j]);
+        } else if (to_cache) {
+          lc[i] = make_uint2(key[j], (uint32_t)pos[j]);
+        }
         if ((key[j] >> 20) == b1) atomicAdd(&sh[(key[j] >> 8) & 0xFFFu], 1u);
       }
     }
@@ -404,7 +441,33 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
   // ordered sequence per round; a block scan of its survivor count gives
   // where they go.
   uint32_t written = 0;
-  if (src.from_row) {
+  if (ordered) {
+    // the copy is in position order: one pass, kGather consecutive entries a thread
+    const uint32_t n = (uint32_t)src.n;
+    for (uint32_t r0 = 0; r0 < n; r0 += (uint32_t)kGather * kThreads) {
+      const uint32_t l0 = r0 + (uint32_t)kGather * threadIdx.x;
+      uint32_t m = 0;
+      int32_t posv[kGather];
+#pragma unroll
+      for (int j = 0; j < kGather; ++j) {
+        posv[j] = 0;
+        if (l0 + j < n) {
+          const uint2 e = lc[l0 + j];
+          posv[j] = (int32_t)e.y;
+          if (e.x > kstar || (e.x == kstar && (int32_t)e.y <= pstar)) m |= 1u << j;
+        }
+      }
+      uint32_t tot;
+      uint32_t o = written + block_excl_scan((uint32_t)__popc(m), S.warp_sums, &tot);
+#pragma unroll
+      for (int j = 0; j < kGather; ++j)
+        if ((m >> j) & 1u) {
+          if (o < (uint32_t)k) out[o] = posv[j] + base;
+          ++o;
+        }
+      written += tot;
+    }
+  } else if (src.from_row) {
     for (int64_t r0 = 0; r0 < L; r0 += (int64_t)kGather * kThreads) {
       const int64_t p0 = r0 + (int64_t)kGather * threadIdx.x;
       uint32_t m = 0;
