@@ -598,9 +598,15 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
   const float *row = scores + (int64_t)t * ld;
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
 
-  // this row's histogram slice, then this thread's scores: all loads in
-  // flight while the threshold is found
+  // this row's histogram slice first
   const HistSlice hs = hist_load(hist + (size_t)t * kHistBins);
+  if (threadIdx.x == 0) { S.s_bin = 0; S.s_before = 0; }
+  __syncthreads();
+  threshold_bin(hs, (uint32_t)k, S.warp_sums, &S.s_bin, &S.s_before);
+  const uint32_t b1 = (uint32_t)S.s_bin;
+  const uint32_t n_gt = S.s_before;
+  // this thread's scores (after the threshold, whose histogram loads then
+  // do not queue behind them)
   uint32_t v[kRounds][kPer];
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
@@ -620,11 +626,6 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
       for (int e = 0; e < kPer; ++e) v[r][e] = p + e < hi ? __float_as_uint(__ldcg(row + p + e)) : 0u;
     }
   }
-  if (threadIdx.x == 0) { S.s_bin = 0; S.s_before = 0; }
-  __syncthreads();
-  threshold_bin(hs, (uint32_t)k, S.warp_sums, &S.s_bin, &S.s_before);
-  const uint32_t b1 = (uint32_t)S.s_bin;
-  const uint32_t n_gt = S.s_before;
 
   // entries at or above bin b1, counted per round (packed: a round holds at
   // most 8192 of them, so the two 16-bit halves of the scan never carry)
