@@ -233,6 +233,7 @@ int dsa_decode(const void *q_idx, int idx_dtype, const float *q_scale, const voi
   ia.slot_base = slot_base; ia.seq_lens = seq_lens;
   ia.T = B; ia.H_I = H_I; ia.d = d_idx; ia.max_len = max_seq_len;
   ia.scores = L.scores; ia.ld_scores = ld; ia.hist = L.topk.hist; ia.topk_k = k;
+  ia.inputs_ready = 1;   // the inputs precede the whole call; only the zeroing precedes us
   ia.err_flag = err_flag;
   e = index_score_launch(ia, s);
   if (e != cudaSuccess) return DSA_ERR_CUDA;

@@ -147,6 +147,10 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a dependent of the histogram's zeroing: with inputs_ready
+  // (fused decode) only the epilogue, which adds into the histogram, waits
+  // for it; otherwise every role waits before touching anything.
+  if (!a.inputs_ready || warp >= 2) pdl_wait();
   pdl_trigger();   // the next kernel may be placed as SMs free up; it waits for us
 
   const int64_t total = (int64_t)a.T * tiles_per_row;
@@ -436,8 +440,8 @@ cudaError_t launch_tc(const IndexScoreArgs &a, cudaStream_t s) {
   auto kern = index_score_tc_kernel<FP8, N, KB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)grid, kThreads, smem, s>>>(kmap, qmap, smap, a, tiles_per_row, per);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, kmap, qmap, smap, a,
+                    tiles_per_row, per);
 }
 
 template <bool FP8, int KB>

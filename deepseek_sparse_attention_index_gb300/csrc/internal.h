@@ -22,7 +22,7 @@ struct TopkWs {
 };
 size_t topk_ws_layout(int T, int64_t max_len, int k, void *ws, TopkWs *out);  // returns bytes
 
-// Clears hist and cnt (one memset each, stream-ordered).
+// Clears hist and cnt (one small kernel, stream-ordered).
 cudaError_t topk_clear(const TopkWs &w, int T, cudaStream_t s);
 // Histogram pass over a score matrix (the standalone entry point; the fused
 // decode builds the histogram in the index-score epilogue instead).
@@ -51,6 +51,9 @@ struct IndexScoreArgs {
   int64_t ld_scores;
   uint32_t *hist;            // optional [T][kHistBins]: fused top-k histogram
   int topk_k;                // rows of length <= topk_k skip the histogram
+  int inputs_ready;          // the inputs were complete before the previous kernel on the
+                             // stream began (fused decode: only the histogram's zeroing
+                             // precedes us); else the kernel waits for it first
   int32_t *err_flag;
 };
 cudaError_t index_score_launch(const IndexScoreArgs &a, cudaStream_t s);

@@ -684,6 +684,13 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
               index_base, list, tab, idx, lens, err_flag);
 }
 
+__global__ void __launch_bounds__(256) zero16_kernel(uint4 *p, size_t n16) {
+  pdl_trigger();
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (size_t)gridDim.x * blockDim.x)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // Positions per collect CTA: the smallest power of two in [kMinChunk,
 // kMaxChunk] whose grid fits in one wave (two CTAs per SM); kMaxChunk when
 // none does.
@@ -710,9 +717,14 @@ size_t topk_ws_layout(int T, int64_t max_len, int k, void *ws, TopkWs *out) {
 }
 
 cudaError_t topk_clear(const TopkWs &w, int T, cudaStream_t s) {
-  // hist and cnt are adjacent in the workspace (topk_ws_layout): one memset
+  // hist and cnt are adjacent in the workspace (topk_ws_layout) and their
+  // size is a multiple of 16 bytes: one grid-stride kernel, which the next
+  // kernel (launched as its dependent) may overlap
   const char *end = reinterpret_cast<const char *>(w.cnt + (size_t)T * 4);
-  return cudaMemsetAsync(w.hist, 0, (size_t)(end - reinterpret_cast<const char *>(w.hist)), s);
+  const size_t n16 = (size_t)(end - reinterpret_cast<const char *>(w.hist)) / 16;
+  const unsigned blocks = (unsigned)std::min<size_t>((n16 + 255) / 256, 4 * (size_t)num_sms());
+  zero16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<uint4 *>(w.hist), n16);
+  return cudaGetLastError();
 }
 
 cudaError_t topk_hist(const float *scores, int64_t ld, const int32_t *row_len, int T,
