@@ -162,6 +162,9 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     if (lane == 0) {
       tc::prefetch_tmap(&kmap);
       tc::prefetch_tmap(&qmap);
+      // the key tiles and scales are read once: evict them first, so the
+      // score rows written by this kernel are still in L2 for the top-k
+      const uint64_t stream_policy = tc::l2_policy_evict_first();
       if (FP8) tc::prefetch_tmap(&smap);
       int stage = 0;
       uint32_t phase = 0;
@@ -207,14 +210,15 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         tc::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
         const int y = (int)(ri.r0 + j * kTileKeys);
         for (int kb = 0; kb < KB; ++kb)
-          tc::tma_load_2d(&kmap, &full[stage], base + L.stage0 + stage * L.stage_bytes + kb * 16384,
-                          kb * (FP8 ? 128 : 64), y);
+          tc::tma_load_2d_hint(&kmap, &full[stage], base + L.stage0 + stage * L.stage_bytes + kb * 16384,
+                               kb * (FP8 ? 128 : 64), y, stream_policy);
         if (FP8) {
           // the 128 key scales, from the nearest 16-byte boundary at or below y,
           // into their own ring (held until the epilogue has read them)
           if (!tc::mbar_wait(&scempty[ss], sphase ^ 1, abort_flag)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(&scfull[ss], kScBox * 4);
-          tc::tma_load_1d(&smap, &scfull[ss], base + L.sc + ss * kScBytes, y & ~3);
+          tc::tma_load_2d_hint(&smap, &scfull[ss], base + L.sc + ss * kScBytes, y & ~3, 0,
+                               stream_policy);
           s_issued |= 1u << ss;
           s_last = (s_last & ~(1u << ss)) | (sphase << ss);
           if (++ss == kScSlots) {

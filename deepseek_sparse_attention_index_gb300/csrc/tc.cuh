@@ -125,6 +125,24 @@ DSA_DEVINLINE void tma_gather4(const CUtensorMap *map, uint64_t *bar, void *dst,
       : "memory");
 }
 
+// L2 policy for data read once (streamed): evict it first, so that lines
+// written nearby (e.g. a score row read back by the next kernel) stay.
+DSA_DEVINLINE uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 cache policy.
+DSA_DEVINLINE void tma_load_2d_hint(const CUtensorMap *map, uint64_t *bar, void *dst, int x, int y,
+                                    uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
 // Tile load of `box` elements starting at element x of a map made by
 // make_tmap_1d.  The caller keeps x * element size a multiple of 16 bytes.
 DSA_DEVINLINE void tma_load_1d(const CUtensorMap *map, uint64_t *bar, void *dst, int x) {
