@@ -233,50 +233,89 @@ sparse_mla_simt_kernel(MlaArgs a) {
   }
 }
 
-// Merge split partials: one CTA per (token, head), 128 threads x 4 values.
-// The splits' lse values are staged in shared memory first, so every
-// partial-row load below is independent of the others and all are in flight
-// together (a split with no valid entry has lse = -inf and weight 0; its
-// partial row holds zeros).
+// Merge split partials: one warp per (token, head) record (Dv <= 512: four
+// float4 columns a lane), the splits folded in batches whose loads -- lse
+// values and partial rows alike -- are all in flight together, so a call with
+// at most kCombineBatch splits waits for one round of L2 latency.
 constexpr int kMaxSplits = 256;
 
-__global__ void __launch_bounds__(128)
-mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
+constexpr int kCombineWarps = 8;     // records per 256-thread CTA, one per warp
+constexpr int kCombineBatch = 4;     // splits whose loads are in flight together
+
+__global__ void __launch_bounds__(32 * kCombineWarps)
+mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse, int T,
                    int H, int Dv, int n_splits, __nv_bfloat16 *__restrict__ out,
                    float *__restrict__ lse) {
-  __shared__ float lse_s[kMaxSplits];
   pdl_wait();      // the partials come from the previous kernel
-  const int t = blockIdx.x, h = blockIdx.y;
-  for (int i = threadIdx.x; i < n_splits; i += blockDim.x)
-    lse_s[i] = __ldcg(part_lse + ((size_t)t * n_splits + i) * H + h);
-  __syncthreads();
-  float mx = -INFINITY;
-  for (int i = 0; i < n_splits; ++i) mx = fmaxf(mx, lse_s[i]);
-  float tot = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int dv = 4 * threadIdx.x;
-#pragma unroll 8
-  for (int i = 0; i < n_splits; ++i) {
-    const float li = lse_s[i];
-    const float wgt = li == -INFINITY ? 0.f : __expf(li - mx);
-    tot += wgt;
-    if (dv < Dv) {
-      const size_t rec = ((size_t)t * n_splits + i) * H + h;
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(part_o + rec * Dv + dv));
-      acc.x = fmaf(wgt, v.x, acc.x);
-      acc.y = fmaf(wgt, v.y, acc.y);
-      acc.z = fmaf(wgt, v.z, acc.z);
-      acc.w = fmaf(wgt, v.w, acc.w);
+  // one warp per record (t, h); lane l holds the float4 columns l + 32 q
+  const int64_t r = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (r >= (int64_t)T * H) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = r / H, h = r - t * H;
+  const int nf = Dv >> 2;                        // float4 columns of a record
+  // the splits in batches: every load of a batch (its lse values and its
+  // partial rows) is issued before any is used, and the batch folds into a
+  // running maximum and sum
+  float mx = -INFINITY, tot = 0.f;
+  float4 acc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = 0; i0 < n_splits; i0 += kCombineBatch) {
+    float li[kCombineBatch];
+    float4 v[kCombineBatch][4];
+#pragma unroll
+    for (int b = 0; b < kCombineBatch; ++b) {
+      const int i = i0 + b;
+      li[b] = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[b][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < n_splits) {
+        const int64_t rec = (t * n_splits + i) * H + h;
+        li[b] = __ldcg(part_lse + rec);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int f = lane + 32 * q;
+          if (f < nf) v[b][q] = __ldcg(reinterpret_cast<const float4 *>(part_o + rec * Dv) + f);
+        }
+      }
     }
+    float bm = mx;
+#pragma unroll
+    for (int b = 0; b < kCombineBatch; ++b) bm = fmaxf(bm, li[b]);
+    if (bm == -INFINITY) continue;               // no split with a valid entry yet
+    const float sc = mx == -INFINITY ? 0.f : __expf(mx - bm);
+    tot *= sc;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[q].x *= sc; acc[q].y *= sc; acc[q].z *= sc; acc[q].w *= sc;
+    }
+#pragma unroll
+    for (int b = 0; b < kCombineBatch; ++b) {
+      // a split with no valid entry has lse = -inf and weight 0
+      const float wgt = li[b] == -INFINITY ? 0.f : __expf(li[b] - bm);
+      tot += wgt;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[q].x = fmaf(wgt, v[b][q].x, acc[q].x);
+        acc[q].y = fmaf(wgt, v[b][q].y, acc[q].y);
+        acc[q].z = fmaf(wgt, v[b][q].z, acc[q].z);
+        acc[q].w = fmaf(wgt, v[b][q].w, acc[q].w);
+      }
+    }
+    mx = bm;
   }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  if (dv < Dv) {
-    uint2 pk;
-    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2 *>(out + ((size_t)t * H + h) * Dv + dv) = pk;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int f = lane + 32 * q;
+    if (f < nf) {
+      uint2 pk;
+      pk.x = pack_bf16x2(acc[q].x * inv, acc[q].y * inv);
+      pk.y = pack_bf16x2(acc[q].z * inv, acc[q].w * inv);
+      *reinterpret_cast<uint2 *>(out + r * Dv + 4 * f) = pk;
+    }
   }
-  if (threadIdx.x == 0) lse[(size_t)t * H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  if (lane == 0) lse[r] = tot > 0.f ? mx + logf(tot) : -INFINITY;
 }
 
 }  // namespace
@@ -331,8 +370,11 @@ cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_splits == 1) return e;
-  return launch_pdl(mla_combine_kernel, dim3((unsigned)a.T, (unsigned)a.H), dim3(128), 0, s,
-                    (const float *)a.part_o, (const float *)a.part_lse, a.H, a.Dv, a.n_splits,
+  const int64_t recs = (int64_t)a.T * a.H;
+  return launch_pdl(mla_combine_kernel,
+                    dim3((unsigned)((recs + kCombineWarps - 1) / kCombineWarps)),
+                    dim3(32 * kCombineWarps), 0, s, (const float *)a.part_o,
+                    (const float *)a.part_lse, a.T, a.H, a.Dv, a.n_splits,
                     static_cast<__nv_bfloat16 *>(a.out), a.lse);
 }
 

@@ -132,7 +132,7 @@ __host__ __device__ inline MlaSmem mla_smem_layout() {
   L.inv_l = L.rows + (FMT == kFmtBf16 ? 0 : 2 * 64 * 16);   // [64] 1 / final sums
   L.flag = L.inv_l + 64 * 4;         // [2][4] ints, by tile parity
   L.bars = L.flag + 32;              // 8-byte aligned
-  L.total = L.bars + 16 * 8;
+  L.total = L.bars + 32 * 8;
   return L;
 }
 
@@ -297,6 +297,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 14);
   uint64_t *qready = bars + 15;   // fp8 pools: Q converted to fp16 by the math warps
+  uint64_t *lastpv = bars + 22;   // [4]: the last tile's PV into dv block j retired
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -329,6 +330,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     tc::mbar_init(&done[1], 1);
     tc::mbar_init(qfull, 1);
     tc::mbar_init(qready, 4);
+    for (int j = 0; j < 4; ++j) tc::mbar_init(&lastpv[j], 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -576,15 +578,12 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
             tc::mma_f16(tmem + kOCol + j * N, adv + j * 1024 + kr * 128,
                         (kk < 4 ? bdp : bdl) + kr * 2, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
           }
+          if (i == nt - 1) tc::mma_commit(&lastpv[j]);   // the epilogue of block j may start
         }
         tc::mma_commit(&kempty[st]);
         tc::mma_commit(pempty);
       }
-      if (nt > 0) {
-        tc::mma_commit(&done[1]);
-        tc::mbar_wait_drain(&done[1], 0);
-      }
-      tc::mbar_wait_drain(qfull, 0);   // the Q load landed before the CTA exits
+      if (nt > 0) tc::mma_commit(&done[1]);   // waited for after the epilogue
     }
     __syncwarp();
   } else {
@@ -710,61 +709,8 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(pfull);
     }
-    // ---- epilogue: O^T / l per head
+    // ---- per-head results: 1 / l for the epilogue, and the lse
     if (head_lane) inv_l[hl] = (l > 0.f) ? 1.f / l : 0.f;
-    if (ok && nt > 0) {
-      ok = tc::mbar_wait(pempty, (nt - 1) & 1, abort_flag);
-      tc::fence_after_sync();
-    }
-    tc::named_bar_sync(1, 128);
-    const bool have_o = ok && nt > 0;
-    // this CTA's records: [nh heads][kDv] bf16 (one piece) or fp32 partials
-    constexpr int kDv = F::kDv;
-    const size_t rec0 = a.n_splits == 1 ? (size_t)t * a.H + h0
-                                        : ((size_t)t * a.n_splits + split) * a.H + h0;
-#pragma unroll 1
-    for (int j = 0; j < 4; ++j) {
-      const int dv = 128 * j + 32 * quad + lane;
-      if (128 * j + 32 * quad >= kDv) break;   // warp-uniform: the RoPE columns of fp8 rows
-#pragma unroll 1
-      for (int c0 = 0; c0 < N && c0 < nh; c0 += 16) {
-        float o[16];
-        if (have_o) {
-          tc::tmem_ld_cols<16>(tmem + lane_base + kOCol + j * N + c0, o);
-        } else {
-#pragma unroll
-          for (int h = 0; h < 16; ++h) o[h] = 0.f;
-        }
-        float inv[16];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 v = *reinterpret_cast<const float4 *>(inv_l + c0 + 4 * q4);
-          inv[4 * q4] = v.x; inv[4 * q4 + 1] = v.y; inv[4 * q4 + 2] = v.z; inv[4 * q4 + 3] = v.w;
-        }
-        const int nq = min(16, nh - c0);   // heads of this chunk that exist
-        if (a.n_splits == 1) {
-          __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + (rec0 + c0) * kDv + dv;
-          if (nq == 16) {
-#pragma unroll
-            for (int hq = 0; hq < 16; ++hq) dst[hq * kDv] = __float2bfloat16_rn(o[hq] * inv[hq]);
-          } else {
-#pragma unroll
-            for (int hq = 0; hq < 16; ++hq)
-              if (hq < nq) dst[hq * kDv] = __float2bfloat16_rn(o[hq] * inv[hq]);
-          }
-        } else {
-          float *dst = a.part_o + (rec0 + c0) * kDv + dv;
-          if (nq == 16) {
-#pragma unroll
-            for (int hq = 0; hq < 16; ++hq) dst[hq * kDv] = o[hq] * inv[hq];
-          } else {
-#pragma unroll
-            for (int hq = 0; hq < 16; ++hq)
-              if (hq < nq) dst[hq * kDv] = o[hq] * inv[hq];
-          }
-        }
-      }
-    }
     if (head_lane && hl < nh) {
       const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       if (a.n_splits == 1)
@@ -772,6 +718,55 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       else
         a.part_lse[((size_t)t * a.n_splits + split) * a.H + h0 + hl] = lse;
     }
+    tc::named_bar_arrive(3, 256);    // inv_l is written: warps 4-7 may start
+    tc::named_bar_sync(1, 128);
+  }
+
+  // ---- epilogue: O^T / l per head, read from TMEM by warps 0-7 (warp w
+  // reaches TMEM lane quadrant w % 4): warps 0-3 take dv blocks 0 and 1,
+  // warps 4-7 blocks 2 and 3, each block as soon as the last tile's PV into
+  // it has retired.  This CTA's records: [nh heads][kDv] bf16 (one piece) or
+  // fp32 partials.
+  if (warp < 8) {
+    if (warp >= 4) tc::named_bar_sync(3, 256);
+    constexpr int kDv = F::kDv;
+    const int quad = warp & 3;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const size_t rec0 = a.n_splits == 1 ? (size_t)t * a.H + h0
+                                        : ((size_t)t * a.n_splits + split) * a.H + h0;
+#pragma unroll 1
+    for (int j = 2 * (warp >> 2); j < 2 * (warp >> 2) + 2; ++j) {
+      const int dv = 128 * j + 32 * quad + lane;
+      if (128 * j + 32 * quad >= kDv) break;   // warp-uniform: the RoPE columns of fp8 rows
+      bool have_o = nt > 0 && !*abort_flag;
+      if (have_o) {
+        have_o = tc::mbar_wait(&lastpv[j], 0, abort_flag);
+        tc::fence_after_sync();
+      }
+      float o[N];
+      if (have_o) {
+        tc::tmem_ld_cols<N>(tmem + lane_base + kOCol + j * N, o);
+      } else {
+#pragma unroll
+        for (int h = 0; h < N; ++h) o[h] = 0.f;
+      }
+      if (a.n_splits == 1) {
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + rec0 * kDv + dv;
+#pragma unroll
+        for (int hq = 0; hq < N; ++hq)
+          if (hq < nh) dst[hq * kDv] = __float2bfloat16_rn(o[hq] * inv_l[hq]);
+      } else {
+        float *dst = a.part_o + rec0 * kDv + dv;
+#pragma unroll
+        for (int hq = 0; hq < N; ++hq)
+          if (hq < nh) dst[hq * kDv] = o[hq] * inv_l[hq];
+      }
+    }
+  }
+  if (warp == 5 && lane == 0) {
+    // the PV warp's MMAs retired and the Q load landed before TMEM is released
+    if (nt > 0) tc::mbar_wait_drain(&done[1], 0);
+    tc::mbar_wait_drain(qfull, 0);
   }
 
   tc::fence_before_sync();

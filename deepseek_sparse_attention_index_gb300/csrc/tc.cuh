@@ -303,6 +303,11 @@ DSA_DEVINLINE void tmem_scale_cols(uint32_t taddr, const float *alpha) {
 DSA_DEVINLINE void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Arrive at named barrier `id` without waiting (the waiting side calls
+// named_bar_sync with the same count); writes before it are visible to them.
+DSA_DEVINLINE void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 // ---------------------------------------------------------------- MMA
 
