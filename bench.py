@@ -139,7 +139,11 @@ def run_ours(args, rank, world):
     def step():
         ops.decode_case(case, ws=ws, idx_out=idx_out, out=out, lse=lse)
 
-    for _ in range(args.warmup):
+    # warm-up iterations are the timed ones untimed: the flush included (the
+    # first launch of its kernels costs ~0.1 ms, which must not land in a
+    # timed step)
+    for i in range(args.warmup):
+        l2_flush(i)
         step()
     torch.cuda.synchronize()
 
@@ -293,9 +297,11 @@ def run_ours(args, rank, world):
 def _timed(fn, steps, warmup, flush_fn):
     """Device µs of fn() per call: W warm-up calls, then K calls each between
     CUDA events on the current stream, the L2 flushed before each (outside the
-    events); all launches queued behind a GPU-side sleep."""
+    events, and before each warm-up call too); all launches queued behind a
+    GPU-side sleep."""
     import torch
-    for _ in range(warmup):
+    for i in range(warmup):
+        flush_fn(i)
         fn()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
