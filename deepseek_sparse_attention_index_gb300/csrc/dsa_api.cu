@@ -111,6 +111,81 @@ DecodeLayout decode_layout(int B, int64_t max_seq_len, int k, int H, int Dv, int
   return L;
 }
 
+// Enqueues one checked fused decode step on s.
+int decode_enqueue(const void *q_idx, int idx_dtype, const float *q_scale, const void *k_idx,
+                   const float *k_scale, int64_t k_rows, const float *w, int H_I, int d_idx, int B,
+                   const int32_t *seq_lens, const int32_t *slot_base, int64_t max_seq_len, int k,
+                   const void *q, int H, int D, int Dv, float softmax_scale, const dsa_kv_pool *kv,
+                   const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa, int32_t *idx_out,
+                   void *out, float *lse, void *ws, int32_t *err_flag, cudaStream_t s) {
+  DecodeLayout L = decode_layout(B, max_seq_len, k, H, Dv, k_swa, ws);
+  const int64_t ld = scores_ld(max_seq_len);
+  int32_t *idx = idx_out ? idx_out : L.idx;
+
+  cudaError_t e = topk_clear(L.topk, B, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  IndexScoreArgs ia{};
+  ia.q_idx = q_idx; ia.idx_dtype = idx_dtype; ia.q_scale = q_scale;
+  ia.k_idx = k_idx; ia.k_scale = k_scale; ia.k_rows = k_rows; ia.w = w;
+  ia.slot_base = slot_base; ia.seq_lens = seq_lens;
+  ia.T = B; ia.H_I = H_I; ia.d = d_idx; ia.max_len = max_seq_len;
+  ia.scores = L.scores; ia.ld_scores = ld; ia.hist = L.topk.hist; ia.topk_k = k;
+  ia.inputs_ready = 1;   // the inputs precede the whole call; only the zeroing precedes us
+  ia.err_flag = err_flag;
+  e = index_score_launch(ia, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  e = topk_select(L.scores, ld, seq_lens, B, max_seq_len, k, slot_base, idx, nullptr, L.topk,
+                  err_flag, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  MlaArgs a{};
+  a.q = q; a.T = B; a.H = H; a.D = D; a.Dv = Dv; a.softmax_scale = softmax_scale;
+  a.q_ready = 1;   // q precedes the whole fused call on the stream
+  a.kv = to_dev(kv); a.idx = idx; a.k = k;
+  a.kv2 = to_dev(k_swa > 0 ? kv_swa : nullptr); a.idx2 = k_swa > 0 ? idx_swa : nullptr;
+  a.k2 = k_swa;
+  a.out = out; a.lse = lse; a.err_flag = err_flag;
+  a.n_splits = mla_num_splits(B, H, k + k_swa);
+  a.part_o = L.part_o; a.part_lse = L.part_lse;
+  return status_of(sparse_mla_launch(a, s));
+}
+
+// Device staging of dsa_decode_host: the decode workspace, then the step's
+// inputs and outputs.
+struct HostStaging {
+  void *dec_ws;
+  size_t dec_bytes;
+  void *q_idx;
+  float *q_scale, *w;
+  int32_t *seq_lens, *slot_base;
+  void *q;
+  int32_t *idx_swa, *idx_out;
+  void *out;
+  float *lse;
+  size_t bytes;
+};
+
+size_t idx_elem_bytes(int idx_dtype) { return idx_dtype == DSA_IDX_FP8_E4M3 ? 1 : 2; }
+
+HostStaging host_staging(int B, int64_t max_seq_len, int k, int H_I, int d_idx, int idx_dtype,
+                         int H, int D, int Dv, int k_swa, void *ws) {
+  HostStaging S{};
+  WsCarver c(ws);
+  S.dec_bytes = decode_layout(B, max_seq_len, k, H, Dv, k_swa, nullptr).bytes;
+  S.dec_ws = c.take<char>(S.dec_bytes);
+  S.q_idx = c.take<char>((size_t)B * H_I * d_idx * idx_elem_bytes(idx_dtype));
+  S.q_scale = c.take<float>((size_t)B * H_I);
+  S.w = c.take<float>((size_t)B * H_I);
+  S.seq_lens = c.take<int32_t>((size_t)B);
+  S.slot_base = c.take<int32_t>((size_t)B);
+  S.q = c.take<char>((size_t)B * H * D * 2);
+  S.idx_swa = c.take<int32_t>((size_t)B * k_swa);
+  S.idx_out = c.take<int32_t>((size_t)B * k);
+  S.out = c.take<char>((size_t)B * H * Dv * 2);
+  S.lse = c.take<float>((size_t)B * H);
+  S.bytes = c.bytes();
+  return S;
+}
+
 }  // namespace
 
 extern "C" {
@@ -220,36 +295,74 @@ int dsa_decode(const void *q_idx, int idx_dtype, const float *q_scale, const voi
   if (!seq_lens || !slot_base) return DSA_ERR_INVALID_ARG;
   const size_t need = dsa_decode_workspace_size(B, max_seq_len, k, H, Dv, k_swa);
   if (ws_bytes < need || !ws) return DSA_ERR_WORKSPACE_TOO_SMALL;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  DecodeLayout L = decode_layout(B, max_seq_len, k, H, Dv, k_swa, ws);
-  const int64_t ld = scores_ld(max_seq_len);
-  int32_t *idx = idx_out ? idx_out : L.idx;
+  return decode_enqueue(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, H_I, d_idx, B,
+                        seq_lens, slot_base, max_seq_len, k, q, H, D, Dv, softmax_scale, kv, kv_swa,
+                        idx_swa, k_swa, idx_out, out, lse, ws, err_flag,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
 
-  cudaError_t e = topk_clear(L.topk, B, s);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
-  IndexScoreArgs ia{};
-  ia.q_idx = q_idx; ia.idx_dtype = idx_dtype; ia.q_scale = q_scale;
-  ia.k_idx = k_idx; ia.k_scale = k_scale; ia.k_rows = k_rows; ia.w = w;
-  ia.slot_base = slot_base; ia.seq_lens = seq_lens;
-  ia.T = B; ia.H_I = H_I; ia.d = d_idx; ia.max_len = max_seq_len;
-  ia.scores = L.scores; ia.ld_scores = ld; ia.hist = L.topk.hist; ia.topk_k = k;
-  ia.inputs_ready = 1;   // the inputs precede the whole call; only the zeroing precedes us
-  ia.err_flag = err_flag;
-  e = index_score_launch(ia, s);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
-  e = topk_select(L.scores, ld, seq_lens, B, max_seq_len, k, slot_base, idx, nullptr, L.topk,
-                  err_flag, s);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
-  MlaArgs a{};
-  a.q = q; a.T = B; a.H = H; a.D = D; a.Dv = Dv; a.softmax_scale = softmax_scale;
-  a.q_ready = 1;   // q precedes the whole fused call on the stream
-  a.kv = to_dev(kv); a.idx = idx; a.k = k;
-  a.kv2 = to_dev(k_swa > 0 ? kv_swa : nullptr); a.idx2 = k_swa > 0 ? idx_swa : nullptr;
-  a.k2 = k_swa;
-  a.out = out; a.lse = lse; a.err_flag = err_flag;
-  a.n_splits = mla_num_splits(B, H, k + k_swa);
-  a.part_o = L.part_o; a.part_lse = L.part_lse;
-  return status_of(sparse_mla_launch(a, s));
+size_t dsa_decode_host_workspace_size(int B, int64_t max_seq_len, int k, int H_I, int d_idx,
+                                      int idx_dtype, int H, int D, int Dv, int k_swa) {
+  if (B < 0 || max_seq_len < 0 || k < 0 || H_I < 0 || d_idx < 0 || H < 0 || D < 0 || Dv < 0 ||
+      k_swa < 0)
+    return 0;
+  return host_staging(B, max_seq_len, k, H_I, d_idx, idx_dtype, H, D, Dv, k_swa, nullptr).bytes;
+}
+
+int dsa_decode_host(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
+                    const void *k_idx, const float *k_scale, int64_t k_rows, const float *h_w,
+                    int H_I, int d_idx, int B, const int32_t *h_seq_lens,
+                    const int32_t *h_slot_base, int64_t max_seq_len, int k, const void *h_q,
+                    int H, int D, int Dv, float softmax_scale, const dsa_kv_pool *kv,
+                    const dsa_kv_pool *kv_swa, const int32_t *h_idx_swa, int k_swa,
+                    int32_t *h_idx_out, void *h_out, float *h_lse, void *ws, size_t ws_bytes,
+                    int32_t *err_flag, dsa_stream_t stream) {
+  if (B < 0 || max_seq_len < 0 || k_swa < 0) return DSA_ERR_INVALID_ARG;
+  if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (idx_dtype != DSA_IDX_FP8_E4M3 && idx_dtype != DSA_IDX_BF16) return DSA_ERR_UNSUPPORTED;
+  if (B == 0) return DSA_OK;
+  if (!h_q_idx || !h_w || !h_seq_lens || !h_slot_base || !h_q || !h_out || !h_lse)
+    return DSA_ERR_INVALID_ARG;
+  if (idx_dtype == DSA_IDX_FP8_E4M3 && !h_q_scale) return DSA_ERR_INVALID_ARG;
+  if (k_swa > 0 && !h_idx_swa) return DSA_ERR_INVALID_ARG;
+  if (H_I < 1 || d_idx < 1 || H < 1 || D < 1 || Dv < 1) return DSA_ERR_UNSUPPORTED;
+  const size_t need =
+      dsa_decode_host_workspace_size(B, max_seq_len, k, H_I, d_idx, idx_dtype, H, D, Dv, k_swa);
+  if (!ws || ws_bytes < need) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  const HostStaging S =
+      host_staging(B, max_seq_len, k, H_I, d_idx, idx_dtype, H, D, Dv, k_swa, ws);
+  // the checks of dsa_decode, on the device copies, before anything is enqueued
+  int st = check_indexer(S.q_idx, idx_dtype, h_q_scale ? S.q_scale : nullptr, k_idx, k_scale,
+                         k_rows, S.w, B, H_I, d_idx);
+  if (st != DSA_OK) return st;
+  st = check_mla_shape(S.q, B, H, D, Dv, kv, S.idx_out, k, kv_swa, k_swa > 0 ? S.idx_swa : nullptr,
+                       k_swa, S.out, S.lse, /*need_idx=*/false);
+  if (st != DSA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t qi_bytes = (size_t)B * H_I * d_idx * idx_elem_bytes(idx_dtype);
+  // the inputs, in stream order ahead of the step (a copy on a second stream
+  // overlapping the index score was measured slower: the wait for it cost the
+  // top-k its early launch), then the step, then the outputs
+  bool ok = cudaMemcpyAsync(S.q, h_q, (size_t)B * H * D * 2, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+            (k_swa == 0 || cudaMemcpyAsync(S.idx_swa, h_idx_swa, (size_t)B * k_swa * 4,
+                                           cudaMemcpyHostToDevice, s) == cudaSuccess) &&
+            cudaMemcpyAsync(S.seq_lens, h_seq_lens, (size_t)B * 4, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+            cudaMemcpyAsync(S.slot_base, h_slot_base, (size_t)B * 4, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+            cudaMemcpyAsync(S.q_idx, h_q_idx, qi_bytes, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+            cudaMemcpyAsync(S.w, h_w, (size_t)B * H_I * 4, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+            (!h_q_scale || cudaMemcpyAsync(S.q_scale, h_q_scale, (size_t)B * H_I * 4,
+                                           cudaMemcpyHostToDevice, s) == cudaSuccess);
+  if (!ok) return DSA_ERR_CUDA;
+  st = decode_enqueue(S.q_idx, idx_dtype, h_q_scale ? S.q_scale : nullptr, k_idx, k_scale,
+                      k_rows, S.w, H_I, d_idx, B, S.seq_lens, S.slot_base, max_seq_len, k, S.q,
+                      H, D, Dv, softmax_scale, kv, kv_swa, k_swa > 0 ? S.idx_swa : nullptr, k_swa,
+                      S.idx_out, S.out, S.lse, S.dec_ws, err_flag, s);
+  if (st != DSA_OK) return st;
+  ok = (!h_idx_out || cudaMemcpyAsync(h_idx_out, S.idx_out, (size_t)B * k * 4,
+                                      cudaMemcpyDeviceToHost, s) == cudaSuccess) &&
+       cudaMemcpyAsync(h_out, S.out, (size_t)B * H * Dv * 2, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+       cudaMemcpyAsync(h_lse, S.lse, (size_t)B * H * 4, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+  return ok ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -59,6 +59,13 @@ _SIGS = {
                            c_p, c_i32, c_i32, c_i32, c_f32, ctypes.POINTER(DsaKvPool),
                            ctypes.POINTER(DsaKvPool), c_p, c_i32,
                            c_p, c_p, c_p, c_p, c_sz, c_p, c_p]),
+    "dsa_decode_host_workspace_size": (c_sz, [c_i32, c_i64, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                              c_i32, c_i32, c_i32]),
+    "dsa_decode_host": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_i32, c_i32,
+                                c_i32, c_p, c_p, c_i64, c_i32,
+                                c_p, c_i32, c_i32, c_i32, c_f32, ctypes.POINTER(DsaKvPool),
+                                ctypes.POINTER(DsaKvPool), c_p, c_i32,
+                                c_p, c_p, c_p, c_p, c_sz, c_p, c_p]),
 }
 
 _lib = None
@@ -102,6 +109,17 @@ def _ptr(t: Optional[torch.Tensor]):
         return None
     if not t.is_cuda:
         raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _hptr(t: Optional[torch.Tensor]):
+    """Host pointer of a contiguous CPU tensor (pinned memory lets the copies overlap)."""
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("expected a host (CPU) tensor")
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
     return ctypes.c_void_p(t.data_ptr())
@@ -229,6 +247,46 @@ def dsa_decode(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, slot_base
                            _ref(s2), _ptr(idx_swa), k_swa, _ptr(idx_out), _ptr(out), _ptr(lse),
                            _ptr(ws), ws.numel(), _ptr(err_flag), _stream())
     _check(st, "dsa_decode")
+    return idx_out, out, lse
+
+
+def dsa_decode_host_workspace_size(B, max_seq_len, k, H_I, d_idx, idx_dtype, H, D, Dv,
+                                   k_swa=0) -> int:
+    return int(load().dsa_decode_host_workspace_size(B, int(max_seq_len), k, H_I, d_idx, idx_dtype,
+                                                     H, D, Dv, k_swa))
+
+
+def dsa_decode_host(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, slot_base,
+                    max_seq_len: int, k: int, q, softmax_scale: float, kv: _inp.KVPool,
+                    kv_swa=None, idx_swa=None, idx_out=None, out=None, lse=None, ws=None,
+                    err_flag=None):
+    """dsa_decode with the step's inputs and outputs in host memory (see
+    dsa_decode_host).  q_idx, q_scale, w, seq_lens, slot_base, q, idx_swa are
+    CPU tensors (pinned for overlap); k_idx, k_scale and the pools are CUDA
+    tensors.  Returns host (idx_out, out, lse), allocated pinned when not
+    given; they hold the results once the current stream has passed the call."""
+    B, H_I, d_idx = q_idx.shape
+    _, H, D = q.shape
+    Dv = kv.d_nope if kv.format != _inp.KV_BF16 else 512
+    k_swa = 0 if idx_swa is None else idx_swa.shape[1]
+    if idx_out is None:
+        idx_out = torch.empty((B, k), dtype=torch.int32).pin_memory()
+    if out is None:
+        out = torch.empty((B, H, Dv), dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    need = dsa_decode_host_workspace_size(B, max_seq_len, k, H_I, d_idx, idx_dtype, H, D, Dv,
+                                          k_swa)
+    if ws is None:
+        ws = workspace(need, k_idx.device)
+    s1, s2 = kv_pool_struct(kv), kv_pool_struct(kv_swa)
+    st = load().dsa_decode_host(_hptr(q_idx), idx_dtype, _hptr(q_scale), _ptr(k_idx),
+                                _ptr(k_scale), k_idx.shape[0], _hptr(w), H_I, d_idx, B,
+                                _hptr(seq_lens), _hptr(slot_base), int(max_seq_len), k, _hptr(q),
+                                H, D, Dv, float(softmax_scale), _ref(s1), _ref(s2),
+                                _hptr(idx_swa), k_swa, _hptr(idx_out), _hptr(out), _hptr(lse),
+                                _ptr(ws), ws.numel(), _ptr(err_flag), _stream())
+    _check(st, "dsa_decode_host")
     return idx_out, out, lse
 
 

@@ -235,6 +235,39 @@ int dsa_decode(const void *q_idx, int idx_dtype, const float *q_scale,
                int32_t *idx_out, void *out, float *lse,
                void *ws, size_t ws_bytes, int32_t *err_flag, dsa_stream_t stream);
 
+/*
+ * dsa_decode_host -- dsa_decode with the step's inputs and outputs in HOST
+ * memory; the model state (index-k cache k_idx / k_scale, the KV pools) stays
+ * in device memory.  The same computation and kernels as dsa_decode, with
+ * the copies enqueued around them on `stream`: h_q, h_idx_swa, h_seq_lens,
+ * h_slot_base, h_q_idx, h_w, h_q_scale into the workspace, then the step,
+ * then h_idx_out (optional), h_out and h_lse back.
+ * Host pointers (h_*) are read and written by the copies when `stream` gets
+ * there: they must stay valid until then, as with cudaMemcpyAsync.  Page-
+ * locked (pinned) host memory lets the copies run asynchronously; pageable
+ * memory is accepted and the CUDA runtime then stages the copies itself.
+ * Shapes, types and limits are those of dsa_decode.  err_flag, if given, is
+ * a device pointer.  No host synchronisation: the outputs are in host memory
+ * once `stream` has passed this call (e.g. after cudaStreamSynchronize).
+ * Workspace: dsa_decode_host_workspace_size(...) bytes of device memory (the
+ * decode workspace plus device copies of the inputs and outputs); calls on
+ * the same stream may share it, a call on another stream may not until this
+ * one has completed.
+ * Returns a status as dsa_decode.
+ */
+size_t dsa_decode_host_workspace_size(int B, int64_t max_seq_len, int k, int H_I, int d_idx,
+                                      int idx_dtype, int H, int D, int Dv, int k_swa);
+int dsa_decode_host(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
+                    const void *k_idx, const float *k_scale, int64_t k_rows,
+                    const float *h_w, int H_I, int d_idx,
+                    int B, const int32_t *h_seq_lens, const int32_t *h_slot_base,
+                    int64_t max_seq_len, int k,
+                    const void *h_q, int H, int D, int Dv, float softmax_scale,
+                    const dsa_kv_pool *kv,
+                    const dsa_kv_pool *kv_swa, const int32_t *h_idx_swa, int k_swa,
+                    int32_t *h_idx_out, void *h_out, float *h_lse,
+                    void *ws, size_t ws_bytes, int32_t *err_flag, dsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
