@@ -85,12 +85,39 @@ __device__ __forceinline__ RowInfo row_info(const IndexScoreArgs &a, int t) {
   return r;
 }
 
+__device__ __forceinline__ int64_t tiles_of(const RowInfo &r) {
+  return (r.len + kTileKeys - 1) / kTileKeys;
+}
+
+// Walks a CTA's share of the valid (row, key tile) units in row-major order,
+// skipping rows without keys.  next() may be called only while units remain.
+struct TileIter {
+  int t;
+  int64_t j, ntile;
+  RowInfo ri;
+  __device__ __forceinline__ void start(const IndexScoreArgs &a, int t0, int64_t j0) {
+    t = t0;
+    j = j0;
+    ri = row_info(a, t);
+    ntile = tiles_of(ri);
+  }
+  __device__ __forceinline__ void next(const IndexScoreArgs &a) {
+    if (++j == ntile) {
+      j = 0;
+      do {
+        ++t;
+        ri = row_info(a, t);
+        ntile = tiles_of(ri);
+      } while (ntile == 0);
+    }
+  }
+};
+
 template <bool FP8, int N, int KB>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap qmap,
-                      const __grid_constant__ CUtensorMap smap, IndexScoreArgs a,
-                      int64_t tiles_per_row, int64_t tiles_per_cta) {
+                      const __grid_constant__ CUtensorMap smap, IndexScoreArgs a) {
   extern __shared__ unsigned char smem_raw[];
   const IdxSmem L = idx_smem_layout(N, KB);
   unsigned char *base = reinterpret_cast<unsigned char *>(
@@ -147,15 +174,69 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  // Launched as a dependent of the histogram's zeroing: with inputs_ready
-  // (fused decode) only the epilogue, which adds into the histogram, waits
-  // for it; otherwise every role waits before touching anything.
-  if (!a.inputs_ready || warp >= 2) pdl_wait();
-  pdl_trigger();   // the next kernel may be placed as SMs free up; it waits for us
+  // Launched as a dependent of the previous kernel (the fused decode: the
+  // histogram's zeroing).  With inputs_ready only the epilogue, which adds
+  // into the histogram, waits for it; otherwise every role waits before
+  // touching anything, the row ranges included.
+  if (!a.inputs_ready) pdl_wait();
 
-  const int64_t total = (int64_t)a.T * tiles_per_row;
-  const int64_t v0 = (int64_t)blockIdx.x * tiles_per_cta;
-  const int64_t v1 = min(total, v0 + tiles_per_cta);
+  // ---- this CTA's share of the valid tiles.  Rows differ in length (causal
+  // prefill: row t has t + 1 keys; ragged decode batches), so the units are
+  // split evenly by count: every thread sums the tiles of a run of rows, a
+  // block scan gives the total and each run's start, and the run holding
+  // this CTA's first unit locates it.
+  __shared__ int64_t s_warp[kThreads / 32];
+  __shared__ int s_t0;
+  __shared__ int64_t s_j0, s_count;
+  {
+    const int R = (a.T + kThreads - 1) / kThreads;
+    const int rlo = min(a.T, (int)threadIdx.x * R), rhi = min(a.T, rlo + R);
+    int64_t mine = 0;
+#pragma unroll 4
+    for (int t = rlo; t < rhi; ++t) {
+      const RowInfo r = row_info(a, t);
+      if (r.bad && blockIdx.x == 0) raise_flag(a.err_flag, DSA_DEVERR_INDEX_RANGE);
+      mine += tiles_of(r);
+    }
+    int64_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    if (threadIdx.x == 0) s_count = 0;
+    __syncthreads();
+    int64_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const int64_t x = s_warp[w];
+      if (w < warp) before += x;
+      total += x;
+    }
+    const int64_t pre = before + incl - mine;      // units before this thread's rows
+    const int64_t u0 = total * (int64_t)blockIdx.x / gridDim.x;
+    const int64_t u1 = total * ((int64_t)blockIdx.x + 1) / gridDim.x;
+    if (u0 < u1 && pre <= u0 && u0 < pre + mine) {
+      int64_t acc = pre;
+      for (int t = rlo; t < rhi; ++t) {
+        const int64_t n = tiles_of(row_info(a, t));
+        if (u0 < acc + n) {
+          s_t0 = t;
+          s_j0 = u0 - acc;
+          s_count = u1 - u0;
+          break;
+        }
+        acc += n;
+      }
+    }
+    __syncthreads();
+  }
+  const int64_t count = s_count;
+  const int t_first = count > 0 ? s_t0 : 0;
+  const int64_t j_first = count > 0 ? s_j0 : 0;
+  if (a.inputs_ready && warp >= 2) pdl_wait();
+  pdl_trigger();   // the next kernel may be placed as SMs free up; it waits for us
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -178,20 +259,12 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       uint32_t sphase = 0;
       uint32_t s_issued = 0, s_last = 0;
       bool ok = true;
-      RowInfo ri{0, 0, false};
-      int ri_t = -1;
-      // tile v = t * tiles_per_row + j: one division up front, then counters
-      int t_it = (int)(v0 / tiles_per_row);
-      int64_t j_it = v0 - (int64_t)t_it * tiles_per_row;
-      for (int64_t v = v0; v < v1 && ok;
-           ++v, (++j_it == tiles_per_row ? (j_it = 0, ++t_it) : 0)) {
-        const int t = t_it;
-        const int64_t j = j_it;
-        if (t != ri_t) {
-          ri = row_info(a, t);
-          ri_t = t;
-        }
-        if (j * kTileKeys >= ri.len) continue;
+      TileIter it;
+      if (count > 0) it.start(a, t_first, j_first);
+      for (int64_t n = 0; n < count && ok; ++n, (n < count ? it.next(a) : (void)0)) {
+        const int t = it.t;
+        const int64_t j = it.j;
+        const RowInfo &ri = it.ri;
         if (t != cur_t) {
           if (cur_t >= 0) {
             qs ^= 1;
@@ -255,20 +328,10 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       int acc = 0;
       uint32_t acc_phase = 0;
       bool any = false;
-      RowInfo ri{0, 0, false};
-      int ri_t = -1;
-      // tile v = t * tiles_per_row + j: one division up front, then counters
-      int t_it = (int)(v0 / tiles_per_row);
-      int64_t j_it = v0 - (int64_t)t_it * tiles_per_row;
-      for (int64_t v = v0; v < v1;
-           ++v, (++j_it == tiles_per_row ? (j_it = 0, ++t_it) : 0)) {
-        const int t = t_it;
-        const int64_t j = j_it;
-        if (t != ri_t) {
-          ri = row_info(a, t);
-          ri_t = t;
-        }
-        if (j * kTileKeys >= ri.len) continue;
+      TileIter it;
+      if (count > 0) it.start(a, t_first, j_first);
+      for (int64_t n = 0; n < count; ++n, (n < count ? it.next(a) : (void)0)) {
+        const int t = it.t;
         if (t != cur_t) {
           if (cur_t >= 0) {
             tc::mma_commit(&qempty[qs]);  // the old query slot is free once its MMAs finish
@@ -330,21 +393,14 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     int cur_t = -1;
     bool hist_on = false;
     bool dead = false;
-    RowInfo ri{0, 0, false};
     float wq[N];
-    int64_t n = 0;                           // valid tiles so far (same sequence as the producer)
-    // tile v = t * tiles_per_row + j: one division up front, then counters
-    int t_it = (int)(v0 / tiles_per_row);
-    int64_t j_it = v0 - (int64_t)t_it * tiles_per_row;
-    for (int64_t v = v0; v < v1;
-         ++v, (++j_it == tiles_per_row ? (j_it = 0, ++t_it) : 0)) {
-      const int t = t_it;
-      const int64_t j = j_it;
-      if (t != cur_t) {
-        ri = row_info(a, t);
-        if (ri.bad && j == 0 && et == 0) raise_flag(a.err_flag, DSA_DEVERR_INDEX_RANGE);
-      }
-      if (j * kTileKeys >= ri.len) continue;
+    TileIter it;
+    if (count > 0) it.start(a, t_first, j_first);
+    // unit n of this CTA (the producer and the issuer walk the same sequence)
+    for (int64_t n = 0; n < count; ++n, (n < count ? it.next(a) : (void)0)) {
+      const int t = it.t;
+      const int64_t j = it.j;
+      const RowInfo &ri = it.ri;
       if (t != cur_t) {
         if (hist_on) {  // flush the previous row's bin counts (both groups)
           tc::named_bar_sync(1, kEpiThreads);
@@ -370,7 +426,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         cur_t = t;
       }
-      const int64_t my_n = n++;
+      const int64_t my_n = n;
       if (dead || (int)(my_n % kGroups) != group) continue;
       const int acc = (int)(my_n % kAcc);
       const uint32_t acc_phase = (uint32_t)((my_n / kAcc) & 1);
@@ -435,17 +491,17 @@ cudaError_t launch_tc(const IndexScoreArgs &a, cudaStream_t s) {
   if (FP8 && !make_tmap_1d(&smap, a.k_scale, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
                            (uint64_t)a.k_rows, kScBox))
     return cudaErrorInvalidValue;
+  // at most T * ceil(max_len / 128) valid tiles; each CTA takes an equal
+  // share of the valid ones (computed in the kernel)
   const int64_t tiles_per_row = (a.max_len + kTileKeys - 1) / kTileKeys;
   const int64_t total = (int64_t)a.T * tiles_per_row;
   const int64_t grid = std::min<int64_t>((int64_t)kCtasPerSm * num_sms(), total);
-  const int64_t per = (total + grid - 1) / grid;
   const IdxSmem L = idx_smem_layout(N, KB);
   const size_t smem = L.total + 1024;
   auto kern = index_score_tc_kernel<FP8, N, KB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, kmap, qmap, smap, a,
-                    tiles_per_row, per);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, kmap, qmap, smap, a);
 }
 
 template <bool FP8, int KB>
