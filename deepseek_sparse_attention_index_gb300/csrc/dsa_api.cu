@@ -49,6 +49,8 @@ PoolDev to_dev(const dsa_kv_pool *kv) {
 int check_indexer(const void *q_idx, int idx_dtype, const float *q_scale, const void *k_idx,
                   const float *k_scale, int64_t k_rows, const float *w, int T, int H_I, int d) {
   if (T < 0 || k_rows < 0) return DSA_ERR_INVALID_ARG;
+  // key rows are tensor-map coordinates (32-bit signed) in the kernel
+  if (k_rows > INT32_MAX || (int64_t)T * H_I > INT32_MAX) return DSA_ERR_UNSUPPORTED;
   if (T > 0 && (!q_idx || !k_idx || !w)) return DSA_ERR_INVALID_ARG;
   if (H_I < 1 || H_I > DSA_MAX_INDEX_HEADS || (H_I % 8)) return DSA_ERR_UNSUPPORTED;
   if (idx_dtype == DSA_IDX_FP8_E4M3) {

@@ -116,7 +116,8 @@ int dsa_abi_version(void);
  * bf16).
  *   q_idx     [T, H_I, d]  bf16 or e4m3 bytes (idx_dtype)
  *   q_scale   [T, H_I]     fp32, fp8 only (NULL for bf16)
- *   k_idx     [k_rows, d]  same type as q_idx (the index-k cache)
+ *   k_idx     [k_rows, d]  same type as q_idx (the index-k cache); k_rows and
+ *             T * H_I below 2^31 (else DSA_ERR_UNSUPPORTED)
  *   k_scale   [k_rows]     fp32, fp8 only (NULL for bf16)
  *   w         [T, H_I]     fp32 head weights (any sign)
  *   row_start, row_end [T] int32 key rows [row_start, row_end) of k_idx;

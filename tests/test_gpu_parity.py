@@ -63,6 +63,25 @@ def test_index_score_integer_grid_bit_exact(H_I, d):
     assert flag.item() == 0
 
 
+def test_index_score_causal_rows_bit_exact():
+    """One causal segment (row t sees keys [0, t]): consecutive rows are scored
+    against shared key tiles, each keeping its own range; odd T leaves a
+    partial last group."""
+    T = 1001
+    ind = I.indexer_grid_bf16(T, T, 64, 128, seed=3, device="cuda")
+    rs = torch.zeros(T, dtype=torch.int32, device="cuda")
+    re = torch.arange(1, T + 1, dtype=torch.int32, device="cuda")
+    flag = _flag()
+    sc = ops.dsa_index_score(ind["q_idx"], 0, None, ind["k_idx"], None, ind["w"], rs, re, T,
+                             err_flag=flag).cpu().numpy()
+    inp = _ind_np(ind)
+    for t in list(range(0, T, 37)) + [126, 127, 128, 129, 255, 256, T - 2, T - 1]:
+        ref = _oracle_scores(inp, t, 0, t + 1)
+        assert np.array_equal(sc[t, :t + 1].astype(np.float64), ref), t
+        assert np.isnan(sc[t, t + 1:]).all(), t
+    assert flag.item() == 0
+
+
 def test_index_score_fp8_prefill_ranges():
     case = I.prefill_case([1, 1, 100, 198, 700], k=64, H=8, device="cuda")
     ind = case.indexer
