@@ -105,6 +105,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over the ranks of the default process group (x itself
+    for one rank).  Each rank serves its own batch of requests (weak
+    scaling), so a step of the whole job takes as long as its slowest rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Seed of the synthetic request batch rank `rank` serves: the ranks'
+    batches are different requests, not copies."""
+    return int(rank)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world):
@@ -121,7 +141,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     Bsz, N, k = args.batch, args.context, 2048
-    case = I.decode_sweep(Bsz, N, device=dev, seed=rank)
+    case = I.decode_sweep(Bsz, N, device=dev, seed=rank_seed(rank))
     ind = case.indexer
     H, Dv = case.H, case.Dv
     ws = ops.workspace(ops.dsa_decode_workspace_size(Bsz, N, k, H, Dv), dev)
@@ -166,11 +186,7 @@ def run_ours(args, rank, world):
     wall = time.perf_counter() - t_wall
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     us_per_step = total_ms * 1000.0 / args.steps
 
     # ---- staged pass: the three stages as separate entry points, events around each
@@ -257,11 +273,7 @@ def run_ours(args, rank, world):
         e2e_step()
         torch.cuda.synchronize()
         e2e_ms.append((time.perf_counter() - t0) * 1000.0)
-    e2e_us = 1000.0 * statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_us], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_us = float(t.item())
+    e2e_us = max_over_ranks(1000.0 * statistics.mean(e2e_ms), world, dev)
 
     splits = 1 if ops.dsa_sparse_mla_workspace_size(Bsz, H, Dv, k, 0) == 0 else 2
     launches_per_step = 1 + 1 + 1 + 1 + (1 if splits > 1 else 0)
