@@ -386,6 +386,34 @@ def decode_sweep(B: int, N: int, device="cpu", seed=0) -> DecodeCase:
                        seed=seed, device=device)
 
 
+def multi_token_decode(B: int, Q: int, N: int, device="cpu", seed=0, k=2048, H=64,
+                       idx_kind="fp8") -> DecodeCase:
+    """Decode with Q query tokens per request (speculative verification):
+    request b's context has N positions, the last Q of them the new tokens.
+    Query row b*Q + i is new token i: it sees positions [0, N - Q + 1 + i) of
+    its request (causal among the new tokens) at the request's slots.  The
+    rows share their request's slot base, so the fused decode serves them as
+    B*Q rows.  Indexer 64 x 128 (fp8, or the bf16 integer grid), sparse MLA
+    H heads over bf16 576-wide rows."""
+    assert 1 <= Q <= N
+    T = B * Q
+    S_total = B * N
+    if idx_kind == "fp8":
+        ind = indexer_fp8(T, S_total, 64, 128, seed, device)
+    else:
+        ind = indexer_grid_bf16(T, S_total, 64, 128, seed, device)
+    kv = kv_bf16_pool(S_total, seed, 5, device)
+    gq = _gen(seed, 4, device)
+    q = to_bf16(torch.randn((T, H, 576), generator=gq, device=device)).contiguous()
+    lens = [N - Q + 1 + i for b in range(B) for i in range(Q)]
+    base = [b * N for b in range(B) for i in range(Q)]
+    return DecodeCase("multi_token_b%d_q%d_n%d" % (B, Q, N), T,
+                      torch.tensor(lens, dtype=torch.int32, device=device),
+                      torch.tensor(base, dtype=torch.int32, device=device), N, 64, 128, ind,
+                      k, H, 576, 512, 1.0 / math.sqrt(192.0), q, kv,
+                      meta={"requests": B, "tokens_per_request": Q})
+
+
 def packed_long_decode(N=1 << 20, device="cpu", seed=0, swa=128, topk=1024) -> DecodeCase:
     """Batch 1, context N on packed fp8_ds_mla pages of 256 tokens; two loops:
     the SWA window (its own packed cache) and the top-k list (indexer 64 x 128

@@ -324,6 +324,29 @@ def test_decode_is_deterministic():
             assert torch.equal(a, b)
 
 
+def test_multi_token_decode_rows_share_a_request():
+    """Q new tokens per request (speculative verification): B*Q rows that share
+    their request's slot base; token i sees the context up to itself."""
+    case = I.multi_token_decode(3, 4, 5000, device="cuda")
+    flag = _flag()
+    idx, out, lse = ops.decode_case(case, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    _check_decode(case, idx, out, lse, range(case.B))
+    # each token's selection stays inside its own causal prefix
+    pos = idx.cpu().numpy() - case.slot_base.cpu().numpy()[:, None]
+    lens = case.seq_lens.cpu().numpy()
+    for r in range(case.B):
+        sel = pos[r][idx[r].cpu().numpy() >= 0]
+        assert sel.max() < lens[r], r
+
+
+def test_multi_token_decode_grid_bit_exact():
+    case = I.multi_token_decode(2, 3, 3000, device="cuda", idx_kind="bf16_grid")
+    idx, out, lse = ops.decode_case(case)
+    _check_decode(case, idx, out, lse, range(case.B), bit_exact=True)
+
+
 def test_decode_sweep_full_size_sampled():
     """Batch 32 x 128k context, the bench workload; three requests checked."""
     case = I.decode_sweep(32, 131072, device="cuda")
