@@ -187,19 +187,32 @@ def kth_score(scores: np.ndarray, k: int) -> float:
 # Sparse MLA
 # --------------------------------------------------------------------------
 
-def sparse_mla_one(q_t: np.ndarray, rows: np.ndarray, softmax_scale: float, Dv: int):
+def sparse_mla_one(q_t: np.ndarray, rows: np.ndarray, softmax_scale: float, Dv: int,
+                   sinks: np.ndarray | None = None):
     """Absorbed-MLA attention of one query token over already-gathered rows.
 
     q_t: [H, D] float64; rows: [n, D] float64 (valid rows only, duplicates
-    count once per occurrence).  Returns out [H, Dv], lse [H] (natural log)."""
+    count once per occurrence).  Returns out [H, Dv], lse [H] (natural log).
+
+    sinks (optional, [H]): a per-head logit in the units of the scores
+    s_j = softmax_scale * q . K_j that joins the softmax denominator and
+    contributes no value (the "sink folded in" of the Miles sparse-attention
+    pull request's forward notes): out = sum_j e^{s_j} V_j / (sum_j e^{s_j} +
+    e^{sink}), lse = ln(sum_j e^{s_j} + e^{sink})."""
     H = q_t.shape[0]
     if rows.shape[0] == 0:
-        return np.zeros((H, Dv)), np.full(H, -np.inf)
+        lse0 = np.full(H, -np.inf) if sinks is None else np.asarray(sinks, dtype=np.float64).copy()
+        return np.zeros((H, Dv)), lse0
     s = softmax_scale * (q_t @ rows.T)          # [H, n]
-    m = s.max(axis=1, keepdims=True)
-    e = np.exp(s - m)
-    lse = m[:, 0] + np.log(e.sum(axis=1))
-    p = np.exp(s - lse[:, None])
+    if sinks is not None:
+        # the sink is one more logit in every head's denominator
+        s_all = np.concatenate([s, np.asarray(sinks, dtype=np.float64)[:, None]], axis=1)
+    else:
+        s_all = s
+    m = s_all.max(axis=1, keepdims=True)
+    m = np.where(np.isfinite(m), m, 0.0)
+    lse = m[:, 0] + np.log(np.exp(s_all - m).sum(axis=1))
+    p = np.exp(s - lse[:, None])                # the rows' weights (the sink carries none)
     return p @ rows[:, :Dv], lse
 
 
@@ -211,10 +224,12 @@ def gather_valid(pool: dict, idx_row) -> np.ndarray:
 
 
 def sparse_mla(q: np.ndarray, pool: dict, idx: np.ndarray, softmax_scale: float, Dv: int,
-               pool_extra: dict | None = None, idx_extra: np.ndarray | None = None):
+               pool_extra: dict | None = None, idx_extra: np.ndarray | None = None,
+               sinks: np.ndarray | None = None):
     """Sparse MLA for T tokens.  q: [T, H, D] float64; idx: [T, k] slots into
     ``pool`` (-1 masked); optional second list idx_extra into pool_extra, in
-    the same softmax.  Returns out [T, H, Dv], lse [T, H]."""
+    the same softmax; optional per-head sinks (see sparse_mla_one).  Returns
+    out [T, H, Dv], lse [T, H]."""
     T, H, _ = q.shape
     out = np.zeros((T, H, Dv))
     lse = np.zeros((T, H))
@@ -222,7 +237,7 @@ def sparse_mla(q: np.ndarray, pool: dict, idx: np.ndarray, softmax_scale: float,
         rows = gather_valid(pool, idx[t])
         if idx_extra is not None:
             rows = np.concatenate([rows, gather_valid(pool_extra, idx_extra[t])], axis=0)
-        out[t], lse[t] = sparse_mla_one(q[t], rows, softmax_scale, Dv)
+        out[t], lse[t] = sparse_mla_one(q[t], rows, softmax_scale, Dv, sinks)
     return out, lse
 
 

@@ -311,6 +311,53 @@ def test_sparse_mla_invariants():
     assert np.allclose(l3, (qz[:, 6:].sum(axis=1)) + np.log(5), atol=1e-13)
 
 
+# ---- attention sinks (a per-head logit in the denominator, no value)
+
+def _sink_case(seed=7, H=4, n=37, D=576, Dv=512):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((H, D))
+    rows = rng.standard_normal((n, D))
+    sinks = rng.standard_normal(H) * 2.0
+    return q, rows, sinks, 1.0 / math.sqrt(192.0), Dv
+
+
+def test_sink_minus_inf_is_no_sink():
+    q, rows, _, sc, Dv = _sink_case()
+    out0, lse0 = O.sparse_mla_one(q, rows, sc, Dv)
+    out1, lse1 = O.sparse_mla_one(q, rows, sc, Dv, np.full(q.shape[0], -np.inf))
+    assert np.allclose(out0, out1, rtol=0, atol=1e-14) and np.allclose(lse0, lse1, rtol=0, atol=1e-14)
+
+
+def test_sink_equals_an_extra_key_with_zero_value():
+    """Brute force: for each head, one more row whose value part (the leading
+    Dv columns) is zero and whose RoPE part scores exactly the sink logit gives
+    the same result as the sink, through the plain (sink-free) attention."""
+    q, rows, sinks, sc, Dv = _sink_case()
+    out_s, lse_s = O.sparse_mla_one(q, rows, sc, Dv, sinks)
+    for h in range(q.shape[0]):
+        qr = q[h, Dv:]
+        extra = np.zeros((1, q.shape[1]))
+        extra[0, Dv:] = sinks[h] * qr / (sc * qr @ qr)    # sc * q_h . extra = sinks[h]
+        out_e, lse_e = O.sparse_mla_one(q[h:h + 1], np.concatenate([rows, extra]), sc, Dv)
+        assert np.allclose(out_e[0], out_s[h], rtol=1e-12, atol=1e-13), h
+        assert abs(lse_e[0] - lse_s[h]) < 1e-12, h
+
+
+def test_sink_one_row_closed_form():
+    q, rows, sinks, sc, Dv = _sink_case(n=1)
+    out, lse = O.sparse_mla_one(q, rows, sc, Dv, sinks)
+    s = sc * (q @ rows[0])
+    assert np.allclose(lse, np.logaddexp(s, sinks), rtol=0, atol=1e-13)
+    weight = 1.0 / (1.0 + np.exp(sinks - s))          # e^s / (e^s + e^sink)
+    assert np.allclose(out, weight[:, None] * rows[0, :Dv][None, :], rtol=1e-13, atol=1e-14)
+
+
+def test_sink_all_masked_row():
+    q, rows, sinks, sc, Dv = _sink_case()
+    out, lse = O.sparse_mla_one(q, rows[:0], sc, Dv, sinks)
+    assert not out.any() and np.array_equal(lse, sinks)
+
+
 def test_split_combine_equals_whole():
     rng = np.random.default_rng(5)
     rows = rng.standard_normal((100, 16)) * 2
