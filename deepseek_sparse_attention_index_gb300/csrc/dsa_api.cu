@@ -119,7 +119,8 @@ int decode_enqueue(const void *q_idx, int idx_dtype, const float *q_scale, const
                    const int32_t *seq_lens, const int32_t *slot_base, int64_t max_seq_len, int k,
                    const void *q, int H, int D, int Dv, float softmax_scale, const dsa_kv_pool *kv,
                    const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa, int32_t *idx_out,
-                   void *out, float *lse, void *ws, int32_t *err_flag, cudaStream_t s) {
+                   void *out, float *lse, void *ws, int32_t *err_flag, cudaStream_t s,
+                   const dsa_attn_opts *opts = nullptr) {
   DecodeLayout L = decode_layout(B, max_seq_len, k, H, Dv, k_swa, ws);
   const int64_t ld = scores_ld(max_seq_len);
   int32_t *idx = idx_out ? idx_out : L.idx;
@@ -146,6 +147,8 @@ int decode_enqueue(const void *q_idx, int idx_dtype, const float *q_scale, const
   a.kv2 = to_dev(k_swa > 0 ? kv_swa : nullptr); a.idx2 = k_swa > 0 ? idx_swa : nullptr;
   a.k2 = k_swa;
   a.out = out; a.lse = lse; a.err_flag = err_flag;
+  a.sinks = opts ? opts->sinks : nullptr;
+  a.lse_log2 = opts ? opts->lse_log2 != 0 : 0;
   a.n_splits = mla_num_splits(B, H, k + k_swa);
   a.part_o = L.part_o; a.part_lse = L.part_lse;
   return status_of(sparse_mla_launch(a, s));
@@ -258,6 +261,16 @@ int dsa_sparse_mla_fwd(const void *q, int T, int H, int D, int Dv, float softmax
                        const dsa_kv_pool *kv_extra, const int32_t *idx_extra, int k2,
                        void *out, float *lse, void *ws, size_t ws_bytes, int32_t *err_flag,
                        dsa_stream_t stream) {
+  return dsa_sparse_mla_fwd_ex(q, T, H, D, Dv, softmax_scale, kv, idx, k, kv_extra, idx_extra, k2,
+                               out, lse, ws, ws_bytes, err_flag, nullptr, stream);
+}
+
+int dsa_sparse_mla_fwd_ex(const void *q, int T, int H, int D, int Dv, float softmax_scale,
+                          const dsa_kv_pool *kv, const int32_t *idx, int k,
+                          const dsa_kv_pool *kv_extra, const int32_t *idx_extra, int k2,
+                          void *out, float *lse, void *ws, size_t ws_bytes, int32_t *err_flag,
+                          const dsa_attn_opts *opts, dsa_stream_t stream) {
+  if (opts && opts->reserved != 0) return DSA_ERR_INVALID_ARG;
   int st = check_mla_shape(q, T, H, D, Dv, kv, idx, k, kv_extra, idx_extra, k2, out, lse);
   if (st != DSA_OK) return st;
   if (T == 0) return DSA_OK;
@@ -268,6 +281,8 @@ int dsa_sparse_mla_fwd(const void *q, int T, int H, int D, int Dv, float softmax
   a.kv = to_dev(kv); a.idx = idx; a.k = k;
   a.kv2 = to_dev(k2 > 0 ? kv_extra : nullptr); a.idx2 = k2 > 0 ? idx_extra : nullptr; a.k2 = k2;
   a.out = out; a.lse = lse; a.err_flag = err_flag;
+  a.sinks = opts ? opts->sinks : nullptr;
+  a.lse_log2 = opts ? opts->lse_log2 != 0 : 0;
   a.n_splits = mla_num_splits(T, H, k + k2);
   if (a.n_splits > 1) mla_ws_layout(T, H, Dv, k + k2, ws, &a.part_o, &a.part_lse);
   return status_of(sparse_mla_launch(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -285,6 +300,19 @@ int dsa_decode(const void *q_idx, int idx_dtype, const float *q_scale, const voi
                const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa, int32_t *idx_out,
                void *out, float *lse, void *ws, size_t ws_bytes, int32_t *err_flag,
                dsa_stream_t stream) {
+  return dsa_decode_ex(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, H_I, d_idx, B,
+                       seq_lens, slot_base, max_seq_len, k, q, H, D, Dv, softmax_scale, kv, kv_swa,
+                       idx_swa, k_swa, idx_out, out, lse, ws, ws_bytes, err_flag, nullptr, stream);
+}
+
+int dsa_decode_ex(const void *q_idx, int idx_dtype, const float *q_scale, const void *k_idx,
+                  const float *k_scale, int64_t k_rows, const float *w, int H_I, int d_idx, int B,
+                  const int32_t *seq_lens, const int32_t *slot_base, int64_t max_seq_len, int k,
+                  const void *q, int H, int D, int Dv, float softmax_scale, const dsa_kv_pool *kv,
+                  const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa, int32_t *idx_out,
+                  void *out, float *lse, void *ws, size_t ws_bytes, int32_t *err_flag,
+                  const dsa_attn_opts *opts, dsa_stream_t stream) {
+  if (opts && opts->reserved != 0) return DSA_ERR_INVALID_ARG;
   if (B < 0 || max_seq_len < 0) return DSA_ERR_INVALID_ARG;
   if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
   int st = check_indexer(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, B, H_I, d_idx);
@@ -300,7 +328,7 @@ int dsa_decode(const void *q_idx, int idx_dtype, const float *q_scale, const voi
   return decode_enqueue(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, H_I, d_idx, B,
                         seq_lens, slot_base, max_seq_len, k, q, H, D, Dv, softmax_scale, kv, kv_swa,
                         idx_swa, k_swa, idx_out, out, lse, ws, err_flag,
-                        reinterpret_cast<cudaStream_t>(stream));
+                        reinterpret_cast<cudaStream_t>(stream), opts);
 }
 
 size_t dsa_decode_host_workspace_size(int B, int64_t max_seq_len, int k, int H_I, int d_idx,

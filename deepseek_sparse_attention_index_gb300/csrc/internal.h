@@ -84,6 +84,8 @@ struct MlaArgs {
   int32_t *err_flag;
   int q_ready;               // q was complete before the previous kernel on the stream
                              // began (fused decode): the kernel may load it before pdl_wait
+  const float *sinks;        // [H] per-head sink logits (natural-log units) or NULL
+  int lse_log2;              // the final lse in log2 units
 };
 int mla_num_splits(int T, int H, int k_total);
 size_t mla_ws_bytes(int T, int H, int Dv, int k_total);

@@ -207,8 +207,9 @@ sparse_mla_simt_kernel(MlaArgs a) {
 
   if (hl >= nh) return;
   const int h = h0 + hl;
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+  float inv = l > 0.f ? 1.f / l : 0.f;
+  float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+  if (a.n_splits == 1 && a.sinks) inv = fold_sink(m, l, a.sinks[h], &lse_v);
   if (a.n_splits == 1) {
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + ((size_t)t * a.H + h) * a.Dv;
 #pragma unroll
@@ -219,7 +220,7 @@ sparse_mla_simt_kernel(MlaArgs a) {
       pk.y = pack_bf16x2(o[4 * i + 2] * inv, o[4 * i + 3] * inv);
       *reinterpret_cast<uint2 *>(out + dv) = pk;
     }
-    if (part == 0) a.lse[(size_t)t * a.H + h] = lse_v;
+    if (part == 0) a.lse[(size_t)t * a.H + h] = lse_report(lse_v, a.lse_log2);
   } else {
     const size_t rec = ((size_t)t * a.n_splits + split) * a.H + h;
     float *po = a.part_o + rec * a.Dv;
@@ -245,7 +246,7 @@ constexpr int kCombineBatch = 4;     // splits whose loads are in flight togethe
 __global__ void __launch_bounds__(32 * kCombineWarps)
 mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse, int T,
                    int H, int Dv, int n_splits, __nv_bfloat16 *__restrict__ out,
-                   float *__restrict__ lse) {
+                   float *__restrict__ lse, const float *__restrict__ sinks, int lse_log2) {
   pdl_wait();      // the partials come from the previous kernel
   // one warp per record (t, h); lane l holds the float4 columns l + 32 q
   const int64_t r = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
@@ -304,6 +305,21 @@ mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ p
     }
     mx = bm;
   }
+  if (sinks) {
+    // the head's sink joins the denominator (no value): rescale to a maximum
+    // that covers it (all splits empty and no sink: nothing to fold)
+    const float sg = sinks[h];
+    const float M = fmaxf(mx, sg);
+    if (M != -INFINITY) {
+      const float sc = mx == -INFINITY ? 0.f : __expf(mx - M);
+      tot = tot * sc + __expf(sg - M);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[q].x *= sc; acc[q].y *= sc; acc[q].z *= sc; acc[q].w *= sc;
+      }
+      mx = M;
+    }
+  }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -315,7 +331,7 @@ mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ p
       *reinterpret_cast<uint2 *>(out + r * Dv + 4 * f) = pk;
     }
   }
-  if (lane == 0) lse[r] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  if (lane == 0) lse[r] = lse_report(tot > 0.f ? mx + logf(tot) : -INFINITY, lse_log2);
 }
 
 }  // namespace
@@ -375,7 +391,7 @@ cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s) {
                     dim3((unsigned)((recs + kCombineWarps - 1) / kCombineWarps)),
                     dim3(32 * kCombineWarps), 0, s, (const float *)a.part_o,
                     (const float *)a.part_lse, a.T, a.H, a.Dv, a.n_splits,
-                    static_cast<__nv_bfloat16 *>(a.out), a.lse);
+                    static_cast<__nv_bfloat16 *>(a.out), a.lse, a.sinks, a.lse_log2);
 }
 
 }  // namespace dsa

@@ -709,14 +709,19 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(pfull);
     }
-    // ---- per-head results: 1 / l for the epilogue, and the lse
-    if (head_lane) inv_l[hl] = (l > 0.f) ? 1.f / l : 0.f;
-    if (head_lane && hl < nh) {
-      const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      if (a.n_splits == 1)
-        a.lse[(size_t)t * a.H + h0 + hl] = lse;
-      else
-        a.part_lse[((size_t)t * a.n_splits + split) * a.H + h0 + hl] = lse;
+    // ---- per-head results: 1 / l for the epilogue, and the lse (one piece:
+    // with the head's sink folded in, if any; split pieces: the combine folds it)
+    if (head_lane) {
+      float inv = (l > 0.f) ? 1.f / l : 0.f;
+      float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (a.n_splits == 1 && a.sinks && hl < nh) inv = fold_sink(m, l, a.sinks[h0 + hl], &lse);
+      inv_l[hl] = inv;
+      if (hl < nh) {
+        if (a.n_splits == 1)
+          a.lse[(size_t)t * a.H + h0 + hl] = lse_report(lse, a.lse_log2);
+        else
+          a.part_lse[((size_t)t * a.n_splits + split) * a.H + h0 + hl] = lse;
+      }
     }
     tc::named_bar_arrive(3, 256);    // inv_l is written: warps 4-7 may start
     tc::named_bar_sync(1, 128);

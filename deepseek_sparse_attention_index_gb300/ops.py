@@ -39,6 +39,10 @@ class DsaKvPool(ctypes.Structure):
                 ("block", c_i32), ("d_nope", c_i32), ("d_rope", c_i32)]
 
 
+class DsaAttnOpts(ctypes.Structure):
+    _fields_ = [("sinks", c_p), ("lse_log2", c_i32), ("reserved", c_i32)]
+
+
 _SIGS = {
     "dsa_status_string": (ctypes.c_char_p, [c_i32]),
     "dsa_abi_version": (c_i32, []),
@@ -53,6 +57,15 @@ _SIGS = {
                                    ctypes.POINTER(DsaKvPool), c_p, c_i32,
                                    ctypes.POINTER(DsaKvPool), c_p, c_i32,
                                    c_p, c_p, c_p, c_sz, c_p, c_p]),
+    "dsa_sparse_mla_fwd_ex": (c_i32, [c_p, c_i32, c_i32, c_i32, c_i32, c_f32,
+                                      ctypes.POINTER(DsaKvPool), c_p, c_i32,
+                                      ctypes.POINTER(DsaKvPool), c_p, c_i32,
+                                      c_p, c_p, c_p, c_sz, c_p, ctypes.POINTER(DsaAttnOpts), c_p]),
+    "dsa_decode_ex": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_i32, c_i32,
+                              c_i32, c_p, c_p, c_i64, c_i32,
+                              c_p, c_i32, c_i32, c_i32, c_f32, ctypes.POINTER(DsaKvPool),
+                              ctypes.POINTER(DsaKvPool), c_p, c_i32,
+                              c_p, c_p, c_p, c_p, c_sz, c_p, ctypes.POINTER(DsaAttnOpts), c_p]),
     "dsa_decode_workspace_size": (c_sz, [c_i32, c_i64, c_i32, c_i32, c_i32, c_i32]),
     "dsa_decode": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_i32, c_i32,
                            c_i32, c_p, c_p, c_i64, c_i32,
@@ -194,9 +207,23 @@ def dsa_sparse_mla_workspace_size(T, H, Dv, k, k2=0) -> int:
     return int(load().dsa_sparse_mla_workspace_size(T, H, Dv, k, k2))
 
 
+def _opts(sinks, lse_log2):
+    """Attention options: per-head sink logits (a CUDA fp32 [H] tensor) and the
+    lse in log2 units; None when neither is asked for."""
+    if sinks is None and not lse_log2:
+        return None
+    o = DsaAttnOpts()
+    o.sinks = None if sinks is None else _ptr(sinks).value
+    o.lse_log2 = 1 if lse_log2 else 0
+    o.reserved = 0
+    return o
+
+
 def dsa_sparse_mla_fwd(q, softmax_scale: float, kv: _inp.KVPool, idx, kv_extra=None,
-                       idx_extra=None, out=None, lse=None, ws=None, err_flag=None):
-    """out bf16 [T, H, Dv], lse fp32 [T, H] (see dsa_sparse_mla_fwd)."""
+                       idx_extra=None, out=None, lse=None, ws=None, err_flag=None,
+                       sinks=None, lse_log2=False):
+    """out bf16 [T, H, Dv], lse fp32 [T, H] (see dsa_sparse_mla_fwd; sinks and
+    lse_log2 as dsa_attn_opts)."""
     T, H, D = q.shape
     Dv = kv.d_nope if kv.format != _inp.KV_BF16 else 512
     k = idx.shape[1]
@@ -210,9 +237,16 @@ def dsa_sparse_mla_fwd(q, softmax_scale: float, kv: _inp.KVPool, idx, kv_extra=N
     if ws is None:
         ws = workspace(need, dev)
     s1, s2 = kv_pool_struct(kv), kv_pool_struct(kv_extra)
-    st = load().dsa_sparse_mla_fwd(_ptr(q), T, H, D, Dv, float(softmax_scale), _ref(s1), _ptr(idx),
-                                   k, _ref(s2), _ptr(idx_extra), k2, _ptr(out), _ptr(lse), _ptr(ws),
-                                   ws.numel(), _ptr(err_flag), _stream())
+    o = _opts(sinks, lse_log2)
+    if o is None:
+        st = load().dsa_sparse_mla_fwd(_ptr(q), T, H, D, Dv, float(softmax_scale), _ref(s1),
+                                       _ptr(idx), k, _ref(s2), _ptr(idx_extra), k2, _ptr(out),
+                                       _ptr(lse), _ptr(ws), ws.numel(), _ptr(err_flag), _stream())
+    else:
+        st = load().dsa_sparse_mla_fwd_ex(_ptr(q), T, H, D, Dv, float(softmax_scale), _ref(s1),
+                                          _ptr(idx), k, _ref(s2), _ptr(idx_extra), k2, _ptr(out),
+                                          _ptr(lse), _ptr(ws), ws.numel(), _ptr(err_flag),
+                                          ctypes.byref(o), _stream())
     _check(st, "dsa_sparse_mla_fwd")
     return out, lse
 
@@ -224,8 +258,9 @@ def dsa_decode_workspace_size(B, max_seq_len, k, H, Dv, k_swa=0) -> int:
 def dsa_decode(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, slot_base,
                max_seq_len: int, k: int, q, softmax_scale: float, kv: _inp.KVPool,
                kv_swa=None, idx_swa=None, idx_out=None, out=None, lse=None, ws=None,
-               err_flag=None):
-    """One fused decode step (see dsa_decode).  Returns (idx_out, out, lse)."""
+               err_flag=None, sinks=None, lse_log2=False):
+    """One fused decode step (see dsa_decode; sinks and lse_log2 as
+    dsa_attn_opts).  Returns (idx_out, out, lse)."""
     B, H_I, d_idx = q_idx.shape
     _, H, D = q.shape
     Dv = kv.d_nope if kv.format != _inp.KV_BF16 else 512
@@ -241,11 +276,15 @@ def dsa_decode(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, slot_base
     if ws is None:
         ws = workspace(need, dev)
     s1, s2 = kv_pool_struct(kv), kv_pool_struct(kv_swa)
-    st = load().dsa_decode(_ptr(q_idx), idx_dtype, _ptr(q_scale), _ptr(k_idx), _ptr(k_scale),
-                           k_idx.shape[0], _ptr(w), H_I, d_idx, B, _ptr(seq_lens), _ptr(slot_base),
-                           int(max_seq_len), k, _ptr(q), H, D, Dv, float(softmax_scale), _ref(s1),
-                           _ref(s2), _ptr(idx_swa), k_swa, _ptr(idx_out), _ptr(out), _ptr(lse),
-                           _ptr(ws), ws.numel(), _ptr(err_flag), _stream())
+    args = (_ptr(q_idx), idx_dtype, _ptr(q_scale), _ptr(k_idx), _ptr(k_scale), k_idx.shape[0],
+            _ptr(w), H_I, d_idx, B, _ptr(seq_lens), _ptr(slot_base), int(max_seq_len), k, _ptr(q),
+            H, D, Dv, float(softmax_scale), _ref(s1), _ref(s2), _ptr(idx_swa), k_swa,
+            _ptr(idx_out), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _ptr(err_flag))
+    o = _opts(sinks, lse_log2)
+    if o is None:
+        st = load().dsa_decode(*args, _stream())
+    else:
+        st = load().dsa_decode_ex(*args, ctypes.byref(o), _stream())
     _check(st, "dsa_decode")
     return idx_out, out, lse
 

@@ -209,6 +209,32 @@ int dsa_sparse_mla_fwd(const void *q, int T, int H, int D, int Dv, float softmax
                        int32_t *err_flag, dsa_stream_t stream);
 
 /*
+ * Attention options (dsa_sparse_mla_fwd_ex, dsa_decode_ex; NULL: none).
+ *   sinks     device fp32 [H] or NULL: per-head sink logits.  A sink is one
+ *             more logit in every softmax denominator of its head, in the
+ *             units of the scores s_j = softmax_scale * q . K_j, with no
+ *             value (the "sink folded in" of the Miles sparse-attention
+ *             notes):  out = sum_j e^{s_j} K_j[0:Dv] / (sum_j e^{s_j} +
+ *             e^{sink}),  lse = ln(sum_j e^{s_j} + e^{sink}).  A token with
+ *             no valid entry then gets out = 0 and lse = sink.
+ *   lse_log2  nonzero: lse is reported in log2 units (the natural-log lse
+ *             divided by ln 2), the form those notes hand to the backward.
+ *   reserved  0 (else DSA_ERR_INVALID_ARG).
+ */
+typedef struct dsa_attn_opts {
+  const float *sinks;
+  int32_t lse_log2;
+  int32_t reserved;
+} dsa_attn_opts;
+
+/* dsa_sparse_mla_fwd with attention options (opts may be NULL). */
+int dsa_sparse_mla_fwd_ex(const void *q, int T, int H, int D, int Dv, float softmax_scale,
+                          const dsa_kv_pool *kv, const int32_t *idx, int k,
+                          const dsa_kv_pool *kv_extra, const int32_t *idx_extra, int k2,
+                          void *out, float *lse, void *ws, size_t ws_bytes,
+                          int32_t *err_flag, const dsa_attn_opts *opts, dsa_stream_t stream);
+
+/*
  * dsa_decode -- one fused decode step: score -> top-k -> sparse MLA for B
  * requests with one query token each (tokenspeed PR #627, Decode table:
  * "scores + TopK + sparse attn = total").
@@ -235,6 +261,19 @@ int dsa_decode(const void *q_idx, int idx_dtype, const float *q_scale,
                const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa,
                int32_t *idx_out, void *out, float *lse,
                void *ws, size_t ws_bytes, int32_t *err_flag, dsa_stream_t stream);
+
+/* dsa_decode with attention options (opts may be NULL). */
+int dsa_decode_ex(const void *q_idx, int idx_dtype, const float *q_scale,
+                  const void *k_idx, const float *k_scale, int64_t k_rows,
+                  const float *w, int H_I, int d_idx,
+                  int B, const int32_t *seq_lens, const int32_t *slot_base,
+                  int64_t max_seq_len, int k,
+                  const void *q, int H, int D, int Dv, float softmax_scale,
+                  const dsa_kv_pool *kv,
+                  const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa,
+                  int32_t *idx_out, void *out, float *lse,
+                  void *ws, size_t ws_bytes, int32_t *err_flag,
+                  const dsa_attn_opts *opts, dsa_stream_t stream);
 
 /*
  * dsa_decode_host -- dsa_decode with the step's inputs and outputs in HOST

@@ -230,6 +230,65 @@ def test_sparse_mla_matches_oracle(fmt, H, k):
     assert (out[1] == 0).all() and torch.isneginf(lse[1]).all()   # all-padded token
 
 
+def _sinks(H, seed=5):
+    g = torch.Generator().manual_seed(seed)
+    s = torch.randn(H, generator=g) * 3.0
+    s[0] = -math.inf     # head 0: no sink
+    if H > 1:
+        s[1] = 40.0      # far above every score: that head's output nearly vanishes
+    return s.float().cuda()
+
+
+@pytest.mark.parametrize("fmt,H,k,T", [(I.KV_BF16, 64, 2048, 3),      # split pieces + combine
+                                       (I.KV_BF16, 64, 256, 160),     # one piece a token
+                                       (I.KV_BF16, 8, 300, 3),
+                                       (I.KV_FP8_UNIFORM, 64, 1152, 3),
+                                       (I.KV_FP8_DS_MLA, 64, 1024, 3)])
+def test_sparse_mla_sinks(fmt, H, k, T):
+    pool, idx, q, D = _mla_case(fmt, T, H, k)
+    scale = 1 / math.sqrt(192.0) if D == 576 else 1 / math.sqrt(512.0)
+    sinks = _sinks(H)
+    out, lse = ops.dsa_sparse_mla_fwd(q, scale, pool, idx, sinks=sinks)
+    ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(pool), raw(idx), scale,
+                                    out.shape[2], sinks=sinks.double().cpu().numpy())
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "mla+sinks")
+    # the all-padded token: no value, the denominator is the sink alone
+    assert (out[1] == 0).all()
+    assert torch.equal(lse[1].cpu(), sinks.cpu())
+
+
+def test_sparse_mla_lse_log2():
+    pool, idx, q, D = _mla_case(I.KV_BF16, 3, 64, 700)
+    scale = 1 / math.sqrt(192.0)
+    out, lse = ops.dsa_sparse_mla_fwd(q, scale, pool, idx)
+    out2, lse2 = ops.dsa_sparse_mla_fwd(q, scale, pool, idx, lse_log2=True)
+    assert torch.equal(out, out2)
+    fin = torch.isfinite(lse)
+    assert torch.equal(torch.isneginf(lse2), torch.isneginf(lse))
+    assert torch.allclose(lse2[fin], lse[fin] / math.log(2.0), rtol=1e-6, atol=1e-6)
+
+
+def test_decode_sinks_and_log2_lse():
+    case = I.decode_case("sinks", 3, [300, 5000, 20000], 64, 128, "fp8", 2048, 64, I.KV_BF16,
+                         device="cuda")
+    sinks = _sinks(case.H)
+    ind = case.indexer
+    idx, out, lse = ops.dsa_decode(ind["q_idx"], ind["idx_dtype"], ind["q_scale"], ind["k_idx"],
+                                   ind["k_scale"], ind["w"], case.seq_lens, case.slot_base,
+                                   case.max_seq_len, case.k, case.q, case.softmax_scale, case.kv,
+                                   sinks=sinks, lse_log2=True)
+    idx_plain, _, _ = ops.decode_case(case)
+    assert torch.equal(idx, idx_plain)          # the sinks change the attention only
+    c = decode_case_np(case)
+    sk = sinks.double().cpu().numpy()
+    for b in range(case.B):
+        rows = O.gather_valid(c["kv"], idx[b].cpu().numpy())
+        ref_out, ref_lse = O.sparse_mla_one(O.decode_bf16(c["q"][b]), rows, c["softmax_scale"],
+                                            c["Dv"], sk)
+        check_out_lse(out[b].float().cpu().numpy(), lse[b].cpu().numpy() * math.log(2.0),
+                      ref_out, ref_lse, "decode+sinks %d" % b)
+
+
 def test_sparse_mla_two_loop_packed():
     T, H = 2, 64
     main = I.kv_packed_pool(T * 256, 256, 3, 6, "cuda")
