@@ -414,6 +414,59 @@ def multi_token_decode(B: int, Q: int, N: int, device="cpu", seed=0, k=2048, H=6
                       meta={"requests": B, "tokens_per_request": Q})
 
 
+def paged_decode(B: int, N, page: int = 64, device="cpu", seed=0, k=2048, H=64,
+                 idx_kind="fp8", shuffle=True) -> DecodeCase:
+    """A decode step on paged caches: the index-k cache (and its scales) and
+    the bf16 KV pool are cut into pages of `page` slots, and position j of
+    request b lives at slot block_table[b][j // page] * page + j % page of
+    both.  Built contiguous (every request a run of whole pages), then the
+    pages are shuffled (the same permutation for both caches) and the block
+    table follows them.  meta: block_table int32 [B, max_pages], page_size,
+    and the permutation's inverse (new page -> old page) for reference."""
+    lens = [int(N)] * B if isinstance(N, int) else [int(x) for x in N]
+    pages = [(L + page - 1) // page for L in lens]
+    npages = sum(pages)
+    S_total = npages * page
+    if idx_kind == "fp8":
+        ind = indexer_fp8(B, S_total, 64, 128, seed, device)
+    else:
+        ind = indexer_grid_bf16(B, S_total, 64, 128, seed, device)
+    kv = kv_bf16_pool(S_total, seed, 5, device)
+    gq = _gen(seed, 4, device)
+    q = to_bf16(torch.randn((B, H, 576), generator=gq, device=device)).contiguous()
+    first = [0]
+    for n in pages[:-1]:
+        first.append(first[-1] + n)
+    if shuffle:
+        gp = torch.Generator().manual_seed(seed * 7919 + 17)
+        perm = torch.randperm(npages, generator=gp)          # old page -> new page
+    else:
+        perm = torch.arange(npages)
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(npages)                          # new page -> old page
+    inv_d = inv.to(device)
+
+    def by_page(x):   # rows grouped by page, reordered so that new page q holds old page inv[q]
+        shp = x.shape
+        return x.reshape(npages, page, *shp[1:])[inv_d].reshape(shp).contiguous()
+
+    ind = dict(ind)
+    ind["k_idx"] = by_page(ind["k_idx"])
+    if ind.get("k_scale") is not None:
+        ind["k_scale"] = by_page(ind["k_scale"])
+    kv = KVPool(kv.format, by_page(kv.data), None, kv.rows, kv.block, kv.d_nope, kv.d_rope)
+    maxp = max(pages)
+    bt = torch.zeros((B, maxp), dtype=torch.int32)
+    for b in range(B):
+        bt[b, :pages[b]] = perm[first[b]:first[b] + pages[b]].to(torch.int32)
+    return DecodeCase("paged_decode_b%d_p%d" % (B, page), B,
+                      torch.tensor(lens, dtype=torch.int32, device=device),
+                      torch.zeros(B, dtype=torch.int32, device=device), max(lens), 64, 128, ind,
+                      k, H, 576, 512, 1.0 / math.sqrt(192.0), q, kv,
+                      meta={"block_table": bt.to(device), "page_size": page,
+                            "new_to_old_page": inv})
+
+
 def packed_long_decode(N=1 << 20, device="cpu", seed=0, swa=128, topk=1024) -> DecodeCase:
     """Batch 1, context N on packed fp8_ds_mla pages of 256 tokens; two loops:
     the SWA window (its own packed cache) and the top-k list (indexer 64 x 128

@@ -262,18 +262,25 @@ def decode_request(b: int, case: dict):
     case (numpy): q_idx, q_scale, k_idx, k_scale, w, is_fp8, seq_lens,
     slot_base, k, q (uint16 bf16 bits [B,H,D]), kv (pool dict), softmax_scale,
     Dv, optional kv_swa / idx_swa.  The index-k cache and the KV pool share
-    slot numbering: position j of request b is slot slot_base[b] + j.
+    slot numbering: position j of request b is slot slot_base[b] + j, or,
+    with a paged layout (case["block_table"] [B, pages], case["page_size"]),
+    slot block_table[b][j // page] * page + j % page.
     Returns dict(scores [L], idx [k] request-local positions, out, lse)."""
     L = int(case["seq_lens"][b])
-    base = int(case["slot_base"][b])
+    pos = np.arange(L, dtype=np.int64)
+    if case.get("block_table") is not None:
+        page = int(case["page_size"])
+        pos_slots = case["block_table"][b][pos // page].astype(np.int64) * page + pos % page
+    else:
+        pos_slots = int(case["slot_base"][b]) + pos
     fp8 = case["is_fp8"]
     qs = None if case["q_scale"] is None else case["q_scale"][b]
-    ks = None if case["k_scale"] is None else case["k_scale"][base:base + L]
+    ks = None if case["k_scale"] is None else case["k_scale"][pos_slots]
     q_t = index_values(case["q_idx"][b], qs, fp8)
-    k_rows = index_values(case["k_idx"][base:base + L], ks, fp8)
+    k_rows = index_values(case["k_idx"][pos_slots], ks, fp8)
     scores = index_scores_one(q_t, case["w"][b].astype(np.float64), k_rows)
     sel = topk_row(scores, case["k"])
-    slots = np.where(sel >= 0, sel + base, -1)
+    slots = np.where(sel >= 0, pos_slots[np.maximum(sel, 0)] if L > 0 else -1, -1)
     rows = gather_valid(case["kv"], slots)
     if case.get("idx_swa") is not None:
         rows = np.concatenate([gather_valid(case["kv_swa"], case["idx_swa"][b]), rows], axis=0)

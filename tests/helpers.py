@@ -28,6 +28,9 @@ def decode_case_np(case):
     if case.kv_swa is not None:
         d["kv_swa"] = pool_np(case.kv_swa)
         d["idx_swa"] = raw(case.idx_swa)
+    if case.meta.get("block_table") is not None:
+        d["block_table"] = raw(case.meta["block_table"])
+        d["page_size"] = case.meta["page_size"]
     return d
 
 

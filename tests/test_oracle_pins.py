@@ -358,6 +358,38 @@ def test_sink_all_masked_row():
     assert not out.any() and np.array_equal(lse, sinks)
 
 
+# ---- paged caches (block table)
+
+def _paged_np(shuffle, seed=3):
+    case = I.paged_decode(3, [150, 64, 333], page=64, seed=seed, k=128, H=8,
+                          idx_kind="bf16_grid", shuffle=shuffle)
+    return case, decode_case_np(case)
+
+
+def test_paged_identity_table_is_the_contiguous_layout():
+    case, c = _paged_np(shuffle=False)
+    flat = dict(c)
+    flat.pop("block_table")
+    pages = [(int(L) + 63) // 64 for L in c["seq_lens"]]
+    flat["slot_base"] = np.cumsum([0] + [64 * n for n in pages[:-1]])
+    for b in range(3):
+        r_p, r_c = O.decode_request(b, c), O.decode_request(b, flat)
+        assert np.array_equal(r_p["scores"], r_c["scores"]) and np.array_equal(r_p["idx"], r_c["idx"])
+        assert np.array_equal(r_p["out"], r_c["out"]) and np.array_equal(r_p["lse"], r_c["lse"])
+
+
+def test_paged_shuffled_pages_give_the_same_results():
+    """The same data with its pages shuffled (and the table following them)
+    scores, selects and attends exactly alike."""
+    _, c0 = _paged_np(shuffle=False)
+    case, c1 = _paged_np(shuffle=True)
+    assert not np.array_equal(c0["block_table"], c1["block_table"])
+    for b in range(3):
+        r0, r1 = O.decode_request(b, c0), O.decode_request(b, c1)
+        assert np.array_equal(r0["scores"], r1["scores"]) and np.array_equal(r0["idx"], r1["idx"])
+        assert np.array_equal(r0["out"], r1["out"]) and np.array_equal(r0["lse"], r1["lse"])
+
+
 def test_split_combine_equals_whole():
     rng = np.random.default_rng(5)
     rows = rng.standard_normal((100, 16)) * 2
