@@ -120,7 +120,7 @@ int decode_enqueue(const void *q_idx, int idx_dtype, const float *q_scale, const
                    const void *q, int H, int D, int Dv, float softmax_scale, const dsa_kv_pool *kv,
                    const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa, int32_t *idx_out,
                    void *out, float *lse, void *ws, int32_t *err_flag, cudaStream_t s,
-                   const dsa_attn_opts *opts = nullptr) {
+                   const dsa_attn_opts *opts = nullptr, const PageMap &pages = PageMap{}) {
   DecodeLayout L = decode_layout(B, max_seq_len, k, H, Dv, k_swa, ws);
   const int64_t ld = scores_ld(max_seq_len);
   int32_t *idx = idx_out ? idx_out : L.idx;
@@ -130,15 +130,16 @@ int decode_enqueue(const void *q_idx, int idx_dtype, const float *q_scale, const
   IndexScoreArgs ia{};
   ia.q_idx = q_idx; ia.idx_dtype = idx_dtype; ia.q_scale = q_scale;
   ia.k_idx = k_idx; ia.k_scale = k_scale; ia.k_rows = k_rows; ia.w = w;
-  ia.slot_base = slot_base; ia.seq_lens = seq_lens;
+  ia.slot_base = pages.table ? nullptr : slot_base; ia.seq_lens = seq_lens;
+  ia.block_table = pages.table; ia.max_pages = pages.max_pages; ia.page_size = pages.page_size;
   ia.T = B; ia.H_I = H_I; ia.d = d_idx; ia.max_len = max_seq_len;
   ia.scores = L.scores; ia.ld_scores = ld; ia.hist = L.topk.hist; ia.topk_k = k;
   ia.inputs_ready = 1;   // the inputs precede the whole call; only the zeroing precedes us
   ia.err_flag = err_flag;
   e = index_score_launch(ia, s);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
-  e = topk_select(L.scores, ld, seq_lens, B, max_seq_len, k, slot_base, idx, nullptr, L.topk,
-                  err_flag, s);
+  e = topk_select(L.scores, ld, seq_lens, B, max_seq_len, k, pages.table ? nullptr : slot_base,
+                  idx, nullptr, L.topk, err_flag, s, pages);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   MlaArgs a{};
   a.q = q; a.T = B; a.H = H; a.D = D; a.Dv = Dv; a.softmax_scale = softmax_scale;
@@ -329,6 +330,35 @@ int dsa_decode_ex(const void *q_idx, int idx_dtype, const float *q_scale, const 
                         seq_lens, slot_base, max_seq_len, k, q, H, D, Dv, softmax_scale, kv, kv_swa,
                         idx_swa, k_swa, idx_out, out, lse, ws, err_flag,
                         reinterpret_cast<cudaStream_t>(stream), opts);
+}
+
+int dsa_decode_paged(const void *q_idx, int idx_dtype, const float *q_scale, const void *k_idx,
+                     const float *k_scale, int64_t k_rows, const float *w, int H_I, int d_idx,
+                     int B, const int32_t *seq_lens, const int32_t *block_table, int max_pages,
+                     int page_size, int64_t max_seq_len, int k, const void *q, int H, int D,
+                     int Dv, float softmax_scale, const dsa_kv_pool *kv,
+                     const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa,
+                     int32_t *idx_out, void *out, float *lse, void *ws, size_t ws_bytes,
+                     int32_t *err_flag, const dsa_attn_opts *opts, dsa_stream_t stream) {
+  if (opts && opts->reserved != 0) return DSA_ERR_INVALID_ARG;
+  if (B < 0 || max_seq_len < 0 || max_pages < 0) return DSA_ERR_INVALID_ARG;
+  if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (page_size < 64 || page_size % 64 != 0) return DSA_ERR_UNSUPPORTED;
+  if ((int64_t)max_pages * page_size < max_seq_len) return DSA_ERR_INVALID_ARG;
+  int st = check_indexer(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, B, H_I, d_idx);
+  if (st != DSA_OK) return st;
+  st = check_mla_shape(q, B, H, D, Dv, kv, idx_out, k, kv_swa, idx_swa, k_swa, out, lse,
+                       /*need_idx=*/false);
+  if (st != DSA_OK) return st;
+  if (B == 0) return DSA_OK;
+  if (!seq_lens || !block_table) return DSA_ERR_INVALID_ARG;
+  const size_t need = dsa_decode_workspace_size(B, max_seq_len, k, H, Dv, k_swa);
+  if (ws_bytes < need || !ws) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  const PageMap pages{block_table, max_pages, page_size};
+  return decode_enqueue(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, H_I, d_idx, B,
+                        seq_lens, nullptr, max_seq_len, k, q, H, D, Dv, softmax_scale, kv, kv_swa,
+                        idx_swa, k_swa, idx_out, out, lse, ws, err_flag,
+                        reinterpret_cast<cudaStream_t>(stream), opts, pages);
 }
 
 size_t dsa_decode_host_workspace_size(int B, int64_t max_seq_len, int k, int H_I, int d_idx,

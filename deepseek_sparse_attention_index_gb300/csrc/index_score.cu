@@ -69,9 +69,18 @@ struct RowInfo {
   bool bad;
 };
 
+template <bool PAGED = false>
 __device__ __forceinline__ RowInfo row_info(const IndexScoreArgs &a, int t) {
   RowInfo r;
   int64_t s, e;
+  if constexpr (PAGED) {
+    // positions 0 .. seq_len-1; their slots come from the block table
+    const int64_t len = a.seq_lens[t];
+    r.bad = len < 0 || len > (int64_t)a.max_pages * a.page_size;
+    r.r0 = 0;
+    r.len = r.bad ? 0 : len;
+    return r;
+  }
   if (a.slot_base) {
     s = a.slot_base[t];
     e = s + a.seq_lens[t];
@@ -91,6 +100,7 @@ __device__ __forceinline__ int64_t tiles_of(const RowInfo &r) {
 
 // Walks a CTA's share of the valid (row, key tile) units in row-major order,
 // skipping rows without keys.  next() may be called only while units remain.
+template <bool PAGED>
 struct TileIter {
   int t;
   int64_t j, ntile;
@@ -98,7 +108,7 @@ struct TileIter {
   __device__ __forceinline__ void start(const IndexScoreArgs &a, int t0, int64_t j0) {
     t = t0;
     j = j0;
-    ri = row_info(a, t);
+    ri = row_info<PAGED>(a, t);
     ntile = tiles_of(ri);
   }
   __device__ __forceinline__ void next(const IndexScoreArgs &a) {
@@ -106,18 +116,23 @@ struct TileIter {
       j = 0;
       do {
         ++t;
-        ri = row_info(a, t);
+        ri = row_info<PAGED>(a, t);
         ntile = tiles_of(ri);
       } while (ntile == 0);
     }
   }
 };
 
-template <bool FP8, int N, int KB>
+// PAGED: the caches are paged (block table, pages of a multiple of 64
+// slots): a tile's 128 positions are two runs of 64 slots, each loaded with
+// the 64-row maps kmap64 / smap64 from the slot the table gives.
+template <bool FP8, int N, int KB, bool PAGED>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap qmap,
-                      const __grid_constant__ CUtensorMap smap, IndexScoreArgs a) {
+                      const __grid_constant__ CUtensorMap smap,
+                      const __grid_constant__ CUtensorMap kmap64,
+                      const __grid_constant__ CUtensorMap smap64, IndexScoreArgs a) {
   extern __shared__ unsigned char smem_raw[];
   const IdxSmem L = idx_smem_layout(N, KB);
   unsigned char *base = reinterpret_cast<unsigned char *>(
@@ -194,7 +209,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     int64_t mine = 0;
 #pragma unroll 4
     for (int t = rlo; t < rhi; ++t) {
-      const RowInfo r = row_info(a, t);
+      const RowInfo r = row_info<PAGED>(a, t);
       if (r.bad && blockIdx.x == 0) raise_flag(a.err_flag, DSA_DEVERR_INDEX_RANGE);
       mine += tiles_of(r);
     }
@@ -220,7 +235,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     if (u0 < u1 && pre <= u0 && u0 < pre + mine) {
       int64_t acc = pre;
       for (int t = rlo; t < rhi; ++t) {
-        const int64_t n = tiles_of(row_info(a, t));
+        const int64_t n = tiles_of(row_info<PAGED>(a, t));
         if (u0 < acc + n) {
           s_t0 = t;
           s_j0 = u0 - acc;
@@ -259,7 +274,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       uint32_t sphase = 0;
       uint32_t s_issued = 0, s_last = 0;
       bool ok = true;
-      TileIter it;
+      TileIter<PAGED> it;
       if (count > 0) it.start(a, t_first, j_first);
       for (int64_t n = 0; n < count && ok; ++n, (n < count ? it.next(a) : (void)0)) {
         const int t = it.t;
@@ -279,19 +294,47 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           q_last = (q_last & ~(1u << qs)) | (qphase << qs);
           cur_t = t;
         }
+        // paged: the slots of the tile's two runs of 64 positions, read from
+        // the block table before the wait, whose time then covers the loads
+        int yseg[2] = {0, 0};
+        if constexpr (PAGED) {
+#pragma unroll
+          for (int sg = 0; sg < 2; ++sg) {
+            int64_t p = j * kTileKeys + 64 * sg;
+            if (p >= ri.len) p = j * kTileKeys;       // a run past the row: reload the first (unused)
+            const int32_t pg = __ldg(a.block_table + (size_t)t * a.max_pages + p / a.page_size);
+            yseg[sg] = pg * a.page_size + (int)(p % a.page_size);
+          }
+        }
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
         tc::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
         const int y = (int)(ri.r0 + j * kTileKeys);
-        for (int kb = 0; kb < KB; ++kb)
-          tc::tma_load_2d_hint(&kmap, &full[stage], base + L.stage0 + stage * L.stage_bytes + kb * 16384,
-                               kb * (FP8 ? 128 : 64), y, stream_policy);
+        if constexpr (PAGED) {
+          for (int kb = 0; kb < KB; ++kb)
+            for (int sg = 0; sg < 2; ++sg)
+              tc::tma_load_2d_hint(&kmap64, &full[stage],
+                                   base + L.stage0 + stage * L.stage_bytes + kb * 16384 + sg * 8192,
+                                   kb * (FP8 ? 128 : 64), yseg[sg], stream_policy);
+        } else {
+          for (int kb = 0; kb < KB; ++kb)
+            tc::tma_load_2d_hint(&kmap, &full[stage], base + L.stage0 + stage * L.stage_bytes + kb * 16384,
+                                 kb * (FP8 ? 128 : 64), y, stream_policy);
+        }
         if (FP8) {
           // the 128 key scales, from the nearest 16-byte boundary at or below y,
           // into their own ring (held until the epilogue has read them)
           if (!tc::mbar_wait(&scempty[ss], sphase ^ 1, abort_flag)) { ok = false; break; }
-          tc::mbar_arrive_expect_tx(&scfull[ss], kScBox * 4);
-          tc::tma_load_2d_hint(&smap, &scfull[ss], base + L.sc + ss * kScBytes, y & ~3, 0,
-                               stream_policy);
+          if constexpr (PAGED) {
+            // the two runs' 64 scales each, at scale 0 and 64 of the slot
+            tc::mbar_arrive_expect_tx(&scfull[ss], 2 * 64 * 4);
+            for (int sg = 0; sg < 2; ++sg)
+              tc::tma_load_2d_hint(&smap64, &scfull[ss], base + L.sc + ss * kScBytes + sg * 256,
+                                   yseg[sg], 0, stream_policy);
+          } else {
+            tc::mbar_arrive_expect_tx(&scfull[ss], kScBox * 4);
+            tc::tma_load_2d_hint(&smap, &scfull[ss], base + L.sc + ss * kScBytes, y & ~3, 0,
+                                 stream_policy);
+          }
           s_issued |= 1u << ss;
           s_last = (s_last & ~(1u << ss)) | (sphase << ss);
           if (++ss == kScSlots) {
@@ -328,7 +371,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       int acc = 0;
       uint32_t acc_phase = 0;
       bool any = false;
-      TileIter it;
+      TileIter<PAGED> it;
       if (count > 0) it.start(a, t_first, j_first);
       for (int64_t n = 0; n < count; ++n, (n < count ? it.next(a) : (void)0)) {
         const int t = it.t;
@@ -394,7 +437,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     bool hist_on = false;
     bool dead = false;
     float wq[N];
-    TileIter it;
+    TileIter<PAGED> it;
     if (count > 0) it.start(a, t_first, j_first);
     // unit n of this CTA (the producer and the issuer walk the same sequence)
     for (int64_t n = 0; n < count; ++n, (n < count ? it.next(a) : (void)0)) {
@@ -446,7 +489,8 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           dead = true;
           continue;
         }
-        sk = sc_s[ss * (kScBytes / 4) + (int)((ri.r0 + j * kTileKeys) & 3) + row_in_tile];
+        sk = sc_s[ss * (kScBytes / 4) + (PAGED ? 0 : (int)((ri.r0 + j * kTileKeys) & 3)) +
+                  row_in_tile];
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&scempty[ss]);
       }
@@ -477,7 +521,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
-template <bool FP8, int N, int KB>
+template <bool FP8, int N, int KB, bool PAGED>
 cudaError_t launch_tc(const IndexScoreArgs &a, cudaStream_t s) {
   CUtensorMap kmap, qmap;
   const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -491,6 +535,15 @@ cudaError_t launch_tc(const IndexScoreArgs &a, cudaStream_t s) {
   if (FP8 && !make_tmap_1d(&smap, a.k_scale, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
                            (uint64_t)a.k_rows, kScBox))
     return cudaErrorInvalidValue;
+  // paged: 64-row boxes, one per run of 64 positions (unused otherwise)
+  CUtensorMap kmap64 = kmap, smap64 = smap;
+  if (PAGED) {
+    if (!make_tmap_2d(&kmap64, a.k_idx, dt, eb, (uint64_t)a.k_rows, (uint64_t)a.d, 64, box_cols))
+      return cudaErrorInvalidValue;
+    if (FP8 && !make_tmap_1d(&smap64, a.k_scale, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                             (uint64_t)a.k_rows, 64))
+      return cudaErrorInvalidValue;
+  }
   // at most T * ceil(max_len / 128) valid tiles; each CTA takes an equal
   // share of the valid ones (computed in the kernel)
   const int64_t tiles_per_row = (a.max_len + kTileKeys - 1) / kTileKeys;
@@ -498,26 +551,33 @@ cudaError_t launch_tc(const IndexScoreArgs &a, cudaStream_t s) {
   const int64_t grid = std::min<int64_t>((int64_t)kCtasPerSm * num_sms(), total);
   const IdxSmem L = idx_smem_layout(N, KB);
   const size_t smem = L.total + 1024;
-  auto kern = index_score_tc_kernel<FP8, N, KB>;
+  auto kern = index_score_tc_kernel<FP8, N, KB, PAGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, kmap, qmap, smap, a);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, kmap, qmap, smap, kmap64,
+                    smap64, a);
+}
+
+template <bool FP8, int KB, bool PAGED>
+cudaError_t launch_heads(const IndexScoreArgs &a, cudaStream_t s) {
+  if (a.H_I <= 16) return launch_tc<FP8, 16, KB, PAGED>(a, s);
+  if (a.H_I <= 32) return launch_tc<FP8, 32, KB, PAGED>(a, s);
+  return launch_tc<FP8, 64, KB, PAGED>(a, s);
 }
 
 template <bool FP8, int KB>
-cudaError_t launch_heads(const IndexScoreArgs &a, cudaStream_t s) {
-  if (a.H_I <= 16) return launch_tc<FP8, 16, KB>(a, s);
-  if (a.H_I <= 32) return launch_tc<FP8, 32, KB>(a, s);
-  return launch_tc<FP8, 64, KB>(a, s);
+cudaError_t launch_paging(const IndexScoreArgs &a, cudaStream_t s) {
+  if (a.block_table) return launch_heads<FP8, KB, true>(a, s);
+  return launch_heads<FP8, KB, false>(a, s);
 }
 
 }  // namespace
 
 cudaError_t index_score_launch(const IndexScoreArgs &a, cudaStream_t s) {
   if (a.T == 0 || a.max_len == 0) return cudaSuccess;
-  if (a.idx_dtype == DSA_IDX_FP8_E4M3) return launch_heads<true, 1>(a, s);
-  if (a.d == 64) return launch_heads<false, 1>(a, s);
-  return launch_heads<false, 2>(a, s);
+  if (a.idx_dtype == DSA_IDX_FP8_E4M3) return launch_paging<true, 1>(a, s);
+  if (a.d == 64) return launch_paging<false, 1>(a, s);
+  return launch_paging<false, 2>(a, s);
 }
 
 }  // namespace dsa

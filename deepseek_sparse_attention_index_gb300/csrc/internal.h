@@ -8,6 +8,13 @@
 
 namespace dsa {
 
+// A row's positions -> pool slots through a block table (paged caches).
+struct PageMap {
+  const int32_t *table;   // [rows][max_pages], or NULL (not paged)
+  int max_pages;
+  int page_size;
+};
+
 // ------------------------------------------------------------------ top-k
 constexpr int kHistBins = 4096;   // first radix level: top 12 bits of the key
 constexpr int kListCap = 8192;    // (key, position) entries per row kept for the resolve pass
@@ -30,7 +37,8 @@ cudaError_t topk_hist(const float *scores, int64_t ld, const int32_t *row_len, i
                       int64_t max_len, int k, const TopkWs &w, cudaStream_t s);
 cudaError_t topk_select(const float *scores, int64_t ld, const int32_t *row_len, int T,
                         int64_t max_len, int k, const int32_t *index_base, int32_t *idx,
-                        int32_t *lens, const TopkWs &w, int32_t *err_flag, cudaStream_t s);
+                        int32_t *lens, const TopkWs &w, int32_t *err_flag, cudaStream_t s,
+                        const PageMap &pages = PageMap{});
 
 // ------------------------------------------------------------------ index score
 struct IndexScoreArgs {
@@ -55,8 +63,14 @@ struct IndexScoreArgs {
                              // stream began (fused decode: only the histogram's zeroing
                              // precedes us); else the kernel waits for it first
   int32_t *err_flag;
+  // paged caches (decode form, with seq_lens): position j of row t lives at
+  // slot block_table[t * max_pages + j / page_size] * page_size + j % page_size
+  const int32_t *block_table;  // or NULL
+  int max_pages;
+  int page_size;               // a multiple of 64
 };
 cudaError_t index_score_launch(const IndexScoreArgs &a, cudaStream_t s);
+
 
 // ------------------------------------------------------------------ sparse MLA
 struct PoolDev {

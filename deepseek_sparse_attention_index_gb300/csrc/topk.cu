@@ -270,6 +270,7 @@ struct ResolveSmem {
   uint32_t warp_sums[32];
   int s_bin;
   uint32_t s_before;
+  PageMap pm;                    // paged caches: the block table (set by the collect kernel)
 };
 
 // Resolves row t once its collect pass is complete.  b1 and n_gt (the count
@@ -280,6 +281,19 @@ struct ResolveSmem {
 // survivors in ascending position order.  The first pass copies the list
 // into `lc` (kListCache entries of dynamic shared memory) when it fits, so
 // the later passes read shared memory.  Run by one whole CTA of kThreads.
+// The output entry of position pos of row t: its slot through the block
+// table (paged caches), else pos + the row's index base.
+template <bool PAGED>
+__device__ __forceinline__ int32_t slot_of(const PageMap &pm, int t, int32_t pos, int32_t base) {
+  if constexpr (!PAGED) {
+    return pos + base;
+  } else {
+    return pm.table[(size_t)t * pm.max_pages + pos / pm.page_size] * pm.page_size +
+           pos % pm.page_size;
+  }
+}
+
+template <bool PAGED>
 __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint32_t b1,
                                          uint32_t n_gt, uint32_t n_list,
                                          const float *__restrict__ scores, int64_t ld, int64_t L,
@@ -289,6 +303,7 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
                                          const uint2 *__restrict__ tab, int32_t *__restrict__ idx,
                                          int32_t *__restrict__ lens, int32_t *err_flag) {
   uint32_t *sh = S.sh;
+  const PageMap &pm = S.pm;   // paged caches only
   const int32_t base = index_base ? index_base[t] : 0;
   int32_t *out = idx + (size_t)t * k;
   if (n_gt >= (uint32_t)k || n_list < (uint32_t)k) {
@@ -462,7 +477,7 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
 #pragma unroll
       for (int j = 0; j < kGather; ++j)
         if ((m >> j) & 1u) {
-          if (o < (uint32_t)k) out[o] = posv[j] + base;
+          if (o < (uint32_t)k) out[o] = slot_of<PAGED>(pm, t, posv[j], base);
           ++o;
         }
       written += tot;
@@ -483,7 +498,7 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
 #pragma unroll
       for (int j = 0; j < kGather; ++j)
         if ((m >> j) & 1u) {
-          if (o < (uint32_t)k) out[o] = (int32_t)(p0 + j) + base;
+          if (o < (uint32_t)k) out[o] = slot_of<PAGED>(pm, t, (int32_t)(p0 + j), base);
           ++o;
         }
       written += tot;
@@ -544,7 +559,7 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
 #pragma unroll
         for (int j = 0; j < kGather; ++j)
           if ((m >> j) & 1u) {
-            if (o < (uint32_t)k) out[o] = posv[j] + base;
+            if (o < (uint32_t)k) out[o] = slot_of<PAGED>(pm, t, posv[j], base);
             ++o;
           }
         written += tot;
@@ -565,18 +580,20 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
 // kMaxChunk: thread i holds positions x * chunk + r * kRound + 16 i + e
 // (round r < 2, e < 16), so the order (r, i, e) is position order and a
 // packed two-round block scan places every entry of the CTA's run.
+template <bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2)
 topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
                     const int32_t *__restrict__ row_len, int k, int chunk, int nch, int max_chunks,
                     const int32_t *__restrict__ index_base, const uint32_t *__restrict__ hist,
                     uint32_t *__restrict__ cnt, uint2 *__restrict__ list,
                     uint2 *__restrict__ tab, int32_t *__restrict__ idx,
-                    int32_t *__restrict__ lens, int32_t *err_flag) {
+                    int32_t *__restrict__ lens, int32_t *err_flag, const PageMap pages) {
   __shared__ ResolveSmem S;
   __shared__ uint32_t s_base;
   __shared__ int s_last;
   __shared__ uint32_t s_total;
   extern __shared__ uint2 list_cache[];   // kListCache entries, used by the resolving CTA
+  if (PAGED && threadIdx.x == 0) S.pm = pages;   // read by the resolve, after later barriers
   pdl_wait();      // scores and histogram come from the previous kernel
   pdl_trigger();
   // 1-D grid of rows x chunks (a 2-D grid would cap the rows at 65535)
@@ -587,7 +604,8 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
     if (c == 0) {
       const int32_t base = index_base ? index_base[t] : 0;
       int32_t *out = idx + (size_t)t * k;
-      for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < L ? (int32_t)j + base : -1;
+      for (int j = threadIdx.x; j < k; j += blockDim.x)
+        out[j] = j < L ? slot_of<PAGED>(pages, t, (int32_t)j, base) : -1;
       if (lens && threadIdx.x == 0) lens[t] = (int32_t)L;
     }
     return;
@@ -680,7 +698,7 @@ topk_collect_kernel(const float *__restrict__ scores, int64_t ld,
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  resolve_row(t, S, list_cache, b1, n_gt, s_total, scores, ld, L, k, chunk, max_chunks,
+  resolve_row<PAGED>(t, S, list_cache, b1, n_gt, s_total, scores, ld, L, k, chunk, max_chunks,
               index_base, list, tab, idx, lens, err_flag);
 }
 
@@ -740,19 +758,20 @@ cudaError_t topk_hist(const float *scores, int64_t ld, const int32_t *row_len, i
 
 cudaError_t topk_select(const float *scores, int64_t ld, const int32_t *row_len, int T,
                         int64_t max_len, int k, const int32_t *index_base, int32_t *idx,
-                        int32_t *lens, const TopkWs &w, int32_t *err_flag, cudaStream_t s) {
+                        int32_t *lens, const TopkWs &w, int32_t *err_flag, cudaStream_t s,
+                        const PageMap &pages) {
   const int chunk = collect_chunk(T, max_len);
   const int64_t nch = max_len > k ? (max_len + chunk - 1) / chunk : 1;
   if (nch > w.max_chunks) return cudaErrorInvalidValue;
   if (nch * T >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
   const dim3 grid((unsigned)(nch * T));
   const size_t dyn = sizeof(uint2) * kListCache;
-  cudaError_t e = cudaFuncSetAttribute(topk_collect_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  auto kern = pages.table ? topk_collect_kernel<true> : topk_collect_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
-  return launch_pdl(topk_collect_kernel, grid, dim3(kThreads), dyn, s, scores, ld, row_len, k,
-                    chunk, (int)nch, w.max_chunks, index_base, (const uint32_t *)w.hist, w.cnt, w.list,
-                    w.tab, idx, lens, err_flag);
+  return launch_pdl(kern, grid, dim3(kThreads), dyn, s, scores, ld, row_len, k, chunk, (int)nch,
+                    w.max_chunks, index_base, (const uint32_t *)w.hist, w.cnt, w.list, w.tab, idx,
+                    lens, err_flag, pages);
 }
 
 }  // namespace dsa

@@ -66,6 +66,11 @@ _SIGS = {
                               c_p, c_i32, c_i32, c_i32, c_f32, ctypes.POINTER(DsaKvPool),
                               ctypes.POINTER(DsaKvPool), c_p, c_i32,
                               c_p, c_p, c_p, c_p, c_sz, c_p, ctypes.POINTER(DsaAttnOpts), c_p]),
+    "dsa_decode_paged": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_i32, c_i32,
+                                 c_i32, c_p, c_p, c_i32, c_i32, c_i64, c_i32,
+                                 c_p, c_i32, c_i32, c_i32, c_f32, ctypes.POINTER(DsaKvPool),
+                                 ctypes.POINTER(DsaKvPool), c_p, c_i32,
+                                 c_p, c_p, c_p, c_p, c_sz, c_p, ctypes.POINTER(DsaAttnOpts), c_p]),
     "dsa_decode_workspace_size": (c_sz, [c_i32, c_i64, c_i32, c_i32, c_i32, c_i32]),
     "dsa_decode": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_i32, c_i32,
                            c_i32, c_p, c_p, c_i64, c_i32,
@@ -329,9 +334,49 @@ def dsa_decode_host(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, slot
     return idx_out, out, lse
 
 
+def dsa_decode_paged(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, block_table,
+                     page_size: int, max_seq_len: int, k: int, q, softmax_scale: float,
+                     kv: _inp.KVPool, kv_swa=None, idx_swa=None, idx_out=None, out=None, lse=None,
+                     ws=None, err_flag=None, sinks=None, lse_log2=False):
+    """The fused decode step on paged caches (see dsa_decode_paged):
+    block_table int32 [B, max_pages] on the device.  Returns (idx_out, out, lse);
+    idx_out holds pool slots."""
+    B, H_I, d_idx = q_idx.shape
+    _, H, D = q.shape
+    Dv = kv.d_nope if kv.format != _inp.KV_BF16 else 512
+    k_swa = 0 if idx_swa is None else idx_swa.shape[1]
+    dev = q.device
+    if idx_out is None:
+        idx_out = torch.empty((B, k), dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty((B, H, Dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    need = dsa_decode_workspace_size(B, max_seq_len, k, H, Dv, k_swa)
+    if ws is None:
+        ws = workspace(need, dev)
+    s1, s2 = kv_pool_struct(kv), kv_pool_struct(kv_swa)
+    o = _opts(sinks, lse_log2)
+    st = load().dsa_decode_paged(_ptr(q_idx), idx_dtype, _ptr(q_scale), _ptr(k_idx), _ptr(k_scale),
+                                 k_idx.shape[0], _ptr(w), H_I, d_idx, B, _ptr(seq_lens),
+                                 _ptr(block_table), block_table.shape[1], int(page_size),
+                                 int(max_seq_len), k, _ptr(q), H, D, Dv, float(softmax_scale),
+                                 _ref(s1), _ref(s2), _ptr(idx_swa), k_swa, _ptr(idx_out), _ptr(out),
+                                 _ptr(lse), _ptr(ws), ws.numel(), _ptr(err_flag),
+                                 None if o is None else ctypes.byref(o), _stream())
+    _check(st, "dsa_decode_paged")
+    return idx_out, out, lse
+
+
 def decode_case(case: _inp.DecodeCase, ws=None, err_flag=None, idx_out=None, out=None, lse=None):
     """dsa_decode on a generated DecodeCase."""
     ind = case.indexer
+    if case.meta.get("block_table") is not None:
+        return dsa_decode_paged(ind["q_idx"], ind["idx_dtype"], ind["q_scale"], ind["k_idx"],
+                                ind["k_scale"], ind["w"], case.seq_lens, case.meta["block_table"],
+                                case.meta["page_size"], case.max_seq_len, case.k, case.q,
+                                case.softmax_scale, case.kv, case.kv_swa, case.idx_swa,
+                                idx_out=idx_out, out=out, lse=lse, ws=ws, err_flag=err_flag)
     return dsa_decode(ind["q_idx"], ind["idx_dtype"], ind["q_scale"], ind["k_idx"], ind["k_scale"],
                       ind["w"], case.seq_lens, case.slot_base, case.max_seq_len, case.k, case.q,
                       case.softmax_scale, case.kv, case.kv_swa, case.idx_swa, idx_out=idx_out,

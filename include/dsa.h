@@ -276,6 +276,32 @@ int dsa_decode_ex(const void *q_idx, int idx_dtype, const float *q_scale,
                   const dsa_attn_opts *opts, dsa_stream_t stream);
 
 /*
+ * dsa_decode_paged -- dsa_decode on paged caches (the block-table layout of
+ * the tokenspeed PR #627 serving stack: pages of page_size slots).  Position
+ * j of request b lives at slot
+ *     block_table[b * max_pages + j / page_size] * page_size + j % page_size
+ * of BOTH the index-k cache (k_idx / k_scale rows) and the KV pool kv; the
+ * selection (idx_out) holds those slots.  page_size a multiple of 64;
+ * max_pages * page_size >= max_seq_len; block_table int32 [B, max_pages] on
+ * the device, entries for positions past seq_lens[b] unused.  A slot outside
+ * the pool is reported (DSA_DEVERR_INDEX_RANGE) and masked by the attention;
+ * index-k rows outside the cache read as zeros.  Everything else as
+ * dsa_decode_ex (opts may be NULL); workspace dsa_decode_workspace_size(...).
+ */
+int dsa_decode_paged(const void *q_idx, int idx_dtype, const float *q_scale,
+                     const void *k_idx, const float *k_scale, int64_t k_rows,
+                     const float *w, int H_I, int d_idx,
+                     int B, const int32_t *seq_lens,
+                     const int32_t *block_table, int max_pages, int page_size,
+                     int64_t max_seq_len, int k,
+                     const void *q, int H, int D, int Dv, float softmax_scale,
+                     const dsa_kv_pool *kv,
+                     const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa,
+                     int32_t *idx_out, void *out, float *lse,
+                     void *ws, size_t ws_bytes, int32_t *err_flag,
+                     const dsa_attn_opts *opts, dsa_stream_t stream);
+
+/*
  * dsa_decode_host -- dsa_decode with the step's inputs and outputs in HOST
  * memory; the model state (index-k cache k_idx / k_scale, the KV pools) stays
  * in device memory.  The same computation and kernels as dsa_decode, with

@@ -330,8 +330,19 @@ def _check_decode(case, idx_gpu, out_gpu, lse_gpu, requests, bit_exact=False):
     lse_gpu = lse_gpu.cpu().numpy()
     for b in requests:
         r = O.decode_request(b, c)
-        base = int(c["slot_base"][b])
-        pos = np.where(idx_gpu[b] >= 0, idx_gpu[b] - base, -1)
+        if c.get("block_table") is not None:
+            # paged: slot -> position through the request's pages
+            page = int(c["page_size"])
+            where = {int(pg): j for j, pg in enumerate(c["block_table"][b])}
+            pos = np.array([where[int(s) // page] * page + int(s) % page if s >= 0 else -1
+                            for s in idx_gpu[b]], dtype=np.int64)
+            slots_of = lambda ps, b=b: np.array(
+                [int(c["block_table"][b][p // page]) * page + p % page for p in ps], dtype=np.int64)
+            base = 0
+        else:
+            base = int(c["slot_base"][b])
+            pos = np.where(idx_gpu[b] >= 0, idx_gpu[b] - base, -1)
+            slots_of = lambda ps, base=base: np.asarray(ps, dtype=np.int64) + base
         n = min(int(c["seq_lens"][b]), case.k)
         assert (pos[:n] >= 0).all() and (pos[n:] == -1).all(), b
         if bit_exact:
@@ -342,7 +353,7 @@ def _check_decode(case, idx_gpu, out_gpu, lse_gpu, requests, bit_exact=False):
             if gset is None:
                 ref_out, ref_lse = r["out"], r["lse"]
             else:   # tolerated ties: compare attention on the GPU's own selection
-                rows = O.gather_valid(c["kv"], gset + base)
+                rows = O.gather_valid(c["kv"], slots_of(gset))
                 if c.get("idx_swa") is not None:
                     rows = np.concatenate([O.gather_valid(c["kv_swa"], c["idx_swa"][b]), rows])
                 ref_out, ref_lse = O.sparse_mla_one(O.decode_bf16(c["q"][b]), rows,
@@ -381,6 +392,40 @@ def test_decode_is_deterministic():
         again = ops.decode_case(case)
         for a, b in zip(first, again):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kind,page", [("fp8", 64), ("bf16_grid", 64), ("fp8", 128)])
+def test_paged_decode_matches_oracle(kind, page):
+    case = I.paged_decode(4, [700, 3000, 9000, 20000], page=page, device="cuda", idx_kind=kind)
+    flag = _flag()
+    idx, out, lse = ops.decode_case(case, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    _check_decode(case, idx, out, lse, range(case.B), bit_exact=kind == "bf16_grid")
+
+
+def test_paged_decode_equals_contiguous_layout():
+    """The same data paged (pages shuffled, or in order) and contiguous: the
+    same positions selected, the same outputs bit for bit."""
+    lens = [1000, 5000, 64, 20000]
+    plain = I.paged_decode(4, lens, device="cuda", shuffle=False)
+    shuf = I.paged_decode(4, lens, device="cuda", shuffle=True)
+    # the in-order layout through the contiguous entry point
+    pages = [(L + 63) // 64 for L in lens]
+    flat = I.DecodeCase(plain.name, plain.B, plain.seq_lens,
+                        torch.tensor(np.cumsum([0] + [64 * n for n in pages[:-1]]),
+                                     dtype=torch.int32, device="cuda"),
+                        plain.max_seq_len, plain.H_I, plain.d_idx, plain.indexer, plain.k, plain.H,
+                        plain.D, plain.Dv, plain.softmax_scale, plain.q, plain.kv)
+    i0, o0, l0 = ops.decode_case(flat)
+    i1, o1, l1 = ops.decode_case(plain)
+    i2, o2, l2 = ops.decode_case(shuf)
+    assert torch.equal(i0, i1) and torch.equal(o0, o1) and torch.equal(l0, l1)
+    assert torch.equal(o0, o2) and torch.equal(l0, l2)
+    # shuffled slots map back to the same positions
+    inv = shuf.meta["new_to_old_page"]
+    old = torch.where(i2 >= 0, inv.cuda()[(i2 // 64).clamp(min=0).long()] * 64 + i2 % 64, -1)
+    assert torch.equal(old.to(torch.int32), i0)
 
 
 def test_multi_token_decode_rows_share_a_request():
