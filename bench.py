@@ -354,7 +354,29 @@ def run_workload(args):
            "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
            "vs_baseline": None, "data": "synthetic", "e2e": None, "gpu_launches": None}
     w = args.workload
-    if w == "mtp":
+    if w == "paged":
+        # the decode step on paged caches: pages of 64 slots, shuffled over the
+        # pool, positions reached through the block table
+        case = I.paged_decode(args.batch, args.context, page=64, device=dev)
+        N = args.context
+        ws = ops.workspace(ops.dsa_decode_workspace_size(case.B, N, case.k, case.H, case.Dv), dev)
+        fn = lambda: ops.decode_case(case, ws=ws)
+        clocks.start()
+        us = _timed(fn, args.steps, args.warmup, l2_flush)
+        clk = clocks.stop()
+        v = statistics.median(us)
+        nbytes = case.B * N * (128 + 4 + 4) + case.B * 64 * (128 + 8) + \
+            case.B * min(N, case.k) * 1152 + case.B * case.H * (576 * 2 + 512 * 2 + 4)
+        res.update({"value": round(v, 3), "ms_per_step": round(v / 1000, 6),
+                    "dtype": "fp8_e4m3 indexer + bf16 attention (fp32 accumulate)",
+                    "config": {"workload": case.name, "batch": case.B, "context": N,
+                               "page_size": 64, "topk": case.k, "heads": case.H},
+                    "step_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": nbytes,
+                                      "achieved_gbs": round(nbytes / (v * 1e-6) / 1e9, 1),
+                                      "frac": round(nbytes / (v * 1e-6) / 1e9 / hbm_gbs, 4),
+                                      "peak": hbm_gbs, "peak_kind": peak_kind},
+                    "clocks": clk})
+    elif w == "mtp":
         # two new tokens per request (speculative verification): B*2 rows of the
         # fused decode, a request's rows sharing its context
         Bq, Q, N = args.batch, 2, args.context
@@ -578,7 +600,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "tiny", "uniform_fp8", "packed_1m", "prefill",
-                             "index", "topk", "mla", "mtp"],
+                             "index", "topk", "mla", "mtp", "paged"],
                     help="decode (default): the driver's line; the others are secondary "
                          "measurements of the remaining configurations")
     ap.add_argument("--heads", type=int, default=64, help="prefill: attention heads")
