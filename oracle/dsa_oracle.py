@@ -216,6 +216,63 @@ def sparse_mla_one(q_t: np.ndarray, rows: np.ndarray, softmax_scale: float, Dv: 
     return p @ rows[:, :Dv], lse
 
 
+def sparse_mla_bwd_one(q_t: np.ndarray, rows: np.ndarray, dout_t: np.ndarray,
+                       softmax_scale: float, Dv: int, sinks: np.ndarray | None = None):
+    """Gradients of sparse_mla_one for one query token, given dL/dout
+    (dout_t [H, Dv]); the lse output is auxiliary (no gradient flows into it).
+
+    With s_j = scale q.K_j, p_j = e^{s_j - lse}, out = sum_j p_j V_j
+    (V_j = K_j[:Dv]) and delta = dout . out (= sum_j p_j dout.V_j):
+        dS_j = p_j (dout . V_j - delta)
+        dq   = scale sum_j dS_j K_j
+        dK_j = scale sum_h dS_hj q_h, plus sum_h p_hj dout_h on the V columns
+        dsink_h = -p_sink,h delta_h,  p_sink = e^{sink - lse}
+    A row's gradient is per occurrence.  Returns dq [H, D], drows [n, D],
+    dsinks [H] (zeros without sinks)."""
+    H, D = q_t.shape
+    n = rows.shape[0]
+    if n == 0:
+        return np.zeros((H, D)), np.zeros((0, D)), np.zeros(H)
+    out, lse = sparse_mla_one(q_t, rows, softmax_scale, Dv, sinks)
+    s = softmax_scale * (q_t @ rows.T)           # [H, n]
+    p = np.exp(s - lse[:, None])
+    dP = dout_t @ rows[:, :Dv].T                 # [H, n]
+    delta = (dout_t * out).sum(axis=1)           # [H]
+    dS = p * (dP - delta[:, None])
+    dq = softmax_scale * (dS @ rows)
+    drows = softmax_scale * (dS.T @ q_t)
+    drows[:, :Dv] += p.T @ dout_t
+    dsinks = np.zeros(H)
+    if sinks is not None:
+        sk = np.asarray(sinks, dtype=np.float64)
+        dsinks = np.where(np.isfinite(sk), -np.exp(sk - lse) * delta, 0.0)
+    return dq, drows, dsinks
+
+
+def sparse_mla_bwd(q: np.ndarray, pool: dict, idx: np.ndarray, dout: np.ndarray,
+                   softmax_scale: float, Dv: int, sinks: np.ndarray | None = None):
+    """Backward of sparse_mla (one list): dq [T, H, D], dkv [pool rows, D]
+    (each selection's row gradient added to its slot; -1 entries skipped),
+    dsinks [H] summed over the tokens."""
+    T, H, D = q.shape
+    dq = np.zeros((T, H, D))
+    data = np.asarray(pool["data"])
+    if pool["format"] == KV_FP8_DS_MLA:
+        n_rows = data.size // 584
+    else:
+        n_rows = data.reshape(-1, pool["d_nope"] + pool["d_rope"]).shape[0]
+    dkv = np.zeros((n_rows, D))
+    dsinks = np.zeros(H)
+    for t in range(T):
+        sl = np.asarray(idx[t], dtype=np.int64)
+        sl = sl[sl >= 0]
+        rows = kv_rows(pool, sl)
+        dq[t], drows, ds = sparse_mla_bwd_one(q[t], rows, dout[t], softmax_scale, Dv, sinks)
+        np.add.at(dkv, sl, drows)
+        dsinks += ds
+    return dq, dkv, dsinks
+
+
 def gather_valid(pool: dict, idx_row) -> np.ndarray:
     """Rows of the non-negative entries of one index list (-1 masked)."""
     idx_row = np.asarray(idx_row, dtype=np.int64)

@@ -390,6 +390,71 @@ def test_paged_shuffled_pages_give_the_same_results():
         assert np.array_equal(r0["out"], r1["out"]) and np.array_equal(r0["lse"], r1["lse"])
 
 
+# ---- backward of the sparse attention
+
+def _bwd_case(seed=11, H=3, n=6, D=12, Dv=8):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((H, D)), rng.standard_normal((n, D)),
+            rng.standard_normal((H, Dv)), rng.standard_normal(H), 0.7, Dv)
+
+
+@pytest.mark.parametrize("with_sinks", [False, True])
+def test_sparse_mla_backward_matches_finite_differences(with_sinks):
+    """Central differences of L = sum(out * G) against the analytic gradients
+    (q, every row entry, every sink)."""
+    q, rows, G, sinks, sc, Dv = _bwd_case()
+    sk = sinks if with_sinks else None
+
+    def loss(q_, rows_, sk_):
+        out, _ = O.sparse_mla_one(q_, rows_, sc, Dv, sk_)
+        return float((out * G).sum())
+
+    dq, drows, dsk = O.sparse_mla_bwd_one(q, rows, G, sc, Dv, sk)
+    eps = 1e-6
+    for arr, grad in ((q, dq), (rows, drows)):
+        num = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            a0 = arr[i]
+            arr[i] = a0 + eps
+            lp = loss(q, rows, sk)
+            arr[i] = a0 - eps
+            lm = loss(q, rows, sk)
+            arr[i] = a0
+            num[i] = (lp - lm) / (2 * eps)
+        assert np.allclose(grad, num, rtol=1e-6, atol=1e-8)
+    if with_sinks:
+        for h in range(len(sinks)):
+            s0 = sinks[h]
+            sinks[h] = s0 + eps
+            lp = loss(q, rows, sinks)
+            sinks[h] = s0 - eps
+            lm = loss(q, rows, sinks)
+            sinks[h] = s0
+            assert abs(dsk[h] - (lp - lm) / (2 * eps)) < 1e-7
+    else:
+        assert not dsk.any()
+
+
+def test_sparse_mla_backward_scatter_adds_shared_rows():
+    """Two tokens selecting the same slot (and -1 entries) add their row
+    gradients into that slot; a slot nobody selects gets zero."""
+    pool = I.kv_bf16_pool(16, 1, 5, "cpu")
+    pn = pool_np(pool)
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((2, 4, 576)) * 0.1
+    dout = rng.standard_normal((2, 4, 512))
+    idx = np.array([[3, 7, -1, 9], [7, 3, 12, -1]])
+    dq, dkv, _ = O.sparse_mla_bwd(q, pn, idx, dout, 0.05, 512)
+    for t in range(2):
+        sl = idx[t][idx[t] >= 0]
+        dq1, dr1, _ = O.sparse_mla_bwd_one(q[t], O.kv_rows(pn, sl), dout[t], 0.05, 512)
+        assert np.allclose(dq[t], dq1)
+    r0 = O.sparse_mla_bwd_one(q[0], O.kv_rows(pn, [3, 7, 9]), dout[0], 0.05, 512)[1]
+    r1 = O.sparse_mla_bwd_one(q[1], O.kv_rows(pn, [7, 3, 12]), dout[1], 0.05, 512)[1]
+    assert np.allclose(dkv[7], r0[1] + r1[0]) and np.allclose(dkv[3], r0[0] + r1[1])
+    assert not dkv[0].any() and not dkv[15].any()
+
+
 def test_split_combine_equals_whole():
     rng = np.random.default_rng(5)
     rows = rng.standard_normal((100, 16)) * 2
