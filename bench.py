@@ -354,7 +354,46 @@ def run_workload(args):
            "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
            "vs_baseline": None, "data": "synthetic", "e2e": None, "gpu_launches": None}
     w = args.workload
-    if w == "paged":
+    if w == "bwd":
+        # the attention's backward over a causal prefill's selections: T tokens,
+        # 64 heads, k = 2048 bf16 rows each (the forward's lse as input)
+        T, H = args.context, args.heads
+        case = I.prefill_case([T], k=2048, H=H, device=dev)
+        ind = case.indexer
+        ld = (T + 3) // 4 * 4
+        scores = torch.empty((T, ld), dtype=torch.float32, device=dev)
+        rl = (case.row_end - case.row_start).contiguous()
+        tws = ops.workspace(ops.dsa_topk_workspace_size(T, T, case.k), dev)
+        idx = torch.empty((T, case.k), dtype=torch.int32, device=dev)
+        ops.dsa_index_score(ind["q_idx"], ind["idx_dtype"], ind["q_scale"], ind["k_idx"],
+                            ind["k_scale"], ind["w"], case.row_start, case.row_end, T, scores=scores)
+        ops.dsa_topk(scores, rl, case.k, T, index_base=case.row_start, idx=idx, ws=tws)
+        out, lse = ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, idx)
+        dout = I.to_bf16(torch.randn(out.shape, generator=torch.Generator(device=dev).manual_seed(1),
+                                     device=dev))
+        dq = torch.empty((T, H, 576), dtype=torch.float32, device=dev)
+        dkv = torch.zeros((int(case.kv.rows), 576), dtype=torch.float32, device=dev)
+        fn = lambda: ops.dsa_sparse_mla_bwd(case.q, case.softmax_scale, case.kv, idx, lse, dout,
+                                            dq=dq, dkv=dkv)
+        clocks.start()
+        us = _timed(fn, args.steps, args.warmup, l2_flush)
+        clk = clocks.stop()
+        v = statistics.median(us)
+        rows = int((idx >= 0).sum())
+        # the backward's products: dS (q.K and dout.V) and dq, dK, dV, about
+        # 2.5 times the forward's 2 * H * 1088 flops per (token, row)
+        flop = 2.5 * 2.0 * H * 1088 * rows
+        res.update({"value": round(v, 3), "ms_per_step": round(v / 1000, 6),
+                    "dtype": "bf16 inputs, fp32 arithmetic (SIMT)",
+                    "config": {"workload": "sparse_mla_bwd_T%d_H%d" % (T, H), "tokens": T,
+                               "heads": H, "topk": case.k},
+                    "roofline": {"bound": "tensor", "unit": "TFLOP/s",
+                                 "achieved": round(flop / (v * 1e-6) / 1e12, 2),
+                                 "peak": bf16_tflops, "peak_kind": "measured bf16 dense",
+                                 "frac": round(flop / (v * 1e-6) / 1e12 / bf16_tflops, 4),
+                                 "flop": flop},
+                    "clocks": clk})
+    elif w == "paged":
         # the decode step on paged caches: pages of 64 slots, shuffled over the
         # pool, positions reached through the block table
         case = I.paged_decode(args.batch, args.context, page=64, device=dev)
@@ -600,7 +639,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "tiny", "uniform_fp8", "packed_1m", "prefill",
-                             "index", "topk", "mla", "mtp", "paged"],
+                             "index", "topk", "mla", "mtp", "paged", "bwd"],
                     help="decode (default): the driver's line; the others are secondary "
                          "measurements of the remaining configurations")
     ap.add_argument("--heads", type=int, default=64, help="prefill: attention heads")

@@ -289,6 +289,29 @@ int dsa_sparse_mla_fwd_ex(const void *q, int T, int H, int D, int Dv, float soft
   return status_of(sparse_mla_launch(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int dsa_sparse_mla_bwd(const void *q, int T, int H, int D, int Dv, float softmax_scale,
+                       const dsa_kv_pool *kv, const int32_t *idx, int k, const float *lse,
+                       const void *dout, const dsa_attn_opts *opts, float *dq, float *dkv,
+                       float *dsinks, int32_t *err_flag, dsa_stream_t stream) {
+  if (opts && opts->reserved != 0) return DSA_ERR_INVALID_ARG;
+  if (T < 0 || k < 1) return DSA_ERR_INVALID_ARG;
+  if (H < 1 || H > DSA_MAX_HEADS) return DSA_ERR_UNSUPPORTED;
+  if (D != 576 || Dv != 512 || !kv || kv->format != DSA_KV_BF16) return DSA_ERR_UNSUPPORTED;
+  int st = check_kv(kv, D);
+  if (st != DSA_OK) return st;
+  if (T == 0) return DSA_OK;
+  if (!q || !idx || !lse || !dout || !dq || !dkv) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(kv->data)) return DSA_ERR_INVALID_ARG;
+  MlaBwdArgs a{};
+  a.q = q; a.T = T; a.H = H; a.softmax_scale = softmax_scale;
+  a.kv = to_dev(kv); a.idx = idx; a.k = k;
+  a.lse = lse; a.lse_log2 = opts ? opts->lse_log2 != 0 : 0;
+  a.dout = dout;
+  a.sinks = opts ? opts->sinks : nullptr; a.dsinks = dsinks;
+  a.dq = dq; a.dkv = dkv; a.err_flag = err_flag;
+  return status_of(sparse_mla_bwd_launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t dsa_decode_workspace_size(int B, int64_t max_seq_len, int k, int H, int Dv, int k_swa) {
   if (B <= 0 || k <= 0 || H <= 0 || max_seq_len < 0 || k_swa < 0) return 0;
   return decode_layout(B, max_seq_len, k, H, Dv, k_swa, nullptr).bytes;

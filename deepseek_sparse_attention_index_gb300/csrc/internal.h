@@ -101,6 +101,25 @@ struct MlaArgs {
   const float *sinks;        // [H] per-head sink logits (natural-log units) or NULL
   int lse_log2;              // the final lse in log2 units
 };
+// backward of the sparse attention (bf16 pool, D = 576, Dv = 512, one list)
+struct MlaBwdArgs {
+  const void *q;             // bf16 [T, H, 576]
+  int T, H;
+  float softmax_scale;
+  PoolDev kv;
+  const int32_t *idx;        // [T, k] slots, -1 masked
+  int k;
+  const float *lse;          // [T, H] from the forward (natural log, or log2 when lse_log2)
+  int lse_log2;
+  const void *dout;          // bf16 [T, H, 512]
+  const float *sinks;        // [H] or NULL
+  float *dsinks;             // [H] accumulated, or NULL
+  float *dq;                 // [T, H, 576] written
+  float *dkv;                // [pool rows, 576] accumulated
+  int32_t *err_flag;
+};
+cudaError_t sparse_mla_bwd_launch(const MlaBwdArgs &a, cudaStream_t s);
+
 int mla_num_splits(int T, int H, int k_total);
 size_t mla_ws_bytes(int T, int H, int Dv, int k_total);
 void mla_ws_layout(int T, int H, int Dv, int k_total, void *ws, float **part_o, float **part_lse);

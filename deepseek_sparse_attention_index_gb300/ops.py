@@ -71,6 +71,9 @@ _SIGS = {
                                  c_p, c_i32, c_i32, c_i32, c_f32, ctypes.POINTER(DsaKvPool),
                                  ctypes.POINTER(DsaKvPool), c_p, c_i32,
                                  c_p, c_p, c_p, c_p, c_sz, c_p, ctypes.POINTER(DsaAttnOpts), c_p]),
+    "dsa_sparse_mla_bwd": (c_i32, [c_p, c_i32, c_i32, c_i32, c_i32, c_f32,
+                                   ctypes.POINTER(DsaKvPool), c_p, c_i32, c_p, c_p,
+                                   ctypes.POINTER(DsaAttnOpts), c_p, c_p, c_p, c_p, c_p]),
     "dsa_decode_workspace_size": (c_sz, [c_i32, c_i64, c_i32, c_i32, c_i32, c_i32]),
     "dsa_decode": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_i32, c_i32,
                            c_i32, c_p, c_p, c_i64, c_i32,
@@ -254,6 +257,28 @@ def dsa_sparse_mla_fwd(q, softmax_scale: float, kv: _inp.KVPool, idx, kv_extra=N
                                           ctypes.byref(o), _stream())
     _check(st, "dsa_sparse_mla_fwd")
     return out, lse
+
+
+def dsa_sparse_mla_bwd(q, softmax_scale: float, kv: _inp.KVPool, idx, lse, dout, sinks=None,
+                       lse_log2=False, dq=None, dkv=None, dsinks=None, err_flag=None):
+    """Backward of dsa_sparse_mla_fwd (see dsa_sparse_mla_bwd): returns dq fp32
+    [T, H, 576], dkv fp32 [pool rows, 576] (accumulated into `dkv` when given,
+    else into zeros) and dsinks fp32 [H] (with sinks)."""
+    T, H, D = q.shape
+    dev = q.device
+    if dq is None:
+        dq = torch.empty((T, H, D), dtype=torch.float32, device=dev)
+    if dkv is None:
+        dkv = torch.zeros((int(kv.rows), D), dtype=torch.float32, device=dev)
+    if dsinks is None and sinks is not None:
+        dsinks = torch.zeros((H,), dtype=torch.float32, device=dev)
+    o = _opts(sinks, lse_log2)
+    st = load().dsa_sparse_mla_bwd(_ptr(q), T, H, D, 512, float(softmax_scale),
+                                   _ref(kv_pool_struct(kv)), _ptr(idx), idx.shape[1], _ptr(lse),
+                                   _ptr(dout), None if o is None else ctypes.byref(o), _ptr(dq),
+                                   _ptr(dkv), _ptr(dsinks), _ptr(err_flag), _stream())
+    _check(st, "dsa_sparse_mla_bwd")
+    return dq, dkv, dsinks
 
 
 def dsa_decode_workspace_size(B, max_seq_len, k, H, Dv, k_swa=0) -> int:

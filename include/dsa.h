@@ -235,6 +235,31 @@ int dsa_sparse_mla_fwd_ex(const void *q, int T, int H, int D, int Dv, float soft
                           int32_t *err_flag, const dsa_attn_opts *opts, dsa_stream_t stream);
 
 /*
+ * dsa_sparse_mla_bwd -- backward of dsa_sparse_mla_fwd(_ex) for training
+ * (the "fwd + bwd per layer" workload of the Miles pull request #3608):
+ * the gradient of its definition given dL/dout, the lse being an auxiliary
+ * output that takes no gradient.  With p_j = e^{s_j - lse}:
+ *   delta = sum_j p_j (dout . V_j);   dS_j = p_j (dout . V_j - delta)
+ *   dq = scale sum_j dS_j K_j;   dK_j = scale sum_h dS_hj q_h, plus
+ *   sum_h p_hj dout_h on its V columns;   dsink_h = -e^{sink_h - lse} delta
+ * Each selected row's gradient (its K part plus its V part: the row serves as
+ * both) is ADDED into dkv at the row's slot, once per selection.
+ *   q, kv, idx, k, softmax_scale: as in the forward (bf16 pool, D = 576,
+ *            Dv = 512, one list); lse fp32 [T, H] as the forward returned it
+ *            with the same opts (sinks folded in; log2 units if lse_log2)
+ *   dout     bf16 [T, H, Dv]
+ *   dq       fp32 [T, H, D], written
+ *   dkv      fp32 [kv->rows, D], accumulated (the caller zeroes it first)
+ *   dsinks   fp32 [H], accumulated, or NULL (used with opts->sinks)
+ * A SIMT kernel (no tensor cores): correct first, not yet fast.
+ */
+int dsa_sparse_mla_bwd(const void *q, int T, int H, int D, int Dv, float softmax_scale,
+                       const dsa_kv_pool *kv, const int32_t *idx, int k,
+                       const float *lse, const void *dout, const dsa_attn_opts *opts,
+                       float *dq, float *dkv, float *dsinks,
+                       int32_t *err_flag, dsa_stream_t stream);
+
+/*
  * dsa_decode -- one fused decode step: score -> top-k -> sparse MLA for B
  * requests with one query token each (tokenspeed PR #627, Decode table:
  * "scores + TopK + sparse attn = total").
