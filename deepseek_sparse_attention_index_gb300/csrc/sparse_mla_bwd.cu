@@ -16,8 +16,8 @@
 // walks it again for dS (recomputing p and dout . V, so the forward's output
 // is not needed) and keeps dq in registers; each 16-row tile's row gradients
 // are a product over the CTA's heads (dS and p kept per tile in shared
-// memory), one global atomic per element.  Written for correctness first: a SIMT kernel, with no tensor
-// cores.
+// memory), one global atomic per element.  Written for correctness first: a
+// SIMT kernel, with no tensor cores.
 #include <cuda_bf16.h>
 #include <math.h>
 
