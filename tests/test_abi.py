@@ -19,7 +19,9 @@ def test_header_declares_the_boundary():
     names = ops.header_functions()
     for n in ["dsa_index_score", "dsa_topk", "dsa_sparse_mla_fwd", "dsa_decode",
               "dsa_topk_workspace_size", "dsa_sparse_mla_workspace_size",
-              "dsa_decode_workspace_size", "dsa_status_string", "dsa_abi_version"]:
+              "dsa_decode_workspace_size", "dsa_status_string", "dsa_abi_version",
+              "dsa_sparse_mla_fwd_ex", "dsa_decode_ex", "dsa_decode_paged", "dsa_decode_host",
+              "dsa_decode_host_workspace_size", "dsa_sparse_mla_bwd"]:
         assert n in names
 
 
@@ -107,3 +109,59 @@ def test_workspace_sizes_grow_with_the_problem(lib):
     b = lib.dsa_decode_workspace_size(32, 1 << 17, 2048, 64, 512, 0)
     assert 0 < a < b
     assert b >= 32 * (1 << 17) * 4   # the score rows live in the workspace
+
+
+def _opts(reserved=0, lse_log2=0):
+    o = ops.DsaAttnOpts()
+    o.sinks = None
+    o.lse_log2 = lse_log2
+    o.reserved = reserved
+    return o
+
+
+def test_attention_options_reserved_field_must_be_zero(lib):
+    st = lib.dsa_sparse_mla_fwd_ex(FAKE, 2, 8, 576, 512, 0.1, ctypes.byref(_pool(0, d_nope=512)),
+                                   FAKE, 4, None, None, 0, FAKE, FAKE, FAKE, 1 << 30, None,
+                                   ctypes.byref(_opts(reserved=1)), None)
+    assert st == 1
+
+
+def test_decode_paged_rejects_bad_arguments(lib):
+    def call(page=64, max_pages=16, max_len=1000, bt=FAKE, k=64, opts=None):
+        return lib.dsa_decode_paged(FAKE, 1, FAKE, FAKE, FAKE, 1 << 20, FAKE, 64, 128, 2, FAKE, bt,
+                                    max_pages, page, max_len, k, FAKE, 8, 576, 512, 0.1,
+                                    ctypes.byref(_pool(0, rows=1 << 20, d_nope=512)), None, None, 0,
+                                    None, FAKE, FAKE, FAKE, 1 << 34, None,
+                                    None if opts is None else ctypes.byref(opts), None)
+    assert call(page=50) == 2           # pages are multiples of 64 slots
+    assert call(page=0) == 2
+    assert call(max_pages=3) == 1       # 3 x 64 < max_seq_len
+    assert call(bt=None) == 1           # no block table
+    assert call(k=0) == 2
+    assert call(opts=_opts(reserved=7)) == 1
+
+
+def test_sparse_mla_backward_rejects_bad_arguments(lib):
+    def call(pool=None, D=576, Dv=512, dq=FAKE, T=2, k=4):
+        pool = pool if pool is not None else _pool(0, d_nope=512)
+        return lib.dsa_sparse_mla_bwd(FAKE, T, 8, D, Dv, 0.1, ctypes.byref(pool), FAKE, k, FAKE,
+                                      FAKE, None, dq, FAKE, None, None, None)
+    assert call(pool=_pool(1, d_nope=448), D=512, Dv=448) == 2   # bf16 pools only
+    assert call(D=512) == 2
+    assert call(dq=None) == 1
+    assert call(k=0) == 1
+    assert call(T=0) == 0
+
+
+def test_decode_host_rejects_bad_arguments(lib):
+    need = lib.dsa_decode_host_workspace_size(2, 1000, 64, 64, 128, 1, 8, 576, 512, 0)
+    assert need > lib.dsa_decode_workspace_size(2, 1000, 64, 8, 512, 0)
+
+    def call(h_q=FAKE, ws_bytes=need, k=64):
+        return lib.dsa_decode_host(FAKE, 1, FAKE, FAKE, FAKE, 1 << 20, FAKE, 64, 128, 2, FAKE,
+                                   FAKE, 1000, k, h_q, 8, 576, 512, 0.1,
+                                   ctypes.byref(_pool(0, rows=1 << 20, d_nope=512)), None, None, 0,
+                                   None, FAKE, FAKE, FAKE, ws_bytes, None, None)
+    assert call(h_q=None) == 1
+    assert call(ws_bytes=need - 1) == 3
+    assert call(k=ops.MAX_TOPK + 1) == 2
