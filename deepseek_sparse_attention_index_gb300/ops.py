@@ -74,6 +74,7 @@ _SIGS = {
     "dsa_sparse_mla_bwd": (c_i32, [c_p, c_i32, c_i32, c_i32, c_i32, c_f32,
                                    ctypes.POINTER(DsaKvPool), c_p, c_i32, c_p, c_p,
                                    ctypes.POINTER(DsaAttnOpts), c_p, c_p, c_p, c_p, c_p]),
+    "dsa_selftest_wait_timeout": (c_i32, [c_p, c_p, c_p]),
     "dsa_decode_workspace_size": (c_sz, [c_i32, c_i64, c_i32, c_i32, c_i32, c_i32]),
     "dsa_decode": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_i32, c_i32,
                            c_i32, c_p, c_p, c_i64, c_i32,
@@ -406,3 +407,15 @@ def decode_case(case: _inp.DecodeCase, ws=None, err_flag=None, idx_out=None, out
                       ind["w"], case.seq_lens, case.slot_base, case.max_seq_len, case.k, case.q,
                       case.softmax_scale, case.kv, case.kv_swa, case.idx_swa, idx_out=idx_out,
                       out=out, lse=lse, ws=ws, err_flag=err_flag)
+
+
+def selftest_wait_timeout():
+    """Runs dsa_selftest_wait_timeout on the current stream and returns
+    (err_flag, completed, cycles waited, limit) after synchronising."""
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    _check(load().dsa_selftest_wait_timeout(_ptr(flag), _ptr(out), _stream()),
+           "dsa_selftest_wait_timeout")
+    torch.cuda.synchronize()
+    o = out.cpu().tolist()
+    return int(flag.item()), o[0], o[1], o[2]

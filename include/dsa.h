@@ -359,6 +359,18 @@ int dsa_decode_host(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
                     int32_t *h_idx_out, void *h_out, float *h_lse,
                     void *ws, size_t ws_bytes, int32_t *err_flag, dsa_stream_t stream);
 
+/*
+ * dsa_selftest_wait_timeout -- a diagnostic of the failure detection: one
+ * GPU thread waits, through the same bounded wait every kernel here uses, on
+ * a barrier phase that nothing completes.  The wait gives up after its
+ * limit (about a second), ORs DSA_DEVERR_TIMEOUT into *err_flag and the
+ * kernel returns; the context stays usable.
+ *   err_flag  device int32
+ *   out       device int64 [3]: 1 if the wait completed (never), the cycles
+ *             waited, the limit in cycles
+ */
+int dsa_selftest_wait_timeout(int32_t *err_flag, long long *out, dsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -569,3 +569,15 @@ def test_prefill_packed_segments_pipeline():
                                                 O.gather_valid(c["kv"], gset + r0[t]),
                                                 c["softmax_scale"], 512)
         check_out_lse(out_np[t], lse_np[t], ref_out, ref_lse, "token %d" % t)
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """Failure detection: a wait on a barrier nothing completes gives up after
+    its limit, reports DSA_DEVERR_TIMEOUT, and the context keeps working."""
+    flag, done, waited, limit = ops.selftest_wait_timeout()
+    assert flag & ops.DEVERR_TIMEOUT
+    assert done == 0 and waited >= limit
+    case = I.tiny_decode(device="cuda")
+    idx, out, lse = ops.decode_case(case)
+    torch.cuda.synchronize()
+    assert torch.isfinite(lse).all()
