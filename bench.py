@@ -396,7 +396,7 @@ def run_workload(args):
     elif w == "paged":
         # the decode step on paged caches: pages of 64 slots, shuffled over the
         # pool, positions reached through the block table
-        case = I.paged_decode(args.batch, args.context, page=64, device=dev)
+        case = I.paged_decode(args.batch, args.context, page=args.page, device=dev)
         N = args.context
         ws = ops.workspace(ops.dsa_decode_workspace_size(case.B, N, case.k, case.H, case.Dv), dev)
         fn = lambda: ops.decode_case(case, ws=ws)
@@ -409,7 +409,7 @@ def run_workload(args):
         res.update({"value": round(v, 3), "ms_per_step": round(v / 1000, 6),
                     "dtype": "fp8_e4m3 indexer + bf16 attention (fp32 accumulate)",
                     "config": {"workload": case.name, "batch": case.B, "context": N,
-                               "page_size": 64, "topk": case.k, "heads": case.H},
+                               "page_size": args.page, "topk": case.k, "heads": case.H},
                     "step_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": nbytes,
                                       "achieved_gbs": round(nbytes / (v * 1e-6) / 1e9, 1),
                                       "frac": round(nbytes / (v * 1e-6) / 1e9 / hbm_gbs, 4),
@@ -643,6 +643,7 @@ def main():
                     help="decode (default): the driver's line; the others are secondary "
                          "measurements of the remaining configurations")
     ap.add_argument("--heads", type=int, default=64, help="prefill: attention heads")
+    ap.add_argument("--page", type=int, default=64, help="paged: slots per page (a multiple of 64)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", 0))
