@@ -365,8 +365,9 @@ def run_workload(args):
         rl = (case.row_end - case.row_start).contiguous()
         tws = ops.workspace(ops.dsa_topk_workspace_size(T, T, case.k), dev)
         idx = torch.empty((T, case.k), dtype=torch.int32, device=dev)
-        ops.dsa_index_score(ind["q_idx"], ind["idx_dtype"], ind["q_scale"], ind["k_idx"],
-                            ind["k_scale"], ind["w"], case.row_start, case.row_end, T, scores=scores)
+        ops.dsa_index_score_prefill(ind["q_idx"], ind["idx_dtype"], ind["q_scale"], ind["k_idx"],
+                                    ind["k_scale"], ind["w"], case.row_start, case.row_end, T,
+                                    scores=scores)
         ops.dsa_topk(scores, rl, case.k, T, index_base=case.row_start, idx=idx, ws=tws)
         out, lse = ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, idx)
         dout = I.to_bf16(torch.randn(out.shape, generator=torch.Generator(device=dev).manual_seed(1),
@@ -496,9 +497,9 @@ def run_workload(args):
         tws = ops.workspace(ops.dsa_topk_workspace_size(T, maxL, case.k), dev)
         mws = ops.workspace(ops.dsa_sparse_mla_workspace_size(T, H, 512, case.k, 0), dev)
         idx = torch.empty((T, case.k), dtype=torch.int32, device=dev)
-        f_idx = lambda: ops.dsa_index_score(ind["q_idx"], 1, ind["q_scale"], ind["k_idx"],
-                                            ind["k_scale"], ind["w"], case.row_start,
-                                            case.row_end, maxL, scores=scores)
+        f_idx = lambda: ops.dsa_index_score_prefill(ind["q_idx"], 1, ind["q_scale"], ind["k_idx"],
+                                                    ind["k_scale"], ind["w"], case.row_start,
+                                                    case.row_end, maxL, scores=scores)
         f_topk = lambda: ops.dsa_topk(scores, rl, case.k, maxL, index_base=case.row_start,
                                       idx=idx, ws=tws)
         f_mla = lambda: ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, idx, ws=mws)

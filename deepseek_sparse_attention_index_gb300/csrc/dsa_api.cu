@@ -192,6 +192,27 @@ HostStaging host_staging(int B, int64_t max_seq_len, int k, int H_I, int d_idx, 
   return S;
 }
 
+// dsa_index_score and dsa_index_score_prefill: the checks and the argument
+// block are the same; `groups` picks the kernel
+int index_score_entry(const void *q_idx, int idx_dtype, const float *q_scale, const void *k_idx,
+                      const float *k_scale, int64_t k_rows, const float *w,
+                      const int32_t *row_start, const int32_t *row_end, int T, int H_I, int d,
+                      int64_t max_len, float *scores, int64_t ld_scores, int32_t *err_flag,
+                      dsa_stream_t stream, bool groups) {
+  int st = check_indexer(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, T, H_I, d);
+  if (st != DSA_OK) return st;
+  if (max_len < 0 || ld_scores < max_len) return DSA_ERR_INVALID_ARG;
+  if (T > 0 && (!row_start || !row_end || !scores)) return DSA_ERR_INVALID_ARG;
+  IndexScoreArgs a{};
+  a.q_idx = q_idx; a.idx_dtype = idx_dtype; a.q_scale = q_scale;
+  a.k_idx = k_idx; a.k_scale = k_scale; a.k_rows = k_rows; a.w = w;
+  a.row_start = row_start; a.row_end = row_end;
+  a.T = T; a.H_I = H_I; a.d = d; a.max_len = max_len;
+  a.scores = scores; a.ld_scores = ld_scores; a.err_flag = err_flag;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return status_of(groups ? index_score_prefill_launch(a, s) : index_score_launch(a, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -214,17 +235,17 @@ int dsa_index_score(const void *q_idx, int idx_dtype, const float *q_scale, cons
                     const int32_t *row_start, const int32_t *row_end, int T, int H_I, int d,
                     int64_t max_len, float *scores, int64_t ld_scores, int32_t *err_flag,
                     dsa_stream_t stream) {
-  int st = check_indexer(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, T, H_I, d);
-  if (st != DSA_OK) return st;
-  if (max_len < 0 || ld_scores < max_len) return DSA_ERR_INVALID_ARG;
-  if (T > 0 && (!row_start || !row_end || !scores)) return DSA_ERR_INVALID_ARG;
-  IndexScoreArgs a{};
-  a.q_idx = q_idx; a.idx_dtype = idx_dtype; a.q_scale = q_scale;
-  a.k_idx = k_idx; a.k_scale = k_scale; a.k_rows = k_rows; a.w = w;
-  a.row_start = row_start; a.row_end = row_end;
-  a.T = T; a.H_I = H_I; a.d = d; a.max_len = max_len;
-  a.scores = scores; a.ld_scores = ld_scores; a.err_flag = err_flag;
-  return status_of(index_score_launch(a, reinterpret_cast<cudaStream_t>(stream)));
+  return index_score_entry(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, row_start, row_end,
+                           T, H_I, d, max_len, scores, ld_scores, err_flag, stream, false);
+}
+
+int dsa_index_score_prefill(const void *q_idx, int idx_dtype, const float *q_scale,
+                            const void *k_idx, const float *k_scale, int64_t k_rows,
+                            const float *w, const int32_t *row_start, const int32_t *row_end,
+                            int T, int H_I, int d, int64_t max_len, float *scores,
+                            int64_t ld_scores, int32_t *err_flag, dsa_stream_t stream) {
+  return index_score_entry(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, row_start, row_end,
+                           T, H_I, d, max_len, scores, ld_scores, err_flag, stream, true);
 }
 
 size_t dsa_topk_workspace_size(int T, int64_t max_len, int k) {

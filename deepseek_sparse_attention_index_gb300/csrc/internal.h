@@ -70,6 +70,10 @@ struct IndexScoreArgs {
   int page_size;               // a multiple of 64
 };
 cudaError_t index_score_launch(const IndexScoreArgs &a, cudaStream_t s);
+// The prefill form (row ranges, no histogram): groups of four consecutive
+// rows share each key tile where they start at the same key
+// (index_score_groups.cu); shapes it does not take go to index_score_launch.
+cudaError_t index_score_prefill_launch(const IndexScoreArgs &a, cudaStream_t s);
 
 
 // ------------------------------------------------------------------ sparse MLA

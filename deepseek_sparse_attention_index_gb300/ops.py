@@ -48,6 +48,8 @@ _SIGS = {
     "dsa_abi_version": (c_i32, []),
     "dsa_index_score": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_p, c_p, c_i32, c_i32,
                                 c_i32, c_i64, c_p, c_i64, c_p, c_p]),
+    "dsa_index_score_prefill": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_p, c_p, c_i32,
+                                        c_i32, c_i32, c_i64, c_p, c_i64, c_p, c_p]),
     "dsa_topk_workspace_size": (c_sz, [c_i32, c_i64, c_i32]),
     "dsa_topk": (c_i32, [c_p, c_i64, c_p, c_i32, c_i64, c_i32, c_p, c_p, c_p, c_p, c_sz, c_p,
                          c_p]),
@@ -175,19 +177,33 @@ def _ref(s):
 
 # ---------------------------------------------------------------- entry points
 
-def dsa_index_score(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, row_start, row_end,
-                    max_len: int, scores=None, err_flag=None):
-    """Scores [T, ld] fp32 (see dsa_index_score in include/dsa.h)."""
+def _index_score(entry, q_idx, idx_dtype, q_scale, k_idx, k_scale, w, row_start, row_end,
+                 max_len, scores, err_flag):
     T, H_I, d = q_idx.shape
     if scores is None:
         ld = (int(max_len) + 3) // 4 * 4
         scores = torch.full((T, max(ld, 1)), float("nan"), dtype=torch.float32, device=q_idx.device)
-    st = load().dsa_index_score(_ptr(q_idx), idx_dtype, _ptr(q_scale), _ptr(k_idx), _ptr(k_scale),
+    st = getattr(load(), entry)(_ptr(q_idx), idx_dtype, _ptr(q_scale), _ptr(k_idx), _ptr(k_scale),
                                 k_idx.shape[0], _ptr(w), _ptr(row_start), _ptr(row_end), T, H_I, d,
                                 int(max_len), _ptr(scores), scores.shape[1], _ptr(err_flag),
                                 _stream())
-    _check(st, "dsa_index_score")
+    _check(st, entry)
     return scores
+
+
+def dsa_index_score(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, row_start, row_end,
+                    max_len: int, scores=None, err_flag=None):
+    """Scores [T, ld] fp32 (see dsa_index_score in include/dsa.h)."""
+    return _index_score("dsa_index_score", q_idx, idx_dtype, q_scale, k_idx, k_scale, w,
+                        row_start, row_end, max_len, scores, err_flag)
+
+
+def dsa_index_score_prefill(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, row_start, row_end,
+                            max_len: int, scores=None, err_flag=None):
+    """The same scores, for causal prefill rows: four rows that start at the
+    same key share each key tile (see dsa_index_score_prefill)."""
+    return _index_score("dsa_index_score_prefill", q_idx, idx_dtype, q_scale, k_idx, k_scale, w,
+                        row_start, row_end, max_len, scores, err_flag)
 
 
 def dsa_topk_workspace_size(T: int, max_len: int, k: int) -> int:

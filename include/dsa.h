@@ -137,6 +137,27 @@ int dsa_index_score(const void *q_idx, int idx_dtype, const float *q_scale,
                     int32_t *err_flag, dsa_stream_t stream);
 
 /*
+ * dsa_index_score_prefill -- dsa_index_score for causal prefill rows.
+ * The same arguments, limits, errors and result as dsa_index_score (the
+ * "Prefill" table of tokenspeed PR #627 times this stage over causal rows).
+ * Rows are taken four at a time (rows 4g .. 4g+3).  Where the group's
+ * non-empty rows all start at the same key -- the rows of one segment of a
+ * causal prefill, [segment start, t + 1) -- each 128-key tile of the union of
+ * their ranges is read and multiplied once for all four rows.  Other groups
+ * (a segment boundary inside the group, unrelated ranges) are walked one row
+ * at a time.  Any ranges are accepted; grouping pays where consecutive rows
+ * share their start.  Shapes without a one-block fast form (bf16 d = 128) and
+ * T < 4 run as dsa_index_score does.  Rows of a decode batch, each with its
+ * own keys, are better served by dsa_index_score.
+ */
+int dsa_index_score_prefill(const void *q_idx, int idx_dtype, const float *q_scale,
+                            const void *k_idx, const float *k_scale, int64_t k_rows,
+                            const float *w, const int32_t *row_start, const int32_t *row_end,
+                            int T, int H_I, int d, int64_t max_len,
+                            float *scores, int64_t ld_scores,
+                            int32_t *err_flag, dsa_stream_t stream);
+
+/*
  * dsa_topk -- per-row top-k with -1 padding.
  * The "TopK" stage of tokenspeed PR #627 (Benchmark results; the selector
  * counts "greater" and "equal" elements against a threshold) with the -1

@@ -21,7 +21,7 @@ def test_header_declares_the_boundary():
               "dsa_topk_workspace_size", "dsa_sparse_mla_workspace_size",
               "dsa_decode_workspace_size", "dsa_status_string", "dsa_abi_version",
               "dsa_sparse_mla_fwd_ex", "dsa_decode_ex", "dsa_decode_paged", "dsa_decode_host",
-              "dsa_decode_host_workspace_size", "dsa_sparse_mla_bwd"]:
+              "dsa_decode_host_workspace_size", "dsa_sparse_mla_bwd", "dsa_index_score_prefill"]:
         assert n in names
 
 
@@ -92,10 +92,11 @@ def test_sparse_mla_rejects_bad_arguments(lib):
         assert _mla(lib, _pool(0, d_nope=512), ws_bytes=need - 1) == 3
 
 
-def test_index_score_rejects_bad_arguments(lib):
+@pytest.mark.parametrize("entry", ["dsa_index_score", "dsa_index_score_prefill"])
+def test_index_score_rejects_bad_arguments(lib, entry):
     def call(idx_dtype=1, H_I=64, d=128, q_scale=FAKE, ld=128, max_len=100):
-        return lib.dsa_index_score(FAKE, idx_dtype, q_scale, FAKE, FAKE, 1000, FAKE, FAKE, FAKE,
-                                   2, H_I, d, max_len, FAKE, ld, None, None)
+        return getattr(lib, entry)(FAKE, idx_dtype, q_scale, FAKE, FAKE, 1000, FAKE, FAKE, FAKE,
+                                   8, H_I, d, max_len, FAKE, ld, None, None)
     assert call(H_I=65) == 2
     assert call(H_I=12) == 2
     assert call(d=64) == 2           # fp8 needs d = 128

@@ -549,8 +549,8 @@ def test_prefill_packed_segments_pipeline():
     case = I.prefill_case([1, 1, 700, 2600, 300], k=2048, H=16, device="cuda")
     ind = case.indexer
     maxL = int((case.row_end - case.row_start).max())
-    sc = ops.dsa_index_score(ind["q_idx"], 1, ind["q_scale"], ind["k_idx"], ind["k_scale"],
-                             ind["w"], case.row_start, case.row_end, maxL)
+    sc = ops.dsa_index_score_prefill(ind["q_idx"], 1, ind["q_scale"], ind["k_idx"],
+                                     ind["k_scale"], ind["w"], case.row_start, case.row_end, maxL)
     rl = (case.row_end - case.row_start).contiguous()
     idx, lens = ops.dsa_topk(sc, rl, case.k, maxL, index_base=case.row_start)
     out, lse = ops.dsa_sparse_mla_fwd(case.q, case.softmax_scale, case.kv, idx)
