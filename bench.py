@@ -488,9 +488,13 @@ def run_workload(args):
                     "clocks": clk})
     elif w == "prefill":
         T, H = args.context, args.heads
-        case = I.prefill_case([T], k=2048, H=H, device=dev)
+        # one causal sequence of T tokens, or a packed batch of segments with
+        # lengths drawn U[1, 8192] (two 1-token segments first) summing to T
+        seg = [T] if args.segments == "single" else I.packed_segment_lengths(T)
+        case = I.prefill_case(seg, k=2048, H=H, device=dev)
         ind = case.indexer
-        maxL = T
+        lens = (case.row_end - case.row_start).cpu()
+        maxL = int(lens.max())
         ld = (maxL + 3) // 4 * 4
         scores = torch.empty((T, ld), dtype=torch.float32, device=dev)
         rl = (case.row_end - case.row_start).contiguous()
@@ -508,15 +512,15 @@ def run_workload(args):
               "topk": statistics.median(_timed(f_topk, args.steps, args.warmup, l2_flush)),
               "sparse_mla": statistics.median(_timed(f_mla, args.steps, args.warmup, l2_flush))}
         clk = clocks.stop()
-        R = sum(min(t + 1, case.k) for t in range(T))
+        R = int(lens.clamp(max=case.k).sum())
         mla_flop = 2.0 * H * R * 1088
-        idx_flop = 2.0 * 64 * 128 * T * (T + 1) / 2
+        idx_flop = 2.0 * 64 * 128 * int(lens.sum())
         v = sum(st.values())
         fp8_tflops = 2.0 * bf16_tflops   # the fp8 dense rate is twice bf16's
         res.update({"value": round(v, 3), "ms_per_step": round(v / 1000, 6),
                     "dtype": "fp8_e4m3 indexer + bf16 attention (fp32 accumulate)",
-                    "config": {"workload": "prefill_T%d_H%d" % (T, H), "tokens": T, "heads": H,
-                               "topk": case.k},
+                    "config": {"workload": "prefill_%sT%d_H%d" % ("" if len(seg) == 1 else "packed_", T, H),
+                               "tokens": T, "heads": H, "topk": case.k, "segments": len(seg)},
                     "stages_us": {k: round(x, 2) for k, x in st.items()},
                     "roofline": {"sparse_mla": {"bound": "tensor", "unit": "TFLOP/s",
                                                 "achieved": round(mla_flop / (st["sparse_mla"] * 1e-6) / 1e12, 1),
@@ -644,6 +648,8 @@ def main():
                     help="decode (default): the driver's line; the others are secondary "
                          "measurements of the remaining configurations")
     ap.add_argument("--heads", type=int, default=64, help="prefill: attention heads")
+    ap.add_argument("--segments", default="single", choices=["single", "packed"],
+                    help="prefill: one causal sequence, or packed segments of U[1, 8192] tokens")
     ap.add_argument("--page", type=int, default=64, help="paged: slots per page (a multiple of 64)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
