@@ -49,12 +49,17 @@
 // of issue each; one warp of cp.async moves as much per instruction at a
 // fraction of that.)
 //
-// S and PV are issued by two warps: small MMAs have a per-instruction issue
-// floor (~55 cycles for any N <= 64 from one thread), and a second issuing
-// thread roughly doubles the rate for the 64 x 64 S products.  The S warp
-// runs ahead as soon as a tile has landed; the PV warp follows the softmax.
+// S and PV are issued by four warps.  Small MMAs have a per-instruction
+// issue floor (~55 cycles for any N <= 64 from one thread, however many
+// accumulators it alternates between), and each further issuing thread adds
+// its own stream.  S is split by K-block: warp 4 issues the even K-blocks
+// into S_a, warp 10 the odd ones into S_b, and the softmax adds the two.  PV
+// is split by dv block: warp 5 issues blocks 0-1, warp 11 blocks 2-3.  The S
+// warps run ahead as soon as a tile has landed; the PV warps follow the
+// softmax.
 //
-// Warps: 0-3 math, 4 S issue, 5 PV issue (and the Q load), 6-7 gather.
+// Warps: 0-3 math, 4 and 10 S issue, 5 (and the Q load) and 11 PV issue,
+// 6-9 gather.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -66,8 +71,9 @@ namespace dsa {
 
 namespace {
 
-// Warps 0-3 math, 4 S issue, 5 PV issue, 6-9 gather: 10 warps, so at most
-// 168 registers a thread (three warps share an SM sub-partition).
+// Warps 0-3 math, 4 and 10 S issue, 5 and 11 PV issue, 6-9 gather: 12
+// warps, so at most 168 registers a thread (three warps share an SM
+// sub-partition).
 constexpr int kTileRows = 64;
 constexpr int kKBlockBytes = kTileRows * 128;               // 8 KB: 64 rows x 64 16-bit values
 
@@ -90,9 +96,9 @@ template <int FMT> struct FmtTraits {
   // gather warps: four, 16 rows each per tile (bf16: cp.async issue split
   // four ways; fp8: every 16-byte load of a tile in flight at once)
   static constexpr int kGatherWarps = 4;
-  static constexpr int kThreads = 32 * (6 + kGatherWarps);
-  // register bound: with 10 warps three share an SM sub-partition (16K
-  // registers), so at most 168 a thread -- declared as a 384-thread bound
+  static constexpr int kThreads = 32 * (8 + kGatherWarps);
+  // register bound: with 12 warps three share an SM sub-partition (16K
+  // registers), so at most 168 a thread
   static constexpr int kBoundThreads = 384;
   static constexpr int kQBytes = kKBlocks * 64 * 128;           // Q padded to 64 heads
 };
@@ -297,6 +303,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 14);
   uint64_t *qready = bars + 15;   // fp8 pools: Q converted to fp16 by the math warps
+  uint64_t *done2 = bars + 16;    // [2]: second S warp, second PV warp
   uint64_t *lastpv = bars + 22;   // [4]: the last tile's PV into dv block j retired
 
   const int warp = threadIdx.x >> 5;
@@ -309,9 +316,10 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   const int j0 = min(total, split * per);   // per: a multiple of the tile
   const int je = min(total, j0 + per);
   const int nt = (je - j0 + kTileRows - 1) / kTileRows;
-  // TMEM: S[2] at columns [0, 128), O^T blocks at [128, 128 + 4N)
-  constexpr uint32_t kSCol = 0, kOCol = 128;
-  constexpr uint32_t kTmemCols = 128 + 4 * N <= 256 ? 256 : 512;
+  // TMEM: S_a[2] at columns [0, 128), S_b[2] at [128, 256), O^T blocks at
+  // [256, 256 + 4N)
+  constexpr uint32_t kSCol = 0, kSbCol = 128, kOCol = 256;
+  constexpr uint32_t kTmemCols = 512;
 
   if ((tc::smem_u32(smem) & 1023u) != 0) {  // the swizzled layouts need 1 KB alignment
     if (threadIdx.x == 0) raise_flag(a.err_flag, DSA_DEVERR_TIMEOUT);
@@ -320,14 +328,16 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&kfull[i], 32 * F::kGatherWarps);
-      tc::mbar_init(&kempty[i], 1);
-      tc::mbar_init(&sfull[i], 1);
+      tc::mbar_init(&kempty[i], 2);       // both PV warps
+      tc::mbar_init(&sfull[i], 2);        // both S warps
       tc::mbar_init(&sempty[i], 4);
     }
     tc::mbar_init(pfull, 4);
-    tc::mbar_init(pempty, 1);
+    tc::mbar_init(pempty, 2);             // both PV warps
     tc::mbar_init(&done[0], 1);
     tc::mbar_init(&done[1], 1);
+    tc::mbar_init(&done2[0], 1);
+    tc::mbar_init(&done2[1], 1);
     tc::mbar_init(qfull, 1);
     tc::mbar_init(qready, 4);
     for (int j = 0; j < 4; ++j) tc::mbar_init(&lastpv[j], 1);
@@ -356,7 +366,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   pdl_trigger();
   if (warp == 5 && lane == 0 && !a.q_ready) load_q();
 
-  if (warp >= 6 && FMT == kFmtBf16) {
+  if (warp >= 6 && warp < 10 && FMT == kFmtBf16) {
     // -------------------------------------------------------------- gather (bf16)
     const int gw = warp - 6;            // rows [16*gw, 16*gw + 16) of every tile
     // this lane's row of tile i (row 16*gw + lane, lanes < 16), or nullptr
@@ -410,7 +420,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     }
     cp_async_wait_all();
     __syncwarp();
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 10) {
     // -------------------------------------------------------------- gather (fp8)
     // A tile is a flat list of 16-byte chunks, CPR per row (uniform: 32 e4m3
     // chunks; packed: 28 e4m3 NoPE chunks + 8 bf16 RoPE chunks); gather lane
@@ -514,8 +524,10 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.err_flag, DSA_DEVERR_FP16_RANGE);
     __syncwarp();
-  } else if (warp == 4) {
+  } else if (warp == 4 || warp == 10) {
     // -------------------------------------------------------------- S issue
+    // warp 4: the even K-blocks into S_a; warp 10: the odd ones into S_b
+    const int sh = warp == 10 ? 1 : 0;
     if (lane == 0) {
       // S = Q K^T: A = Q (K-major, M = 64), B = K tile (K-major, N = 64)
       constexpr uint32_t idesc_s = tc::idesc_f32acc(F::kOpType, F::kOpType, 0, 0, 64, 64);
@@ -530,13 +542,14 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         // descriptors: the start-address field is the byte address / 16, so
         // a K-block (8192 B) adds 512 and 32 bytes of K add 2
         const uint64_t bdk = tc::sdesc_sw128(tc::smem_u32(k_s + st * kStageBytes), 16, 1024);
-        const uint32_t dcol = tmem + kSCol + sb * 64;
+        const uint32_t dcol = tmem + (sh ? kSbCol : kSCol) + sb * 64;
 #pragma unroll
         for (int kb = 0; kb < kKBlocks; ++kb) {
+          if ((kb & 1) != sh) continue;
 #pragma unroll
           for (int ko = 0; ko < 4; ++ko)   // 32 bytes (16 values) of K per instruction
             tc::mma_f16(dcol, adq + kb * 512 + 2 * ko, bdk + kb * 512 + 2 * ko, idesc_s,
-                        (kb > 0 || ko > 0) ? 1u : 0u);
+                        (kb > sh || ko > 0) ? 1u : 0u);
           if (F::kLoBlocks > 0) {          // the low plane of the same K-block
 #pragma unroll
             for (int ko = 0; ko < 4; ++ko)
@@ -548,13 +561,16 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       }
       if (nt > 0) {
         // this warp's MMAs retired before TMEM is released
-        tc::mma_commit(&done[0]);
-        tc::mbar_wait_drain(&done[0], 0);
+        uint64_t *d = sh ? &done2[0] : &done[0];
+        tc::mma_commit(d);
+        tc::mbar_wait_drain(d, 0);
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 5 || warp == 11) {
     // -------------------------------------------------------------- PV issue
+    // warp 5: dv blocks 0 and 1; warp 11: blocks 2 and 3
+    const int ph = warp == 11 ? 1 : 0;
     if (lane == 0) {
       // O^T += V^T P^T: A = V^T (MN-major, M = 128), B = P (K-major, N heads)
       constexpr uint32_t idesc_pv = tc::idesc_f32acc(F::kOpType, F::kOpType, 1, 0, N, 128);
@@ -571,7 +587,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         const uint64_t bdp = tc::sdesc_sw128(p_addr, 16, 1024);
         const uint64_t bdl = tc::sdesc_sw128(k_addr + 8 * kKBlockBytes, 16, 1024);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 2 * ph; j < 2 * ph + 2; ++j) {
 #pragma unroll
           for (int kk = 0; kk < F::kPvSteps; ++kk) {
             const uint32_t kr = kk & 3;   // 16 kv rows per instruction
@@ -583,7 +599,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         tc::mma_commit(&kempty[st]);
         tc::mma_commit(pempty);
       }
-      if (nt > 0) tc::mma_commit(&done[1]);   // waited for after the epilogue
+      if (nt > 0) tc::mma_commit(ph ? &done2[1] : &done[1]);   // waited for after the epilogue
     }
     __syncwarp();
   } else {
@@ -625,7 +641,13 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       if (!tc::mbar_wait(&sfull[b], (i >> 1) & 1, abort_flag)) { ok = false; break; }
       tc::fence_after_sync();
       float x[32];                          // this lane's half of its head's 64 scores
-      tc::tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kSCol + b * 64, x);
+      {
+        float xb[32];                       // S = S_a + S_b (even and odd K-blocks)
+        tc::tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kSCol + b * 64, x);
+        tc::tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kSbCol + b * 64, xb);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] += xb[j];
+      }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sempty[b]);
@@ -769,10 +791,11 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     }
   }
   if (warp == 5 && lane == 0) {
-    // the PV warp's MMAs retired and the Q load landed before TMEM is released
+    // the PV warps' MMAs retired and the Q load landed before TMEM is released
     if (nt > 0) tc::mbar_wait_drain(&done[1], 0);
     tc::mbar_wait_drain(qfull, 0);
   }
+  if (warp == 11 && lane == 0 && nt > 0) tc::mbar_wait_drain(&done2[1], 0);
 
   tc::fence_before_sync();
   __syncthreads();
