@@ -2,6 +2,7 @@
 // Host side only: argument checks, workspace carving and stream-ordered
 // launches of the kernels in index_score.cu, topk.cu and sparse_mla.cu.
 #include <stdint.h>
+#include <new>
 #include <string.h>
 
 #include "common.cuh"
@@ -214,6 +215,11 @@ int index_score_entry(const void *q_idx, int idx_dtype, const float *q_scale, co
 }
 
 }  // namespace
+
+// A captured host-buffer decode step (dsa_decode_graph_create).
+struct dsa_decode_graph_s {
+  cudaGraphExec_t exec;
+};
 
 extern "C" {
 
@@ -467,6 +473,55 @@ int dsa_decode_host(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
        cudaMemcpyAsync(h_out, S.out, (size_t)B * H * Dv * 2, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
        cudaMemcpyAsync(h_lse, S.lse, (size_t)B * H * 4, cudaMemcpyDeviceToHost, s) == cudaSuccess;
   return ok ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_decode_graph_create(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
+                            const void *k_idx, const float *k_scale, int64_t k_rows,
+                            const float *h_w, int H_I, int d_idx, int B,
+                            const int32_t *h_seq_lens, const int32_t *h_slot_base,
+                            int64_t max_seq_len, int k, const void *h_q, int H, int D, int Dv,
+                            float softmax_scale, const dsa_kv_pool *kv, const dsa_kv_pool *kv_swa,
+                            const int32_t *h_idx_swa, int k_swa, int32_t *h_idx_out, void *h_out,
+                            float *h_lse, void *ws, size_t ws_bytes, int32_t *err_flag,
+                            dsa_decode_graph *graph) {
+  if (!graph) return DSA_ERR_INVALID_ARG;
+  *graph = nullptr;
+  if (B < 1) return DSA_ERR_INVALID_ARG;   // an empty step has nothing to capture
+  cudaStream_t cs;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return DSA_ERR_CUDA;
+  int st = DSA_ERR_CUDA;
+  cudaGraph_t g = nullptr;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+    st = dsa_decode_host(h_q_idx, idx_dtype, h_q_scale, k_idx, k_scale, k_rows, h_w, H_I, d_idx, B,
+                         h_seq_lens, h_slot_base, max_seq_len, k, h_q, H, D, Dv, softmax_scale, kv,
+                         kv_swa, h_idx_swa, k_swa, h_idx_out, h_out, h_lse, ws, ws_bytes, err_flag,
+                         reinterpret_cast<dsa_stream_t>(cs));
+    // the capture ends whatever happened inside it
+    if (cudaStreamEndCapture(cs, &g) != cudaSuccess && st == DSA_OK) st = DSA_ERR_CUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (st == DSA_OK && cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) st = DSA_ERR_CUDA;
+  if (g) cudaGraphDestroy(g);
+  cudaStreamDestroy(cs);
+  if (st != DSA_OK) return st;
+  dsa_decode_graph h = new (std::nothrow) dsa_decode_graph_s{exec};
+  if (!h) {
+    cudaGraphExecDestroy(exec);
+    return DSA_ERR_CUDA;
+  }
+  *graph = h;
+  return DSA_OK;
+}
+
+int dsa_decode_graph_launch(dsa_decode_graph graph, dsa_stream_t stream) {
+  if (!graph) return DSA_ERR_INVALID_ARG;
+  return status_of(cudaGraphLaunch(graph->exec, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+void dsa_decode_graph_destroy(dsa_decode_graph graph) {
+  if (!graph) return;
+  cudaGraphExecDestroy(graph->exec);
+  delete graph;
 }
 
 }  // extern "C"

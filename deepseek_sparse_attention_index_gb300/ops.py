@@ -90,6 +90,14 @@ _SIGS = {
                                 c_p, c_i32, c_i32, c_i32, c_f32, ctypes.POINTER(DsaKvPool),
                                 ctypes.POINTER(DsaKvPool), c_p, c_i32,
                                 c_p, c_p, c_p, c_p, c_sz, c_p, c_p]),
+    "dsa_decode_graph_create": (c_i32, [c_p, c_i32, c_p, c_p, c_p, c_i64, c_p, c_i32, c_i32,
+                                        c_i32, c_p, c_p, c_i64, c_i32,
+                                        c_p, c_i32, c_i32, c_i32, c_f32,
+                                        ctypes.POINTER(DsaKvPool), ctypes.POINTER(DsaKvPool), c_p,
+                                        c_i32, c_p, c_p, c_p, c_p, c_sz, c_p,
+                                        ctypes.POINTER(c_p)]),
+    "dsa_decode_graph_launch": (c_i32, [c_p, c_p]),
+    "dsa_decode_graph_destroy": (None, [c_p]),
 }
 
 _lib = None
@@ -374,6 +382,64 @@ def dsa_decode_host(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, slot
                                 _ptr(ws), ws.numel(), _ptr(err_flag), _stream())
     _check(st, "dsa_decode_host")
     return idx_out, out, lse
+
+
+class DecodeGraph:
+    """dsa_decode_graph: the host-buffer decode step captured once and
+    replayed by launch().  Every buffer is bound at creation: the caller
+    rewrites the pinned inputs in place between launches (q_idx, q_scale, w,
+    seq_lens, slot_base, q, idx_swa) and reads idx_out / out / lse once a
+    launch has completed on its stream.  The arguments are those of
+    dsa_decode_host; host tensors must be pinned."""
+
+    def __init__(self, q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, slot_base,
+                 max_seq_len: int, k: int, q, softmax_scale: float, kv: _inp.KVPool,
+                 kv_swa=None, idx_swa=None, idx_out=None, out=None, lse=None, ws=None,
+                 err_flag=None):
+        for t in (q_idx, q_scale, w, seq_lens, slot_base, q, idx_swa, idx_out, out, lse):
+            if t is not None and (t.is_cuda or not t.is_pinned()):
+                raise ValueError("DecodeGraph binds pinned host buffers")
+        B, H_I, d_idx = q_idx.shape
+        _, H, D = q.shape
+        Dv = kv.d_nope if kv.format != _inp.KV_BF16 else 512
+        k_swa = 0 if idx_swa is None else idx_swa.shape[1]
+        self.idx_out = idx_out if idx_out is not None else \
+            torch.empty((B, k), dtype=torch.int32).pin_memory()
+        self.out = out if out is not None else \
+            torch.empty((B, H, Dv), dtype=torch.bfloat16).pin_memory()
+        self.lse = lse if lse is not None else torch.empty((B, H), dtype=torch.float32).pin_memory()
+        need = dsa_decode_host_workspace_size(B, max_seq_len, k, H_I, d_idx, idx_dtype, H, D, Dv,
+                                              k_swa)
+        self.ws = ws if ws is not None else workspace(need, k_idx.device)
+        # everything the graph reads or writes stays referenced as long as it
+        self._keep = (q_idx, q_scale, k_idx, k_scale, w, seq_lens, slot_base, q, kv, kv_swa,
+                      idx_swa, err_flag)
+        self._s1, self._s2 = kv_pool_struct(kv), kv_pool_struct(kv_swa)
+        h = c_p()
+        st = load().dsa_decode_graph_create(
+            _hptr(q_idx), idx_dtype, _hptr(q_scale), _ptr(k_idx), _ptr(k_scale), k_idx.shape[0],
+            _hptr(w), H_I, d_idx, B, _hptr(seq_lens), _hptr(slot_base), int(max_seq_len), k,
+            _hptr(q), H, D, Dv, float(softmax_scale), _ref(self._s1), _ref(self._s2),
+            _hptr(idx_swa), k_swa, _hptr(self.idx_out), _hptr(self.out), _hptr(self.lse),
+            _ptr(self.ws), self.ws.numel(), _ptr(err_flag), ctypes.byref(h))
+        _check(st, "dsa_decode_graph_create")
+        self._h = h
+
+    def launch(self):
+        """Enqueues one step on the current stream."""
+        _check(load().dsa_decode_graph_launch(self._h, _stream()), "dsa_decode_graph_launch")
+        return self.idx_out, self.out, self.lse
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load().dsa_decode_graph_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def dsa_decode_paged(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, block_table,

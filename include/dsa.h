@@ -381,6 +381,46 @@ int dsa_decode_host(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
                     void *ws, size_t ws_bytes, int32_t *err_flag, dsa_stream_t stream);
 
 /*
+ * dsa_decode_graph -- the host-buffer decode step (dsa_decode_host) captured
+ * once into a CUDA graph and replayed step after step.  No passage of the
+ * DSA pages has a counterpart: this is a service of this library for decode
+ * loops, where one graph launch replaces the call's ten copies and five
+ * kernel launches.
+ * dsa_decode_graph_create takes the arguments of dsa_decode_host (no stream:
+ * it captures on a stream of its own) and binds every pointer: the graph
+ * copies from and to the SAME host buffers, reads the same caches and pools
+ * and uses the same workspace at every launch.  Between launches the caller
+ * rewrites the inputs in place (h_q, h_q_idx, h_q_scale, h_w, h_seq_lens,
+ * h_slot_base, h_idx_swa; the caches and pools on the device) and reads the
+ * outputs (h_idx_out, h_out, h_lse) once the launch has completed on its
+ * stream.  B, max_seq_len, k and the shapes are fixed at creation; host
+ * buffers must be page-locked (pinned); max_seq_len must bound every later
+ * seq_lens.  The host checks of dsa_decode_host run once, at creation.
+ *   *graph     receives the handle (NULL on error); it owns a CUDA graph,
+ *              not device memory
+ * dsa_decode_graph_launch enqueues one step on `stream` (a launch on another
+ * stream may not overlap one in flight: they share the workspace and the host
+ * buffers).  dsa_decode_graph_destroy frees the handle (NULL is accepted);
+ * no launch of it may be in flight.
+ * Returns a status as dsa_decode; DSA_ERR_CUDA if the capture or the
+ * instantiation fails.
+ */
+typedef struct dsa_decode_graph_s *dsa_decode_graph;
+int dsa_decode_graph_create(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
+                            const void *k_idx, const float *k_scale, int64_t k_rows,
+                            const float *h_w, int H_I, int d_idx,
+                            int B, const int32_t *h_seq_lens, const int32_t *h_slot_base,
+                            int64_t max_seq_len, int k,
+                            const void *h_q, int H, int D, int Dv, float softmax_scale,
+                            const dsa_kv_pool *kv,
+                            const dsa_kv_pool *kv_swa, const int32_t *h_idx_swa, int k_swa,
+                            int32_t *h_idx_out, void *h_out, float *h_lse,
+                            void *ws, size_t ws_bytes, int32_t *err_flag,
+                            dsa_decode_graph *graph);
+int dsa_decode_graph_launch(dsa_decode_graph graph, dsa_stream_t stream);
+void dsa_decode_graph_destroy(dsa_decode_graph graph);
+
+/*
  * dsa_selftest_wait_timeout -- a diagnostic of the failure detection: one
  * GPU thread waits, through the same bounded wait every kernel here uses, on
  * a barrier phase that nothing completes.  The wait gives up after its

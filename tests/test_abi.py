@@ -166,3 +166,19 @@ def test_decode_host_rejects_bad_arguments(lib):
     assert call(h_q=None) == 1
     assert call(ws_bytes=need - 1) == 3
     assert call(k=ops.MAX_TOPK + 1) == 2
+
+
+def test_decode_graph_host_rejections(lib):
+    """No graph is made: a NULL out-handle or an empty batch is rejected before
+    any CUDA call; launching or destroying a NULL handle is harmless."""
+    pool = _pool(0, d_nope=512)
+    h = ctypes.c_void_p(1234)
+    def create(B=2, out=ctypes.byref(h)):
+        return lib.dsa_decode_graph_create(FAKE, 1, FAKE, FAKE, FAKE, 1000, FAKE, 64, 128, B, FAKE,
+                                           FAKE, 4096, 2048, FAKE, 64, 576, 512, 0.1,
+                                           ctypes.byref(pool), None, None, 0, None, FAKE, FAKE,
+                                           FAKE, 1 << 30, None, out)
+    assert create(out=None) == 1
+    assert create(B=0) == 1 and h.value is None
+    assert lib.dsa_decode_graph_launch(None, None) == 1
+    lib.dsa_decode_graph_destroy(None)

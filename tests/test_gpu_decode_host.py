@@ -109,3 +109,64 @@ def test_decode_host_rejects_device_tensors_and_small_workspace():
         _run_host(case, bad)
     with pytest.raises(ops.DsaError):
         _run_host(case, h, ws=ops.workspace(16, "cuda"))
+
+
+# ---------------------------------------------------------------- dsa_decode_graph
+
+def _graph(case, h, **kw):
+    ind = case.indexer
+    return ops.DecodeGraph(h["q_idx"], ind["idx_dtype"], h["q_scale"], ind["k_idx"],
+                           ind["k_scale"], h["w"], h["seq_lens"], h["slot_base"],
+                           case.max_seq_len, case.k, h["q"], case.softmax_scale, case.kv,
+                           kv_swa=case.kv_swa, idx_swa=h["idx_swa"], **kw)
+
+
+@pytest.mark.parametrize("name,make", [
+    ("fp8_ragged", lambda: I.decode_case("graph_fp8", 5, [1, 300, 2048, 2049, 10000], 64, 128,
+                                         "fp8", 2048, 64, I.KV_BF16, device="cuda")),
+    ("packed_two_loop", lambda: I.decode_case("graph_packed", 3, [5000, 20000, 70000], 64, 128,
+                                              "fp8", 1024, 64, I.KV_FP8_DS_MLA, device="cuda",
+                                              swa=128)),
+])
+def test_decode_graph_replays_equal_direct_calls(name, make):
+    """A captured step, launched twice: first on the case's inputs, then on
+    inputs rewritten in place in the same pinned buffers (other queries,
+    shorter contexts, the same caches).  Each launch equals dsa_decode on the
+    same inputs bit for bit."""
+    import dataclasses
+    case = make()
+    h = _host_inputs(case)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = _graph(case, h, err_flag=flag)
+    try:
+        for step in range(2):
+            if step == 1:
+                # step 2: new queries and weights, every context shortened
+                ind = dict(case.indexer)
+                gen = torch.Generator(device="cuda").manual_seed(7)
+                ind["w"] = (torch.randn(ind["w"].shape, generator=gen, device="cuda") / 8).contiguous()
+                q = I.to_bf16(torch.randn(case.q.shape, generator=gen, device="cuda")).contiguous()
+                seq = (case.seq_lens - torch.clamp(case.seq_lens // 3, max=500)).clamp(min=1)
+                case = dataclasses.replace(case, indexer=ind, q=q, seq_lens=seq.to(torch.int32).contiguous())
+                for key, src in (("w", ind["w"]), ("q", q), ("seq_lens", case.seq_lens)):
+                    h[key].copy_(src.cpu())
+            got = g.launch()
+            torch.cuda.synchronize()
+            ref = ops.decode_case(case)
+            torch.cuda.synchronize()
+            for x, y in zip(got, ref):
+                _same(x, y)
+        assert flag.item() == 0
+    finally:
+        g.close()
+
+
+def test_decode_graph_rejects_pageable_buffers_and_bad_shapes():
+    case = I.tiny_decode(device="cuda")
+    h = _host_inputs(case)
+    bad = dict(h)
+    bad["q"] = case.q.cpu()            # pageable: the graph's copies need pinned memory
+    with pytest.raises(ValueError):
+        _graph(case, bad)
+    with pytest.raises(ops.DsaError):
+        _graph(case, h, ws=ops.workspace(16, "cuda"))
