@@ -103,3 +103,28 @@ def test_named_configurations():
     assert s.indexer["idx_dtype"] == I.IDX_FP8
     # w ~ N(0, 1) / 8: 128 draws, standard deviation within a loose band
     assert 0.08 < float(s.indexer["w"].std()) < 0.17
+
+
+def test_packed_pool_scale_bytes_recipe():
+    """aiter PR #4382, Packed fp8_ds_mla: per page 256 x 576 data bytes, then
+    256 x 8 scale bytes, 7 UE8M0 exponents in [120, 134] and one pad byte."""
+    pool = I.kv_packed_pool(512, 256, seed=0, n=5, device="cpu")
+    assert pool.data.shape == (2, 256, 584) and pool.rows == 512
+    flat = pool.data.view(2, 256 * 584)
+    sc = flat[:, 256 * 576:].view(2, 256, 8)
+    assert (sc[:, :, 7] == 0).all()                              # the pad byte
+    e = sc[:, :, :7]
+    assert int(e.min()) >= 120 and int(e.max()) <= 134
+    assert len(torch.unique(e)) == 15                            # every exponent of the range drawn
+
+
+def test_uniform_pool_scales_recipe():
+    """Uniform fp8 pool decode: one fp32 scale per 64 columns (D = 512: 8 per
+    row), drawn log-uniform in [2^-4, 2^4]."""
+    pool = I.kv_uniform_fp8_pool(4096, seed=0, n=5, device="cpu")
+    assert pool.data.shape == (4096, 512) and pool.scales.shape == (4096, 8)
+    l2 = torch.log2(pool.scales)
+    assert float(l2.min()) >= -4 and float(l2.max()) <= 4
+    # log-uniform: the log2 scales fill the interval evenly (8 bins of width 1)
+    hist = torch.histc(l2, bins=8, min=-4, max=4)
+    assert float(hist.min()) > 0.8 * float(hist.mean())
