@@ -2,6 +2,7 @@
 declares; host-side argument checks reject bad calls before any launch.
 No GPU is needed: nothing here reaches a kernel."""
 import ctypes
+import os
 
 import pytest
 
@@ -182,3 +183,21 @@ def test_decode_graph_host_rejections(lib):
     assert create(B=0) == 1 and h.value is None
     assert lib.dsa_decode_graph_launch(None, None) == 1
     lib.dsa_decode_graph_destroy(None)
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/dsa.h is a C ABI: it compiles as strict C99 with only the C
+    standard headers (no CUDA or C++ types in the signatures)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not installed")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "dsa.h"\n'
+                   "int main(void) { dsa_decode_graph g = 0; (void)g; return dsa_abi_version() ? 0 : 1; }\n")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", inc,
+                        "-c", str(src), "-o", str(tmp_path / "use_header.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
