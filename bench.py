@@ -221,11 +221,18 @@ def run_ours(args, rank, world):
     stage_us = {s: 1000.0 * statistics.median(v) for s, v in stage_ms.items()}
 
     # algorithmic bytes (per launch) of the dominant kernel, the index score:
-    # per key 128 B fp8 + 4 B scale read, 4 B score written
+    # per key 128 B fp8 + 4 B scale; per request the query's 64 x 128 fp8
+    # head rows, their 64 scales and 64 weights (8704 B).  The score row the
+    # kernel writes (4 B a key, re-read from L2 by the top-k) is workspace
+    # traffic, not an input or output of the method: it is reported beside
+    # the figure, not in it.
     hbm_gbs, _, peak_kind = measured_peaks()
-    idx_bytes = Bsz * N * (128 + 4 + 4) + Bsz * 64 * (128 + 8)
+    q_idx_bytes = 64 * 128 + 64 * 4 + 64 * 4
+    idx_bytes = Bsz * N * (128 + 4) + Bsz * q_idx_bytes
+    score_bytes = Bsz * N * 4
     idx_gbs = idx_bytes / (stage_us["index_score"] * 1e-6) / 1e9
-    # whole-step algorithmic bytes: keys + scores + gathered KV rows + q/out/lse
+    # whole-step algorithmic bytes: keys and scales, the gathered KV rows,
+    # the indexer query, q, out and lse
     rows = Bsz * min(N, k)
     step_bytes = idx_bytes + rows * 1152 + Bsz * H * (576 * 2 + Dv * 2 + 4)
     step_gbs = step_bytes / (us_per_step * 1e-6) / 1e9
@@ -317,6 +324,7 @@ def run_ours(args, rank, world):
                      "peak": hbm_gbs, "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
                      "unit": "GB/s", "frac": round(idx_gbs / hbm_gbs, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": idx_bytes,
+                     "score_write_bytes_per_launch": score_bytes,
                      "launch_us": round(stage_us["index_score"], 2)},
         "step_roofline": {"achieved_gbs": round(step_gbs, 1), "frac": round(step_gbs / hbm_gbs, 4),
                           "algorithmic_bytes_per_step": step_bytes},
@@ -616,23 +624,55 @@ def run_workload(args):
 
 
 # ---------------------------------------------------------------- oracle (CPU)
+#
+# The oracle is plain numpy in float64, one request at a time.  It is timed
+# on the host's cores as a pool of worker processes (spawned, so no CUDA
+# state is inherited), each with one BLAS thread and its own request of the
+# workload; a barrier starts a round of requests on every worker at once, and
+# a round lasts as long as its slowest request.
 
-def oracle_sample(B, N, n_req, seed=1):
-    """Time the CPU oracle on n_req requests of a (B, N) decode; returns
-    (seconds per request, sample description)."""
-    import numpy as np
+_OW = {}
+
+
+def _oracle_init(N, barrier):
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        os.environ[v] = "1"
+    _OW["N"], _OW["barrier"] = N, barrier
+
+
+def _oracle_round(seed):
+    """One request of the decode workload through the oracle; returns its
+    seconds.  The worker builds its request once (context N, its own seed)."""
     import torch
+    torch.set_num_threads(1)
     import oracle.dsa_oracle as O
     from deepseek_sparse_attention_index_gb300 import inputs as I
     from tests.helpers import decode_case_np
-    case = I.decode_sweep(n_req, N, device="cpu", seed=seed)
-    c = decode_case_np(case)
+    if "case" not in _OW:
+        _OW["case"] = decode_case_np(I.decode_sweep(1, _OW["N"], device="cpu", seed=100 + seed))
+    _OW["barrier"].wait()
     t0 = time.perf_counter()
-    for b in range(n_req):
-        O.decode_request(b, c)
-    dt = (time.perf_counter() - t0) / n_req
-    return dt, "%d of the %d requests (context %d, full index sweep, sort and attention each)" % (
-        n_req, B, N)
+    O.decode_request(0, _OW["case"])
+    return time.perf_counter() - t0
+
+
+class OraclePool:
+    """`workers` processes timing the oracle on requests of context N."""
+
+    def __init__(self, N, workers):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.workers = workers
+        self.barrier = ctx.Barrier(workers)
+        self.pool = ctx.Pool(workers, initializer=_oracle_init, initargs=(N, self.barrier))
+
+    def round(self):
+        """Seconds of one round: `workers` requests at once, one per worker."""
+        return max(self.pool.map(_oracle_round, range(self.workers), chunksize=1))
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
 
 
 def cpu_cores():
@@ -642,32 +682,51 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def cpu_baseline(B, N, rounds=1):
+    """The oracle on the host cores for a (B, N) decode step: all cores (one
+    request per core at once, scaled to the batch) and one thread (one
+    request, scaled to the batch)."""
+    cores = cpu_cores()
+    pool = OraclePool(N, cores)
+    pool.round()                                   # builds each worker's request
+    t_all = statistics.mean(pool.round() for _ in range(rounds))
+    pool.close()
+    one = OraclePool(N, 1)
+    one.round()
+    t_one = statistics.mean(one.round() for _ in range(rounds))
+    one.close()
+    return {"value": round(t_all * B / cores * 1e6, 1), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": "%d requests of context %d at once, one per core (1 BLAS thread each), "
+                      "the round's time scaled x%d/%d to the batch of %d" % (cores, N, B, cores, B),
+            "one_thread": {"value": round(t_one * B * 1e6, 1), "unit": UNIT, "cores": 1,
+                           "sample": "1 request of context %d, scaled x%d" % (N, B)}}
+
+
 def run_reference(args):
+    """The reference arm: the CPU oracle on this host's cores, on the default
+    decode workload.  Each step is one round of requests on every core at once
+    (one request per core), scaled to the batch."""
     Bsz, N = args.batch, args.context
-    n_req = 2
-    per_req, sample = oracle_sample(Bsz, N, n_req)
-    # steps: each step times a bounded sample (one request) and scales to the batch
-    for _ in range(args.warmup):
-        pass
-    per = []
-    import oracle.dsa_oracle as O
-    from deepseek_sparse_attention_index_gb300 import inputs as I
-    from tests.helpers import decode_case_np
-    case = decode_case_np(I.decode_sweep(1, N, device="cpu", seed=2))
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        O.decode_request(0, case)
-        per.append(time.perf_counter() - t0)
-    us = statistics.mean(per) * Bsz * 1e6
+    cores = cpu_cores()
+    pool = OraclePool(N, cores)
+    for _ in range(args.warmup):                   # the first round builds the requests
+        pool.round()
+    per = [pool.round() for _ in range(args.steps)]
+    pool.close()
+    us = statistics.mean(per) * Bsz / cores * 1e6
+    sample = ("each step: %d requests of context %d at once, one per core (1 BLAS thread each), "
+              "the round's time scaled x%d/%d to the batch of %d (extrapolated from the sample)"
+              % (cores, N, Bsz, cores, Bsz))
     res = {
         "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1000, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(Bsz, N, 2048),
-        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cpu_cores(),
-                         "kind": "oracle",
-                         "sample": "each step: 1 of the %d requests (context %d), scaled x%d"
-                                   % (Bsz, N, Bsz)},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "extrapolated": {"timed_requests_per_step": cores, "batch": Bsz,
+                         "timed_s_per_step": round(statistics.mean(per), 3)},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -697,6 +756,11 @@ def main():
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.gpus != world:
+        # one process per GPU: N GPUs need N ranks (torchrun --nproc-per-node N)
+        sys.exit("bench.py: --gpus %d but WORLD_SIZE=%d; launch N > 1 GPUs with "
+                 "python -m torch.distributed.run --nproc-per-node N bench.py --gpus N"
+                 % (args.gpus, world))
 
     if args.impl == "reference":
         if rank == 0:
@@ -713,10 +777,7 @@ def main():
     res = run_ours(args, rank, world)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            per_req, sample = oracle_sample(args.batch, args.context, 2)
-            us = per_req * args.batch * 1e6
-            res["cpu_baseline"] = {"value": round(us, 1), "unit": UNIT, "cores": cpu_cores(),
-                                   "kind": "oracle", "sample": sample + ", scaled to the batch"}
+            res["cpu_baseline"] = cpu_baseline(args.batch, args.context)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

@@ -91,22 +91,23 @@ struct WsCarver {
   size_t bytes() const { return align_up(off, 256); }
 };
 
-// A finished softmax over rows, m the reference maximum and l the sum of
-// exp2(x - m) (exp2 units), with a sink logit (natural-log units, -inf: none)
-// joining the denominator: returns the factor that turns the rows' weighted
-// sum (in the frame of m) into the output, and sets *lse_nat to the natural
-// log of the whole denominator.  No row (l = 0): factor 0, lse = the sink.
-__device__ __forceinline__ float fold_sink(float m, float l, float sink_nat, float *lse_nat) {
-  const float s2 = sink_nat * 1.4426950408889634f;
+// A finished softmax over rows: m is the reference maximum in raw products
+// q . K (before the softmax scale), l the sum of exp(scale (x - m)) over the
+// rows.  A sink logit (natural-log units, -inf: none) joins the denominator.
+// Returns the factor that turns the rows' weighted sum (in the frame of m)
+// into the output, and sets *lse_nat to the natural log of the whole
+// denominator.  No row (l = 0): factor 0, lse = the sink.
+__device__ __forceinline__ float fold_sink(float m, float scale, float l, float sink_nat,
+                                           float *lse_nat) {
   if (!(l > 0.f)) {
     *lse_nat = sink_nat;
     return 0.f;
   }
-  const float r2 = m + log2f(l);               // log2 of the rows' part
-  const float hi = fmaxf(r2, s2), lo = fminf(r2, s2);
-  const float t2 = hi + log2f(1.f + exp2f(lo - hi));
-  *lse_nat = t2 * 0.6931471805599453f;
-  return exp2f(m - t2);
+  const float r = fmaf(m, scale, logf(l));     // ln of the rows' part
+  const float hi = fmaxf(r, sink_nat), lo = fminf(r, sink_nat);
+  const float t = hi + log1pf(expf(lo - hi));  // no sink: lo = -inf, t = r
+  *lse_nat = t;
+  return expf(r - t) / l;
 }
 
 // The lse as reported: natural log, or log2 units on request.

@@ -66,10 +66,14 @@ int check_indexer(const void *q_idx, int idx_dtype, const float *q_scale, const 
   return DSA_OK;
 }
 
-int check_mla_shape(const void *q, int T, int H, int D, int Dv, const dsa_kv_pool *kv,
-                    const int32_t *idx, int k, const dsa_kv_pool *kv2, const int32_t *idx2,
-                    int k2, const void *out, const float *lse, bool need_idx = true) {
+int check_mla_shape(const void *q, int T, int H, int D, int Dv, float softmax_scale,
+                    const dsa_kv_pool *kv, const int32_t *idx, int k, const dsa_kv_pool *kv2,
+                    const int32_t *idx2, int k2, const void *out, const float *lse,
+                    bool need_idx = true) {
   if (T < 0 || k < 0 || k2 < 0) return DSA_ERR_INVALID_ARG;
+  // the softmax keeps its running maximum of the raw products q . K, which
+  // is the maximum of the scores only for a positive scale
+  if (!(softmax_scale > 0.f) || !(softmax_scale <= 3.4e38f)) return DSA_ERR_INVALID_ARG;
   if (H < 1 || H > DSA_MAX_HEADS) return DSA_ERR_UNSUPPORTED;
   if (!((D == 576 && Dv == 512) || (D == 512 && Dv == 448))) return DSA_ERR_UNSUPPORTED;
   if (k + k2 < 1) return DSA_ERR_INVALID_ARG;
@@ -299,7 +303,7 @@ int dsa_sparse_mla_fwd_ex(const void *q, int T, int H, int D, int Dv, float soft
                           void *out, float *lse, void *ws, size_t ws_bytes, int32_t *err_flag,
                           const dsa_attn_opts *opts, dsa_stream_t stream) {
   if (opts && opts->reserved != 0) return DSA_ERR_INVALID_ARG;
-  int st = check_mla_shape(q, T, H, D, Dv, kv, idx, k, kv_extra, idx_extra, k2, out, lse);
+  int st = check_mla_shape(q, T, H, D, Dv, softmax_scale, kv, idx, k, kv_extra, idx_extra, k2, out, lse);
   if (st != DSA_OK) return st;
   if (T == 0) return DSA_OK;
   const size_t need = dsa_sparse_mla_workspace_size(T, H, Dv, k, k2);
@@ -324,6 +328,7 @@ int dsa_sparse_mla_bwd(const void *q, int T, int H, int D, int Dv, float softmax
   if (T < 0 || k < 1) return DSA_ERR_INVALID_ARG;
   if (H < 1 || H > DSA_MAX_HEADS) return DSA_ERR_UNSUPPORTED;
   if (D != 576 || Dv != 512 || !kv || kv->format != DSA_KV_BF16) return DSA_ERR_UNSUPPORTED;
+  if (!(softmax_scale > 0.f) || !(softmax_scale <= 3.4e38f)) return DSA_ERR_INVALID_ARG;
   int st = check_kv(kv, D);
   if (st != DSA_OK) return st;
   if (T == 0) return DSA_OK;
@@ -369,7 +374,7 @@ int dsa_decode_ex(const void *q_idx, int idx_dtype, const float *q_scale, const 
   int st = check_indexer(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, B, H_I, d_idx);
   if (st != DSA_OK) return st;
   // idx_out is optional: the selection then lives in the workspace
-  st = check_mla_shape(q, B, H, D, Dv, kv, idx_out, k, kv_swa, idx_swa, k_swa, out, lse,
+  st = check_mla_shape(q, B, H, D, Dv, softmax_scale, kv, idx_out, k, kv_swa, idx_swa, k_swa, out, lse,
                        /*need_idx=*/false);
   if (st != DSA_OK) return st;
   if (B == 0) return DSA_OK;
@@ -397,7 +402,7 @@ int dsa_decode_paged(const void *q_idx, int idx_dtype, const float *q_scale, con
   if ((int64_t)max_pages * page_size < max_seq_len) return DSA_ERR_INVALID_ARG;
   int st = check_indexer(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, B, H_I, d_idx);
   if (st != DSA_OK) return st;
-  st = check_mla_shape(q, B, H, D, Dv, kv, idx_out, k, kv_swa, idx_swa, k_swa, out, lse,
+  st = check_mla_shape(q, B, H, D, Dv, softmax_scale, kv, idx_out, k, kv_swa, idx_swa, k_swa, out, lse,
                        /*need_idx=*/false);
   if (st != DSA_OK) return st;
   if (B == 0) return DSA_OK;
@@ -445,7 +450,7 @@ int dsa_decode_host(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
   int st = check_indexer(S.q_idx, idx_dtype, h_q_scale ? S.q_scale : nullptr, k_idx, k_scale,
                          k_rows, S.w, B, H_I, d_idx);
   if (st != DSA_OK) return st;
-  st = check_mla_shape(S.q, B, H, D, Dv, kv, S.idx_out, k, kv_swa, k_swa > 0 ? S.idx_swa : nullptr,
+  st = check_mla_shape(S.q, B, H, D, Dv, softmax_scale, kv, S.idx_out, k, kv_swa, k_swa > 0 ? S.idx_swa : nullptr,
                        k_swa, S.out, S.lse, /*need_idx=*/false);
   if (st != DSA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -23,7 +23,6 @@ constexpr int kHeadsPerCta = 64;
 constexpr int kKStride = 580;   // float row stride of the gathered tile (bank spread)
 constexpr int kQStride = 584;   // bf16 row stride of q in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 // Fetch list entry j (of the concatenated list) for token t: slot and pool.
 struct ListRef {
@@ -115,6 +114,8 @@ sparse_mla_simt_kernel(MlaArgs a) {
   float o[NACC];
 #pragma unroll
   for (int i = 0; i < NACC; ++i) o[i] = 0.f;
+  // m: running maximum of the raw products q . K (the scores before the
+  // softmax scale); p = exp2((x - m) sc), lse = softmax_scale m + ln l
   float m = -INFINITY, l = 0.f;
   const float sc = a.softmax_scale * kLog2e;
   __syncthreads();
@@ -146,16 +147,18 @@ sparse_mla_simt_kernel(MlaArgs a) {
       if (s_valid[r]) {
         const float *kr = k_s + r * kKStride;
         const __nv_bfloat162 *qh = reinterpret_cast<const __nv_bfloat162 *>(q_s + hl * kQStride);
+        // four partial sums (columns c mod 4), added pairwise at the end
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
         for (int c = 0; c < D; c += 4) {
           const float4 kv = *reinterpret_cast<const float4 *>(kr + c);
           const float2 qa = __bfloat1622float2(qh[c / 2]);
           const float2 qb = __bfloat1622float2(qh[c / 2 + 1]);
-          x = fmaf(qa.x, kv.x, x);
-          x = fmaf(qa.y, kv.y, x);
-          x = fmaf(qb.x, kv.z, x);
-          x = fmaf(qb.y, kv.w, x);
+          x0 = fmaf(qa.x, kv.x, x0);
+          x1 = fmaf(qa.y, kv.y, x1);
+          x2 = fmaf(qb.x, kv.z, x2);
+          x3 = fmaf(qb.y, kv.w, x3);
         }
-        x *= sc;
+        x = (x0 + x1) + (x2 + x3);
       } else {
         x = -INFINITY;
       }
@@ -170,9 +173,9 @@ sparse_mla_simt_kernel(MlaArgs a) {
     if (mn == -INFINITY) {
       alpha = 1.f; p0 = 0.f; p1 = 0.f;
     } else {
-      alpha = exp2f(m - mn);
-      p0 = exp2f(s2[0] - mn);
-      p1 = exp2f(s2[1] - mn);
+      alpha = exp2f((m - mn) * sc);
+      p0 = exp2f((s2[0] - mn) * sc);
+      p1 = exp2f((s2[1] - mn) * sc);
     }
     float ps = p0 + p1;
     ps += __shfl_xor_sync(0xffffffffu, ps, 1);
@@ -208,8 +211,8 @@ sparse_mla_simt_kernel(MlaArgs a) {
   if (hl >= nh) return;
   const int h = h0 + hl;
   float inv = l > 0.f ? 1.f / l : 0.f;
-  float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-  if (a.n_splits == 1 && a.sinks) inv = fold_sink(m, l, a.sinks[h], &lse_v);
+  float lse_v = l > 0.f ? fmaf(m, a.softmax_scale, logf(l)) : -INFINITY;
+  if (a.n_splits == 1 && a.sinks) inv = fold_sink(m, a.softmax_scale, l, a.sinks[h], &lse_v);
   if (a.n_splits == 1) {
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + ((size_t)t * a.H + h) * a.Dv;
 #pragma unroll

@@ -103,7 +103,6 @@ template <int FMT> struct FmtTraits {
   static constexpr int kQBytes = kKBlocks * 64 * 128;           // Q padded to 64 heads
 };
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.0f;      // log2 of the largest tolerated p
 constexpr int kPrefetchTiles = 4;  // rows are pulled into L2 this many tiles ahead
 
@@ -611,8 +610,13 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     const int half = lane >> 4;
     const bool head_lane = half == 0;       // the lane that writes per-head results
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    // The scores stay in the frame of the raw products S = q . K: the
+    // reference maximum m is a raw product, p = exp2((S - m) c) with c =
+    // softmax_scale log2(e), and the lse is softmax_scale m + ln l.  Rounding
+    // S c or m c first would cost the lse several ulps of its magnitude (an
+    // fp8 pool with UE8M0 exponents up to 2^7 gives scores near 300).
     const float c = a.softmax_scale * kLog2e;
-    float m = -INFINITY;                    // reference maximum (exp2 units)
+    float m = -INFINITY;                    // reference maximum (raw products)
     float l = 0.f;                          // running sum of p
     bool ok = true;
     if (FMT != kFmtBf16) {
@@ -655,14 +659,16 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       float tmax = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        x[j] = ((vm >> j) & 1u) ? x[j] * c : -INFINITY;
+        x[j] = ((vm >> j) & 1u) ? x[j] : -INFINITY;
         tmax = fmaxf(tmax, x[j]);
       }
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));   // the head's maximum
       float al = 1.f;
       int need = 0;
-      if (tmax > m + kLazy) {               // both lanes of the pair decide alike
-        al = (m == -INFINITY) ? 0.f : exp2f(m - tmax);
+      // both lanes of the pair decide alike; nothing valid yet on either
+      // side: (-inf) - (-inf) is NaN and the test fails
+      if ((tmax - m) * c > kLazy) {
+        al = (m == -INFINITY) ? 0.f : exp2f((m - tmax) * c);
         m = tmax;
         need = 1;
       }
@@ -683,8 +689,8 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       uint32_t phi[16], plo[4];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const float p0 = exp2f(x[j] - msafe);      // -inf -> 0
-        const float p1 = exp2f(x[j + 1] - msafe);
+        const float p0 = exp2f((x[j] - msafe) * c);      // -inf -> 0
+        const float p1 = exp2f((x[j + 1] - msafe) * c);
         ps += p0 + p1;
         if (FMT == kFmtBf16) {
           const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
@@ -735,8 +741,9 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     // with the head's sink folded in, if any; split pieces: the combine folds it)
     if (head_lane) {
       float inv = (l > 0.f) ? 1.f / l : 0.f;
-      float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      if (a.n_splits == 1 && a.sinks && hl < nh) inv = fold_sink(m, l, a.sinks[h0 + hl], &lse);
+      float lse = l > 0.f ? fmaf(m, a.softmax_scale, logf(l)) : -INFINITY;
+      if (a.n_splits == 1 && a.sinks && hl < nh)
+        inv = fold_sink(m, a.softmax_scale, l, a.sinks[h0 + hl], &lse);
       inv_l[hl] = inv;
       if (hl < nh) {
         if (a.n_splits == 1)

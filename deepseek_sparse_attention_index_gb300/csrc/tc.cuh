@@ -112,19 +112,6 @@ DSA_DEVINLINE void tma_load_3d(const CUtensorMap *map, uint64_t *bar, void *dst,
       : "memory");
 }
 
-// Row gather: rows y0..y3 (each in [0, rows) of the map), columns [x, x +
-// box width), into four consecutive box-sized rows at dst.  The map's box
-// must be one row high.
-DSA_DEVINLINE void tma_gather4(const CUtensorMap *map, uint64_t *bar, void *dst, int x, int y0,
-                               int y1, int y2, int y3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1),
-      "r"(y2), "r"(y3)
-      : "memory");
-}
-
 // L2 policy for data read once (streamed): evict it first, so that lines
 // written nearby (e.g. a score row read back by the next kernel) stay.
 DSA_DEVINLINE uint64_t l2_policy_evict_first() {

@@ -344,6 +344,12 @@ def packed_segment_lengths(total=16384, hi=8192, n_single=2, seed=0):
     return lens
 
 
+def prefill_q(T: int, H: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Attention queries of a prefill: bf16 N(0,1) [T, H, 576] (tensor number 4)."""
+    gq = _gen(seed, 4, device)
+    return to_bf16(torch.randn((T, H, 576), generator=gq, device=device)).contiguous()
+
+
 def prefill_case(seg_lens, H_I=64, d_idx=128, idx_kind="fp8", k=2048, H=64, seed=0,
                  device="cpu", name=None) -> PrefillCase:
     """Tensor numbers: 1-3 indexer, 4 q, 5 KV."""
@@ -360,8 +366,7 @@ def prefill_case(seg_lens, H_I=64, d_idx=128, idx_kind="fp8", k=2048, H=64, seed
     else:
         ind = indexer_grid_bf16(T, T, H_I, d_idx, seed, device)
     kv = kv_bf16_pool(T, seed, 5, device)
-    gq = _gen(seed, 4, device)
-    q = to_bf16(torch.randn((T, H, 576), generator=gq, device=device)).contiguous()
+    q = prefill_q(T, H, seed, device)
     return PrefillCase(name or ("prefill_T%d" % T), T, list(seg_lens),
                        torch.tensor(starts, dtype=torch.int32, device=device),
                        torch.tensor(ends, dtype=torch.int32, device=device),

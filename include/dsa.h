@@ -193,8 +193,11 @@ int dsa_topk(const float *scores, int64_t ld_scores, const int32_t *row_len, int
  * max_len, k) <= 4 MiB (about 80 KiB a row: up to 50 rows of 128K scores);
  * larger calls return DSA_ERR_UNSUPPORTED without launching anything.
  * The first call on a device looks up the array's device address (with that
- * device current), so make that first call before any stream capture.  All
- * calls share the array and it keeps the last call's contents; each call
+ * device current), so make that first call before any stream capture.  The
+ * address is kept for the life of the process: after cudaDeviceReset the
+ * module may be loaded again elsewhere, so do not call this function on a
+ * device that was reset.
+ * All calls share the array and it keeps the last call's contents; each call
  * clears what must start at zero.  Calls whose work overlaps on the GPU race
  * on the array: serialise them.  The function allocates nothing.
  */
@@ -219,7 +222,9 @@ int dsa_topk_noalloc(const float *scores, int64_t ld_scores, const int32_t *row_
  *            (both NULL with k2 = 0); kv_extra must have kv's D
  *   out      bf16 [T, H, Dv];  lse fp32 [T, H]
  * Limits: D = 576 with Dv = 512 (bf16 pool) or D = 512 with Dv = 448 (fp8
- * pools); 1 <= H <= 128; k + k2 >= 1.
+ * pools); 1 <= H <= 128; k + k2 >= 1; q and out 16-byte aligned;
+ * softmax_scale positive and finite.  Anything else returns
+ * DSA_ERR_INVALID_ARG or DSA_ERR_UNSUPPORTED before any launch.
  * Workspace: dsa_sparse_mla_workspace_size(T, H, Dv, k, k2) bytes.
  */
 size_t dsa_sparse_mla_workspace_size(int T, int H, int Dv, int k, int k2);

@@ -71,8 +71,8 @@ def _pool(fmt, rows=16, block=1, d_nope=512, scales=True):
     return p
 
 
-def _mla(lib, pool, D=576, Dv=512, H=8, k=4, idx=FAKE, ws_bytes=1 << 30):
-    return lib.dsa_sparse_mla_fwd(FAKE, 2, H, D, Dv, 0.1, ctypes.byref(pool), idx, k, None, None,
+def _mla(lib, pool, D=576, Dv=512, H=8, k=4, idx=FAKE, ws_bytes=1 << 30, scale=0.1, q=FAKE):
+    return lib.dsa_sparse_mla_fwd(q, 2, H, D, Dv, scale, ctypes.byref(pool), idx, k, None, None,
                                   0, FAKE, FAKE, FAKE, ws_bytes, None, None)
 
 
@@ -91,6 +91,11 @@ def test_sparse_mla_rejects_bad_arguments(lib):
     need = lib.dsa_sparse_mla_workspace_size(2, 8, 512, 4, 0)
     if need:
         assert _mla(lib, _pool(0, d_nope=512), ws_bytes=need - 1) == 3
+    # the softmax scale must be positive and finite
+    for bad in (0.0, -0.1, float("nan"), float("inf")):
+        assert _mla(lib, _pool(0, d_nope=512), scale=bad) == 1, bad
+    # q must start on a 16-byte boundary
+    assert _mla(lib, _pool(0, d_nope=512), q=ctypes.c_void_p(FAKE.value + 2)) == 1
 
 
 @pytest.mark.parametrize("entry", ["dsa_index_score", "dsa_index_score_prefill"])

@@ -13,7 +13,7 @@ from deepseek_sparse_attention_index_gb300 import build as B
 from deepseek_sparse_attention_index_gb300 import inputs as I
 from deepseek_sparse_attention_index_gb300 import ops
 from tests.helpers import raw, pool_np, decode_case_np, prefill_case_np
-from tests.parity import check_index_sets, check_out_lse
+from tests.parity import check_index_sets, check_out_lse, lse_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -226,7 +226,8 @@ def test_sparse_mla_matches_oracle(fmt, H, k):
     assert flag.item() == 0
     ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(pool), raw(idx), scale,
                                     out.shape[2])
-    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "mla")
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "mla",
+                  lse_tol=lse_tol(fmt))
     assert (out[1] == 0).all() and torch.isneginf(lse[1]).all()   # all-padded token
 
 
@@ -251,7 +252,8 @@ def test_sparse_mla_sinks(fmt, H, k, T):
     out, lse = ops.dsa_sparse_mla_fwd(q, scale, pool, idx, sinks=sinks)
     ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(pool), raw(idx), scale,
                                     out.shape[2], sinks=sinks.double().cpu().numpy())
-    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "mla+sinks")
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "mla+sinks",
+                  lse_tol=lse_tol(fmt))
     # the all-padded token: no value, the denominator is the sink alone
     assert (out[1] == 0).all()
     assert torch.equal(lse[1].cpu(), sinks.cpu())
@@ -350,7 +352,40 @@ def test_sparse_mla_two_loop_packed():
     out, lse = ops.dsa_sparse_mla_fwd(q, scale, main, idx_main, extra, idx_extra)
     ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(main), raw(idx_main), scale, 448,
                                     pool_np(extra), raw(idx_extra))
-    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "2-loop")
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "2-loop",
+                  lse_tol=lse_tol(I.KV_FP8_DS_MLA))
+
+
+@pytest.mark.parametrize("main_fmt,extra_fmt", [(I.KV_FP8_UNIFORM, I.KV_FP8_DS_MLA),
+                                               (I.KV_FP8_DS_MLA, I.KV_FP8_UNIFORM)])
+def test_sparse_mla_two_loop_mixed_formats(main_fmt, extra_fmt):
+    """Main and extra lists in pools of different fp8 formats (one softmax
+    over both): the SIMT kernel serves these calls (the only ones the
+    tensor-core kernel does not take: q must be 16-byte aligned anyway)."""
+    T, H = 3, 64
+    g = torch.Generator().manual_seed(21)
+
+    def pool(fmt, rows, n):
+        if fmt == I.KV_FP8_UNIFORM:
+            return I.kv_uniform_fp8_pool(rows, 2, n, "cuda")
+        return I.kv_packed_pool(rows, 256, 2, n, "cuda")
+
+    main, extra = pool(main_fmt, 512, 5), pool(extra_fmt, 4096, 6)
+    idx_main = torch.stack([torch.randperm(512, generator=g)[:128] for _ in range(T)]).to(torch.int32)
+    idx_extra = torch.stack([torch.randperm(4096, generator=g)[:1024] for _ in range(T)]).to(torch.int32)
+    idx_extra[:, ::7] = -1
+    idx_main[1] = -1
+    q = I.to_bf16(torch.randn(T, H, 512, generator=g)).cuda()
+    scale = 1 / math.sqrt(512.0)
+    flag = _flag()
+    out, lse = ops.dsa_sparse_mla_fwd(q, scale, main, idx_main.cuda(), extra, idx_extra.cuda(),
+                                      err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(main), raw(idx_main), scale, 448,
+                                    pool_np(extra), raw(idx_extra))
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "mixed 2-loop",
+                  lse_tol=lse_tol(main_fmt, extra_fmt))
 
 
 def test_sparse_mla_masks_and_flags_out_of_range_entries():
@@ -405,7 +440,9 @@ def _check_decode(case, idx_gpu, out_gpu, lse_gpu, requests, bit_exact=False):
                     rows = np.concatenate([O.gather_valid(c["kv_swa"], c["idx_swa"][b]), rows])
                 ref_out, ref_lse = O.sparse_mla_one(O.decode_bf16(c["q"][b]), rows,
                                                     c["softmax_scale"], c["Dv"])
-        check_out_lse(out_gpu[b], lse_gpu[b], ref_out, ref_lse, "request %d" % b)
+        fmts = [case.kv.format] + ([] if case.kv_swa is None else [case.kv_swa.format])
+        check_out_lse(out_gpu[b], lse_gpu[b], ref_out, ref_lse, "request %d" % b,
+                      lse_tol=lse_tol(*fmts))
 
 
 def test_decode_tiny_bit_exact_indices():
@@ -508,11 +545,16 @@ def test_decode_sweep_full_size_sampled():
     _check_decode(case, idx, out, lse, [0, 17, 31])
 
 
-@pytest.mark.parametrize("N", [512, 2048, 8192])
-def test_decode_sweep_short_contexts(N):
-    case = I.decode_sweep(32 if N < 8192 else 8, N, device="cuda")
-    idx, out, lse = ops.decode_case(case)
-    _check_decode(case, idx, out, lse, [0, case.B - 1])
+@pytest.mark.parametrize("B,N", [(1, 512), (1, 2048), (1, 8192), (1, 32768), (1, 131072),
+                                 (32, 512), (32, 2048), (32, 8192), (32, 32768)])
+def test_decode_sweep_points(B, N):
+    """The decode sweep's other points: batch 1 and 32 at 512 .. 128k."""
+    case = I.decode_sweep(B, N, device="cuda")
+    flag = _flag()
+    idx, out, lse = ops.decode_case(case, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    _check_decode(case, idx, out, lse, sorted({0, B // 2, B - 1}))
 
 
 def test_packed_long_context_two_loop_full_size():
