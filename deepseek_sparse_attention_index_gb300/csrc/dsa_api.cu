@@ -333,7 +333,7 @@ int dsa_sparse_mla_bwd(const void *q, int T, int H, int D, int Dv, float softmax
   if (st != DSA_OK) return st;
   if (T == 0) return DSA_OK;
   if (!q || !idx || !lse || !dout || !dq || !dkv) return DSA_ERR_INVALID_ARG;
-  if (!aligned16(kv->data)) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(kv->data) || !aligned16(q) || !aligned16(dout)) return DSA_ERR_INVALID_ARG;
   MlaBwdArgs a{};
   a.q = q; a.T = T; a.H = H; a.softmax_scale = softmax_scale;
   a.kv = to_dev(kv); a.idx = idx; a.k = k;

@@ -11,13 +11,15 @@
 //     needs one term.  With an fp32 scale (uniform pool) K also keeps its
 //     fp16 residual plane, S = Q K_hi^T + Q K_lo^T, because the scores are
 //     large enough (|s| ~ 20) that 2^-11 in K would move the lse by ~1e-3;
-//     that second plane fits only one stage.  A value beyond fp16's range (|x| > 65504) raises
+//     with that second plane a tile holds 32 rows, so that two stages still
+//     fit beside Q.  A value beyond fp16's range (|x| > 65504) raises
 //     DSA_DEVERR_FP16_RANGE.
 // (The "sparse attn" stage of tokenspeed PR #627 "Add gluon kernel for DSA";
 // semantics of miles PR #3608: natural-log lse, -1 entries masked.)
 //
 // One CTA handles one (token, piece of its index list, group of <= 64 heads)
-// and walks the piece in tiles of 64 gathered rows.  Per tile:
+// and walks the piece in tiles of 64 gathered rows (32 for the uniform pool).
+// Per tile:
 //   S[h, kv] = Q[h, :] . K_tile[kv, :]          tcgen05 M = 64 (heads, Q
 //                                                zero-padded to 64 rows),
 //                                                N = 64 (kv), K = 576;
@@ -74,8 +76,7 @@ namespace {
 // Warps 0-3 math, 4 and 10 S issue, 5 and 11 PV issue, 6-9 gather: 12
 // warps, so at most 168 registers a thread (three warps share an SM
 // sub-partition).
-constexpr int kTileRows = 64;
-constexpr int kKBlockBytes = kTileRows * 128;               // 8 KB: 64 rows x 64 16-bit values
+constexpr int kQKBlock = 64 * 128;       // one K-block of Q: 64 head rows x 64 16-bit values
 
 enum { kFmtBf16 = 0, kFmtUniform = 1, kFmtPacked = 2 };
 // Per pool format: K-blocks of 64 columns per row, stored V width, PV
@@ -83,16 +84,21 @@ enum { kFmtBf16 = 0, kFmtUniform = 1, kFmtPacked = 2 };
 // otherwise), and the operand type code of the instruction descriptor
 // (1 = bf16, 0 = fp16).
 template <int FMT> struct FmtTraits {
+  // gathered rows per tile: 64, or 32 for the uniform pool, whose two fp16
+  // planes per row would otherwise leave room for one stage only
+  static constexpr int kRows = FMT == kFmtUniform ? 32 : 64;
+  static constexpr int kKBlockBytes = kRows * 128;   // one K-block of a tile: kRows x 64 values
   static constexpr int kKBlocks = FMT == kFmtBf16 ? 9 : 8;
   static constexpr int kDv = FMT == kFmtBf16 ? 512 : 448;
-  static constexpr int kPvSteps = FMT == kFmtBf16 ? 8 : 4;
+  static constexpr int kPvSteps = FMT == kFmtBf16 ? 8 : kRows / 16;
   static constexpr uint32_t kOpType = FMT == kFmtBf16 ? 1u : 0u;
   // uniform pool: K = K_hi + K_lo (two fp16 planes) for the S product, so an
-  // e4m3 value times an arbitrary fp32 scale keeps ~22 significant bits;
-  // the second plane leaves room for one stage only
+  // e4m3 value times an arbitrary fp32 scale keeps ~22 significant bits
   static constexpr int kLoBlocks = FMT == kFmtUniform ? kKBlocks : 0;
-  static constexpr int kStages = FMT == kFmtUniform ? 1 : 2;
-  static constexpr int kStageBytes = (kKBlocks + kLoBlocks) * kKBlockBytes;   // 72, 64 or 128 KB
+  static constexpr int kStages = 2;
+  static constexpr int kStageBytes = (kKBlocks + kLoBlocks) * kKBlockBytes;   // 72, 64 or 64 KB
+  // rows are pulled into L2 this many tiles ahead (256 rows)
+  static constexpr int kPrefetchTiles = 256 / kRows;
   // gather warps: four, 16 rows each per tile (bf16: cp.async issue split
   // four ways; fp8: every 16-byte load of a tile in flight at once)
   static constexpr int kGatherWarps = 4;
@@ -104,7 +110,6 @@ template <int FMT> struct FmtTraits {
 };
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;      // log2 of the largest tolerated p
-constexpr int kPrefetchTiles = 4;  // rows are pulled into L2 this many tiles ahead
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -314,7 +319,11 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
   const int total = a.k + a.k2;
   const int j0 = min(total, split * per);   // per: a multiple of the tile
   const int je = min(total, j0 + per);
-  const int nt = (je - j0 + kTileRows - 1) / kTileRows;
+  constexpr int R = F::kRows;          // rows of a tile
+  constexpr int RH = R / 2;            // scores of a head a math lane holds
+  constexpr int kKBlockBytes = F::kKBlockBytes;
+  constexpr int kPrefetchTiles = F::kPrefetchTiles;
+  int nt = (je - j0 + R - 1) / R;       // tiles of the piece (trimmed below, one piece a token)
   // TMEM: S_a[2] at columns [0, 128), S_b[2] at [128, 256), O^T blocks at
   // [256, 256 + 4N)
   constexpr uint32_t kSCol = 0, kSbCol = 128, kOCol = 256;
@@ -358,19 +367,41 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     tc::prefetch_tmap(&qmap);
     tc::mbar_arrive_expect_tx(qfull, F::kQBytes);
     for (int kb = 0; kb < kKBlocks; ++kb)
-      tc::tma_load_3d(&qmap, qfull, q_s + kb * kKBlockBytes, kb * 64, h0, t);
+      tc::tma_load_3d(&qmap, qfull, q_s + kb * kQKBlock, kb * 64, h0, t);
   };
   if (warp == 5 && lane == 0 && a.q_ready) load_q();
   pdl_wait();      // the index lists come from the previous kernel
   pdl_trigger();
   if (warp == 5 && lane == 0 && !a.q_ready) load_q();
+  if (a.n_splits == 1) {
+    // one piece a token (prefill): the tiles up to the list's last entry
+    // other than -1 -- a causal prefill's early tokens end in a long -1 tail,
+    // whose tiles would gather nothing.  (Split decode pieces skip this scan:
+    // their lists are full, and the scan's load latency would precede every
+    // piece.)
+    int *last_s = reinterpret_cast<int *>(bars + 26);
+    int last = -1;
+    for (int e = j0 + threadIdx.x; e < je; e += blockDim.x) {
+      const int32_t v = e < a.k ? __ldg(a.idx + (size_t)t * a.k + e)
+                                : __ldg(a.idx2 + (size_t)t * a.k2 + (e - a.k));
+      if (v != -1) last = e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    if (threadIdx.x == 0) *last_s = -1;
+    __syncthreads();
+    if (lane == 0 && last >= 0) atomicMax(last_s, last);
+    __syncthreads();
+    nt = (*last_s + 1 - j0 + R - 1) / R;
+    if (nt < 0) nt = 0;
+  }
 
   if (warp >= 6 && warp < 10 && FMT == kFmtBf16) {
     // -------------------------------------------------------------- gather (bf16)
     const int gw = warp - 6;            // rows [16*gw, 16*gw + 16) of every tile
     // this lane's row of tile i (row 16*gw + lane, lanes < 16), or nullptr
     auto row_of = [&](int i) -> const uint8_t * {
-      const int e = j0 + i * kTileRows + 16 * gw + lane;
+      const int e = j0 + i * R + 16 * gw + lane;
       if (lane >= 16 || e >= je) return nullptr;
       const int64_t slot = entry_slot(a, t, e, false);
       if (slot < 0) return nullptr;
@@ -427,15 +458,15 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     // to fp16 and stores them swizzled: chunk cc of a row covers columns
     // [16 cc, 16 cc + 16) (K-block cc / 4, 16-byte slots 2 (cc % 4) and +1),
     // a RoPE chunk the 8 columns 448 + 8 (cc - 28) (K-block 7, slot cc - 28).
-    // Lanes 0..63 publish the tile's row addresses in shared memory first.
+    // Lanes 0..R-1 publish the tile's row addresses in shared memory first.
     constexpr int CPR = FMT == kFmtUniform ? 32 : 36;
-    constexpr int CPL = 64 * CPR / 128;            // chunks per lane per tile
+    constexpr int CPL = R * CPR / 128;             // chunks per lane per tile
     const int gl = threadIdx.x - 192;              // 0..127
     Fp8Row *rtab = reinterpret_cast<Fp8Row *>(smem + L.rows);
     auto row_of = [&](int i) -> Fp8Row {
       Fp8Row r{nullptr, nullptr};
-      const int e = j0 + i * kTileRows + gl;
-      if (gl < 64 && e < je) {
+      const int e = j0 + i * R + gl;
+      if (gl < R && e < je) {
         const int64_t slot = entry_slot(a, t, e, false);
         if (slot >= 0) r = fp8_row<FMT>(e < a.k ? a.kv : a.kv2, slot);
       }
@@ -455,19 +486,27 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     };
     for (int i = 1; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);   // tile 0 is loaded at once
     bool bad = false;
+    // Software pipeline (uniform pool, 8 chunks a lane): tile i+1's loads
+    // are issued (into a second register set) as soon as tile i's stage is
+    // free, before tile i is dequantised, so one tile's global-load latency
+    // overlaps the previous tile's conversion.  The packed pool's 18 chunks
+    // a lane leave no room for a second set: its next loads follow the
+    // conversion.  The row table is double-buffered by tile parity: a lane
+    // reads tile i's half only in issue(i), which every lane has left before
+    // any lane passes the barrier of issue(i+1).
+    constexpr bool kPipe = FMT == kFmtUniform;
+    uint4 v[CPL];
+    uint32_t sc[CPL];                     // fp32 scale bits (uniform) or UE8M0 byte (packed)
+    uint32_t has = 0;
     Fp8Row next = nt > 0 ? row_of(0) : Fp8Row{nullptr, nullptr};
-    for (int i = 0; i < nt; ++i) {
-      const int st = i % NS;
-      if (!tc::mbar_wait(&kempty[st], ((i / NS) & 1) ^ 1, abort_flag)) break;
-      Fp8Row *rt = rtab + (i & 1) * 64;   // by tile parity: a lane still on tile i-1 reads the other half
-      if (gl < 64) rt[gl] = next;
+    auto issue = [&](int i) {             // publish tile i's rows, then load its chunks
+      Fp8Row *rt = rtab + (i & 1) * 64;
+      if (gl < R) rt[gl] = next;
+      if (i + 1 < nt) next = row_of(i + 1);   // the next index loads overlap these
       tc::named_bar_sync(2, 128);
-      unsigned char *stage = k_s + st * kStageBytes;
-      uint4 v[CPL];
-      uint32_t sc[CPL];                   // fp32 scale bits (uniform) or UE8M0 byte (packed)
-      uint32_t has = 0;
+      has = 0;
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) {     // every load of the tile in flight
+      for (int j = 0; j < CPL; ++j) {
         const int c = gl + 128 * j;
         const int r = c / CPR, cc = c - r * CPR;
         const Fp8Row R = rt[r];
@@ -486,14 +525,34 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
           }
         }
       }
+    };
+    if (nt > 0) issue(0);
+    for (int i = 0; i < nt; ++i) {
+      const int st = i % NS;
+      if (!tc::mbar_wait(&kempty[st], ((i / NS) & 1) ^ 1, abort_flag)) break;
+      unsigned char *stage = k_s + st * kStageBytes;
+      uint4 cv[kPipe ? CPL : 1];
+      uint32_t csc[kPipe ? CPL : 1];
+      uint32_t chas = has;
+      if constexpr (kPipe) {
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+          cv[j] = v[j];
+          csc[j] = sc[j];
+        }
+        if (i + 1 < nt) issue(i + 1);
+      }
+      // this tile's chunks: the copy (pipelined) or the loads themselves
+      auto chunk = [&](int j) -> const uint4 & { if constexpr (kPipe) return cv[j]; else return v[j]; };
+      auto scale = [&](int j) -> uint32_t { if constexpr (kPipe) return csc[j]; else return sc[j]; };
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
         const int c = gl + 128 * j;
         const int r = c / CPR, cc = c - r * CPR;
         const uint32_t ph = (uint32_t)(r & 7);
-        const bool hv = (has >> j) & 1u;
+        const bool hv = (chas >> j) & 1u;
         if (FMT == kFmtPacked && cc >= 28) {
-          const uint4 o = hv ? bf16x8_to_f16(v[j], bad) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 o = hv ? bf16x8_to_f16(chunk(j), bad) : make_uint4(0u, 0u, 0u, 0u);
           *reinterpret_cast<uint4 *>(stage + 7 * kKBlockBytes + r * 128 +
                                      (((uint32_t)(cc - 28) ^ ph) << 4)) = o;
           continue;
@@ -502,9 +561,9 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         o[0] = o[1] = ol[0] = ol[1] = make_uint4(0u, 0u, 0u, 0u);
         if (hv) {
           if (FMT == kFmtUniform)
-            deq16_e4m3_hilo(v[j], __uint_as_float(sc[j]), o, ol, bad);
+            deq16_e4m3_hilo(chunk(j), __uint_as_float(scale(j)), o, ol, bad);
           else
-            deq16_e4m3_pow2(v[j], sc[j], o[0], o[1], bad);
+            deq16_e4m3_pow2(chunk(j), scale(j), o[0], o[1], bad);
         }
         const uint32_t s0 = 2u * (uint32_t)(cc & 3);
         unsigned char *rowp = stage + (cc >> 2) * kKBlockBytes + r * 128;
@@ -517,9 +576,9 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         }
       }
       if (i + kPrefetchTiles < nt) prefetch_row(i + kPrefetchTiles);
-      if (i + 1 < nt) next = row_of(i + 1);
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&kfull[st]);
+      if (!kPipe && i + 1 < nt) issue(i + 1);
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.err_flag, DSA_DEVERR_FP16_RANGE);
     __syncwarp();
@@ -529,7 +588,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     const int sh = warp == 10 ? 1 : 0;
     if (lane == 0) {
       // S = Q K^T: A = Q (K-major, M = 64), B = K tile (K-major, N = 64)
-      constexpr uint32_t idesc_s = tc::idesc_f32acc(F::kOpType, F::kOpType, 0, 0, 64, 64);
+      constexpr uint32_t idesc_s = tc::idesc_f32acc(F::kOpType, F::kOpType, 0, 0, R, 64);
       const uint64_t adq = tc::sdesc_sw128(tc::smem_u32(q_s), 16, 1024);
       bool ok = nt == 0 || tc::mbar_wait(FMT == kFmtBf16 ? qfull : qready, 0, abort_flag);
       for (int i = 0; i < nt && ok; ++i) {
@@ -539,7 +598,8 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         if (!tc::mbar_wait(&sempty[sb], ((i >> 1) & 1) ^ 1, abort_flag)) break;
         tc::fence_after_sync();
         // descriptors: the start-address field is the byte address / 16, so
-        // a K-block (8192 B) adds 512 and 32 bytes of K add 2
+        // a K-block of Q (8192 B) adds 512, one of the tile kKBlockBytes / 16,
+        // and 32 bytes of K add 2
         const uint64_t bdk = tc::sdesc_sw128(tc::smem_u32(k_s + st * kStageBytes), 16, 1024);
         const uint32_t dcol = tmem + (sh ? kSbCol : kSCol) + sb * 64;
 #pragma unroll
@@ -547,13 +607,13 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
           if ((kb & 1) != sh) continue;
 #pragma unroll
           for (int ko = 0; ko < 4; ++ko)   // 32 bytes (16 values) of K per instruction
-            tc::mma_f16(dcol, adq + kb * 512 + 2 * ko, bdk + kb * 512 + 2 * ko, idesc_s,
+            tc::mma_f16(dcol, adq + kb * 512 + 2 * ko, bdk + kb * (kKBlockBytes >> 4) + 2 * ko, idesc_s,
                         (kb > sh || ko > 0) ? 1u : 0u);
           if (F::kLoBlocks > 0) {          // the low plane of the same K-block
 #pragma unroll
             for (int ko = 0; ko < 4; ++ko)
               tc::mma_f16(dcol, adq + kb * 512 + 2 * ko,
-                          bdk + (kKBlocks + kb) * 512 + 2 * ko, idesc_s, 1u);
+                          bdk + (kKBlocks + kb) * (kKBlockBytes >> 4) + 2 * ko, idesc_s, 1u);
           }
         }
         tc::mma_commit(&sfull[sb]);
@@ -579,9 +639,9 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         if (!tc::mbar_wait(pfull, i & 1, abort_flag)) break;
         tc::fence_after_sync();
         const uint32_t k_addr = tc::smem_u32(k_s + st * kStageBytes);
-        // A = V^T: dv block j is K-blocks 2j, 2j+1 (+1024 in the descriptor),
-        // 16 kv rows = 2048 B (+128); B = P (or P_lo, bf16: the RoPE block),
-        // 16 kv = 32 B (+2)
+        // A = V^T: dv block j is K-blocks 2j, 2j+1 (+2 kKBlockBytes / 16 in the
+        // descriptor), 16 kv rows = 2048 B (+128); B = P (or P_lo, bf16: the
+        // RoPE block), 16 kv = 32 B (+2)
         const uint64_t adv = tc::sdesc_sw128(k_addr, kKBlockBytes, 1024);
         const uint64_t bdp = tc::sdesc_sw128(p_addr, 16, 1024);
         const uint64_t bdl = tc::sdesc_sw128(k_addr + 8 * kKBlockBytes, 16, 1024);
@@ -590,7 +650,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
 #pragma unroll
           for (int kk = 0; kk < F::kPvSteps; ++kk) {
             const uint32_t kr = kk & 3;   // 16 kv rows per instruction
-            tc::mma_f16(tmem + kOCol + j * N, adv + j * 1024 + kr * 128,
+            tc::mma_f16(tmem + kOCol + j * N, adv + j * (kKBlockBytes >> 3) + kr * 128,
                         (kk < 4 ? bdp : bdl) + kr * 2, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
           }
           if (i == nt - 1) tc::mma_commit(&lastpv[j]);   // the epilogue of block j may start
@@ -636,29 +696,35 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     }
     for (int i = 0; i < nt && ok; ++i) {
       const int b = i & 1;                  // S buffer of tile i (= its K stage with two stages)
-      // validity of the 64 entries of this tile as a bit mask (2 loads per lane)
-      const int e = j0 + i * kTileRows + lane;
+      // validity of the R entries of this tile as a bit mask (1 or 2 loads a lane)
+      const int e = j0 + i * R + lane;
       const bool v_lo = e < je && entry_slot(a, t, e, quad == 0) >= 0;
-      const bool v_hi = e + 32 < je && entry_slot(a, t, e + 32, quad == 0) >= 0;
+      const bool v_hi = R > 32 && e + 32 < je && entry_slot(a, t, e + 32, quad == 0) >= 0;
       const uint32_t vm_lo = __ballot_sync(0xffffffffu, v_lo);
       const uint32_t vm_hi = __ballot_sync(0xffffffffu, v_hi);
       if (!tc::mbar_wait(&sfull[b], (i >> 1) & 1, abort_flag)) { ok = false; break; }
       tc::fence_after_sync();
-      float x[32];                          // this lane's half of its head's 64 scores
+      float x[RH];                          // this lane's half of its head's R scores
       {
-        float xb[32];                       // S = S_a + S_b (even and odd K-blocks)
-        tc::tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kSCol + b * 64, x);
-        tc::tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kSbCol + b * 64, xb);
+        float xb[RH];                       // S = S_a + S_b (even and odd K-blocks)
+        if constexpr (R == 64) {
+          tc::tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kSCol + b * 64, x);
+          tc::tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kSbCol + b * 64, xb);
+        } else {
+          tc::tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kSCol + b * 64, x);
+          tc::tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kSbCol + b * 64, xb);
+        }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] += xb[j];
+        for (int j = 0; j < RH; ++j) x[j] += xb[j];
       }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sempty[b]);
-      const uint32_t vm = half ? vm_hi : vm_lo;
+      // this lane's entries: kv RH * half + j
+      const uint32_t vm = R == 64 ? (half ? vm_hi : vm_lo) : (vm_lo >> (RH * half));
       float tmax = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < RH; ++j) {
         x[j] = ((vm >> j) & 1u) ? x[j] : -INFINITY;
         tmax = fmaxf(tmax, x[j]);
       }
@@ -686,9 +752,9 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       // P_hi + P_lo; fp8 pools: one fp16 term)
       const float msafe = m == -INFINITY ? 0.f : m;   // all masked so far: p = 0
       float ps = 0.f;
-      uint32_t phi[16], plo[4];
+      uint32_t phi[RH / 2], plo[4];
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
+      for (int j = 0; j < RH; j += 2) {
         const float p0 = exp2f((x[j] - msafe) * c);      // -inf -> 0
         const float p1 = exp2f((x[j + 1] - msafe) * c);
         ps += p0 + p1;
@@ -722,11 +788,12 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         for (int j = 0; j < 4; ++j) tc::tmem_scale_cols<N>(tmem + lane_base + kOCol + j * N, alpha);
       }
       if (hl < N) {
-        // row hl of P (K-major B operand): 64 kv 16-bit values = 128 bytes,
-        // swizzled; this lane's half is chunks 4 half .. 4 half + 3
+        // row hl of P (K-major B operand): R kv 16-bit values in a 128-byte
+        // swizzled row; this lane's half is chunks CH half .. CH half + CH - 1
+        constexpr int CH = RH / 8;          // 16-byte chunks a lane writes
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int ch = 4 * half + cc;
+        for (int cc = 0; cc < CH; ++cc) {
+          const int ch = CH * half + cc;
           const uint32_t off = hl * 128 + ((ch ^ (hl & 7)) << 4);
           *reinterpret_cast<uint4 *>(p_s + off) =
               make_uint4(phi[4 * cc], phi[4 * cc + 1], phi[4 * cc + 2], phi[4 * cc + 3]);
@@ -823,7 +890,7 @@ cudaError_t launch_n(const MlaArgs &a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const int total = a.k + a.k2;
   int per = (total + a.n_splits - 1) / a.n_splits;
-  per = (per + kTileRows - 1) / kTileRows * kTileRows;
+  per = (per + F::kRows - 1) / F::kRows * F::kRows;
   const MlaSmem L = mla_smem_layout<FMT>();
   auto kern = sparse_mla_tc_kernel<FMT, N>;
   cudaError_t e =

@@ -259,6 +259,23 @@ DSA_DEVINLINE void tmem_ld_16x32bx2_x32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// As tmem_ld_16x32bx2_x32, 16 columns: threads 0-15 read columns [c, c+16),
+// threads 16-31 columns [c+OFF, c+OFF+16) of the same 16 lanes.
+template <int OFF>
+DSA_DEVINLINE void tmem_ld_16x32bx2_x16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr), "n"(OFF));
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 32 lanes x 32 bits stores, 16 / 32 / 64 consecutive columns of this lane.
 DSA_DEVINLINE void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
