@@ -32,9 +32,11 @@
 // 128-dim blocks of 64 heads, then the 64 RoPE dims), dK^T [384, 512) (four
 // 128-dim blocks of 32 rows).
 //
-// Warps: 0-3 math (softmax terms, dS, the per-tile dK drain, dq at the end),
-// 4 the Q / dO loads and the S and dQ products, 5 the dP product and dK^T
-// blocks 0-1, 6 dK^T blocks 2-3 and RoPE, 7-10 the row gather.
+// Warps: 0-3 math (softmax terms, dS, dq at the end), 4 the Q / dO loads and
+// the S and dQ products, 5 the dP product and dK^T blocks 0-1, 6 dK^T blocks
+// 2-3 and RoPE, 7-10 the row gather, 11-14 the per-tile dK drain into dkv.
+// The drain reads the RoPE block first, which frees S's columns for the next
+// tile, so a tile's reductions overlap the next tile's S, softmax and dQ.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -51,7 +53,7 @@ constexpr int kKB = 9;                 // 64-column K-blocks of a row (576)
 constexpr int kKBV = 8;                // K-blocks of V (512)
 constexpr int kTileKB = kR * 128;      // one K-block of the tile: 4 KB
 constexpr int kHKB = 64 * 128;         // one K-block of Q or dO: 64 head rows, 8 KB
-constexpr int kThreads = 11 * 32;
+constexpr int kThreads = 15 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM columns
@@ -97,10 +99,11 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
   uint64_t *kfull = bars + 0;     // the tile landed (gather lanes)
   uint64_t *kempty = bars + 1;    // the tile's readers retired (S / dQ issuer, dP issuer)
   uint64_t *sfull = bars + 2;     // S and dP in TMEM (both issuers)
-  uint64_t *tfree = bars + 3;     // TMEM [0, 64) free again (math warps)
+  uint64_t *tfree = bars + 3;     // TMEM [0, 64) free again (math warps; pass 2: drain warps)
   uint64_t *pfull = bars + 4;     // dS / P planes written (math warps)
   uint64_t *dkfull = bars + 5;    // dQ^T and dK^T of the tile retired (three issuers)
   uint64_t *qfull = bars + 6;     // Q and dO landed
+  uint64_t *dkfree = bars + 13;   // the drain has read dK^T blocks 0-3 (drain warps)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 7);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 8);
 
@@ -123,6 +126,7 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
     tc::mbar_init(pfull, 4);
     tc::mbar_init(dkfull, 3);
     tc::mbar_init(qfull, 1);
+    tc::mbar_init(dkfree, 4);
     for (int b = 9; b < 12; ++b) tc::mbar_init(&bars[b], 1);   // each issuer's final drain
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -160,7 +164,7 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
   const int nt = (*last_s + 1 + kR - 1) / kR;
   const int steps = 2 * nt;       // step g: pass 1 for g < nt, pass 2 after; tile g % nt
 
-  if (warp >= 7) {
+  if (warp >= 7 && warp < 11) {
     // ------------------------------------------------------------ gather
     // lane gl < 32 publishes row gl's slot; every lane copies 18 of the
     // tile's 32 x 72 16-byte chunks (row r = c / 72, chunk cc = c % 72 into
@@ -289,6 +293,8 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
         if (g < nt) continue;
         const int g2 = g - nt;
         if (!tc::mbar_wait(pfull, g2 & 1, abort_flag)) break;
+        // blocks 0-3 of the previous tile drained (the RoPE block: tfree, which S waited for)
+        if (g2 > 0 && !tc::mbar_wait(dkfree, (g2 - 1) & 1, abort_flag)) break;
         tc::fence_after_sync();
         // warp 5: blocks 0, 1; warp 6: blocks 2, 3 and the RoPE block
         const int jb = w5 ? 0 : 2, je = w5 ? 2 : 5;
@@ -316,6 +322,52 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
       }
       tc::mma_commit(&bars[10 + (w5 ? 0 : 1)]);
       tc::mbar_wait_drain(&bars[10 + (w5 ? 0 : 1)], 0);
+    }
+    __syncwarp();
+  } else if (warp >= 11) {
+    // ------------------------------------------------------------ dK drain
+    // warp w reads TMEM lane quadrant w % 4: dims 128 j + 32 quad + lane of
+    // blocks 0-3 (32 rows each), and the RoPE dims 512 + 16 quad + lane % 16
+    // (rows 16 (lane / 16) .. +15)
+    const int quad = warp & 3;
+    const int half = lane >> 4;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    for (int g = nt; g < steps; ++g) {
+      if (!tc::mbar_wait(dkfull, (g - nt) & 1, abort_flag)) break;
+      tc::fence_after_sync();
+      // this tile's slots, before the columns are released: the gather may
+      // rewrite the slot table once the next tile is under way
+      const int *sl = slot_s + (g & 1) * kR;
+      int slots[kR];
+#pragma unroll
+      for (int r = 0; r < kR; ++r) slots[r] = sl[r];
+      float vr[16];
+      tc::tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColDKR, vr);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tfree);     // S of the next tile may be written
+      {
+        const int d = 512 + 16 * quad + (lane & 15);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const int sr = half ? slots[16 + r] : slots[r];   // constant indices: registers
+          if (sr >= 0) atomicAdd(a.dkv + (size_t)sr * 576 + d, vr[r]);
+        }
+      }
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        float v[32];
+        tc::tmem_ld_cols<32>(tmem + lane_base + kColDK + kR * j, v);
+        if (j == 3) {
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(dkfree);   // the next tile's dK^T may be written
+        }
+        const int d = 128 * j + 32 * quad + lane;
+#pragma unroll
+        for (int r = 0; r < kR; ++r)
+          if (slots[r] >= 0) atomicAdd(a.dkv + (size_t)slots[r] * 576 + d, v[r]);
+      }
     }
     __syncwarp();
   } else {
@@ -365,8 +417,12 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
         dsh[j / 2] = *reinterpret_cast<const uint32_t *>(&hi);
         dsl[j / 2] = pack_bf16x2(d0 - hf.x, d1 - hf.y);
       }
-      // the dK^T products of the previous tile have retired (dkfull) before
-      // these planes are rewritten: the wait below the drain ensures it
+      // the previous tile's dQ^T and dK^T products read these planes: they
+      // have retired before the planes are rewritten
+      if (g > nt) {
+        if (!tc::mbar_wait(dkfull, (g - nt - 1) & 1, abort_flag)) { ok = false; break; }
+        tc::fence_after_sync();
+      }
       // dS [heads][rows]: this lane's 16 rows are chunks 2 half, 2 half + 1 of row hl
 #pragma unroll
       for (int pl = 0; pl < 2; ++pl) {
@@ -397,35 +453,10 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(pfull);
-      // ---- the tile's dK^T into dkv: dims 128 j + 32 quad + lane (blocks
-      // 0-3, 32 rows each), then the RoPE dims 512 + 16 quad + lane % 16
-      if (!tc::mbar_wait(dkfull, (g - nt) & 1, abort_flag)) { ok = false; break; }
-      tc::fence_after_sync();
-#pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        float v[32];
-        tc::tmem_ld_cols<32>(tmem + lane_base + kColDK + kR * j, v);
-        const int d = 128 * j + 32 * quad + lane;
-#pragma unroll
-        for (int r = 0; r < kR; ++r) {
-          const int sr = sl[r];
-          if (sr >= 0) atomicAdd(a.dkv + (size_t)sr * 576 + d, v[r]);
-        }
-      }
-      {
-        float v[16];
-        tc::tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColDKR, v);
-        const int d = 512 + 16 * quad + (lane & 15);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          const int sr = sl[16 * half + r];
-          if (sr >= 0) atomicAdd(a.dkv + (size_t)sr * 576 + d, v[r]);
-        }
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tfree);
     }
+    // the last tile's dQ^T products retired (its dkfull) before dq is read
+    if (ok && nt > 0 && !tc::mbar_wait(dkfull, (nt - 1) & 1, abort_flag)) ok = false;
+    tc::fence_after_sync();
     // ---- dq: dQ^T from TMEM (all dQ products retired: the last dkfull)
     float *dqt = a.dq + (size_t)t * a.H * 576;
     const bool have = ok && nt > 0 && !*abort_flag;

@@ -8,12 +8,15 @@
 //     exact in fp16; times an fp32 scale it rounds once, to 2^-11 relative),
 //     Q is converted bf16 -> fp16 in shared memory, and the products run in
 //     fp16 -- whose 11-bit significand also carries p exactly enough that P
-//     needs one term.  With an fp32 scale (uniform pool) K also keeps its
-//     fp16 residual plane, S = Q K_hi^T + Q K_lo^T, because the scores are
-//     large enough (|s| ~ 20) that 2^-11 in K would move the lse by ~1e-3;
-//     with that second plane a tile holds 32 rows, so that two stages still
-//     fit beside Q.  A value beyond fp16's range (|x| > 65504) raises
-//     DSA_DEVERR_FP16_RANGE.
+//     needs one term.  The uniform pool's fp32 scales would cost S 2^-11 of
+//     relative accuracy if folded into fp16 K (with scores near 20 that moves
+//     the lse by ~1e-3), so its K stays the exact fp16 value of the e4m3 byte:
+//     each 64-column K-block (one scale group) gets its own TMEM accumulator,
+//     and the math warps add the eight products times their fp32 scales.  V
+//     (448 columns) is a second plane, the scaled value rounded once to fp16
+//     (2^-12 relative in the output).  With that plane a tile holds 32 rows,
+//     so that two stages fit beside Q.  A value beyond fp16's range (|x| >
+//     65504) raises DSA_DEVERR_FP16_RANGE.
 // (The "sparse attn" stage of tokenspeed PR #627 "Add gluon kernel for DSA";
 // semantics of miles PR #3608: natural-log lse, -1 entries masked.)
 //
@@ -92,11 +95,16 @@ template <int FMT> struct FmtTraits {
   static constexpr int kDv = FMT == kFmtBf16 ? 512 : 448;
   static constexpr int kPvSteps = FMT == kFmtBf16 ? 8 : kRows / 16;
   static constexpr uint32_t kOpType = FMT == kFmtBf16 ? 1u : 0u;
-  // uniform pool: K = K_hi + K_lo (two fp16 planes) for the S product, so an
-  // e4m3 value times an arbitrary fp32 scale keeps ~22 significant bits
-  static constexpr int kLoBlocks = FMT == kFmtUniform ? kKBlocks : 0;
+  // uniform pool: every 64-column K-block is one scale group, so S is the
+  // sum over K-blocks g of scale[row, g] * (Q_g . K8_g), where K8 is the
+  // e4m3 byte converted to fp16 (exact).  Each K-block's product has its own
+  // TMEM accumulator (8 x 32 columns, one buffer) and the math warps apply
+  // the fp32 scales as they add them up.  V (the first 448 columns) gets a
+  // second plane: the scaled value rounded to fp16 once.
+  static constexpr bool kGroupS = FMT == kFmtUniform;
+  static constexpr int kVBlocks = kGroupS ? kKBlocks : 0;   // the scaled V plane
   static constexpr int kStages = 2;
-  static constexpr int kStageBytes = (kKBlocks + kLoBlocks) * kKBlockBytes;   // 72, 64 or 64 KB
+  static constexpr int kStageBytes = (kKBlocks + kVBlocks) * kKBlockBytes;   // 72, 64 or 64 KB
   // rows are pulled into L2 this many tiles ahead (256 rows)
   static constexpr int kPrefetchTiles = 256 / kRows;
   // gather warps: four, 16 rows each per tile (bf16: cp.async issue split
@@ -127,7 +135,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 struct MlaSmem {
-  uint32_t q, k, p, alpha, rows, inv_l, flag, bars, total;
+  uint32_t q, k, p, alpha, rows, gsc, inv_l, flag, bars, total;
 };
 
 template <int FMT>
@@ -139,7 +147,8 @@ __host__ __device__ inline MlaSmem mla_smem_layout() {
   L.p = L.k + F::kStages * F::kStageBytes;
   L.alpha = L.p + 64 * 128;          // [2][64] rescale factors, by tile parity
   L.rows = L.alpha + 2 * 64 * 4;     // [2][64] fp8 row descriptors, by tile parity
-  L.inv_l = L.rows + (FMT == kFmtBf16 ? 0 : 2 * 64 * 16);   // [64] 1 / final sums
+  L.gsc = L.rows + (FMT == kFmtBf16 ? 0 : 2 * 64 * 16);     // uniform: [2 stages][8 groups][32 rows] scales
+  L.inv_l = L.gsc + (FmtTraits<FMT>::kGroupS ? 2 * 8 * 32 * 4 : 0);   // [64] 1 / final sums
   L.flag = L.inv_l + 64 * 4;         // [2][4] ints, by tile parity
   L.bars = L.flag + 32;              // 8-byte aligned
   L.total = L.bars + 32 * 8;
@@ -244,9 +253,10 @@ __device__ __forceinline__ void deq16_e4m3_pow2(const uint4 v, uint32_t e, uint4
   o1 = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
-// As deq16_e4m3, and the fp16 residuals x - hi(x) as a second plane.
-__device__ __forceinline__ void deq16_e4m3_hilo(const uint4 v, float s, uint4 (&hi)[2],
-                                                uint4 (&lo)[2], bool &bad) {
+// 16 e4m3 values -> their exact fp16 values (kx) and the values times s
+// rounded to fp16 (vv), two 16-byte words each, same order.
+__device__ __forceinline__ void deq16_e4m3_kx_v(const uint4 v, float s, uint4 (&kx)[2],
+                                                uint4 (&vv)[2], bool &bad) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t h[8], r[8];
 #pragma unroll
@@ -255,19 +265,15 @@ __device__ __forceinline__ void deq16_e4m3_hilo(const uint4 v, float s, uint4 (&
     for (int hh = 0; hh < 2; ++hh) {
       const __half2_raw raw = __nv_cvt_fp8x2_to_halfraw2(
           (__nv_fp8x2_storage_t)((w[i] >> (16 * hh)) & 0xffffu), __NV_E4M3);
+      h[2 * i + hh] = *reinterpret_cast<const uint32_t *>(&raw);
       const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&raw));
-      const float x0 = f.x * s, x1 = f.y * s;
-      const uint32_t hv = to_f16x2(x0, x1, bad);
-      const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hv));
-      bool unused = false;
-      h[2 * i + hh] = hv;
-      r[2 * i + hh] = to_f16x2(x0 - hf.x, x1 - hf.y, unused);
+      r[2 * i + hh] = to_f16x2(f.x * s, f.y * s, bad);
     }
   }
-  hi[0] = make_uint4(h[0], h[1], h[2], h[3]);
-  hi[1] = make_uint4(h[4], h[5], h[6], h[7]);
-  lo[0] = make_uint4(r[0], r[1], r[2], r[3]);
-  lo[1] = make_uint4(r[4], r[5], r[6], r[7]);
+  kx[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  kx[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  vv[0] = make_uint4(r[0], r[1], r[2], r[3]);
+  vv[1] = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
 // 8 bf16 values (one 16-byte word) -> 8 fp16, same order.
@@ -486,15 +492,10 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
     };
     for (int i = 1; i < min(nt, kPrefetchTiles); ++i) prefetch_row(i);   // tile 0 is loaded at once
     bool bad = false;
-    // Software pipeline (uniform pool, 8 chunks a lane): tile i+1's loads
-    // are issued (into a second register set) as soon as tile i's stage is
-    // free, before tile i is dequantised, so one tile's global-load latency
-    // overlaps the previous tile's conversion.  The packed pool's 18 chunks
-    // a lane leave no room for a second set: its next loads follow the
-    // conversion.  The row table is double-buffered by tile parity: a lane
-    // reads tile i's half only in issue(i), which every lane has left before
-    // any lane passes the barrier of issue(i+1).
-    constexpr bool kPipe = FMT == kFmtUniform;
+    // The row table is double-buffered by tile parity: a lane reads tile i's
+    // half only in issue(i), which every lane has left before any lane
+    // passes the barrier of issue(i+1).  (Issuing tile i+1's loads before
+    // converting tile i, into a second register set, was measured: no gain.)
     uint4 v[CPL];
     uint32_t sc[CPL];                     // fp32 scale bits (uniform) or UE8M0 byte (packed)
     uint32_t has = 0;
@@ -531,20 +532,9 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       const int st = i % NS;
       if (!tc::mbar_wait(&kempty[st], ((i / NS) & 1) ^ 1, abort_flag)) break;
       unsigned char *stage = k_s + st * kStageBytes;
-      uint4 cv[kPipe ? CPL : 1];
-      uint32_t csc[kPipe ? CPL : 1];
-      uint32_t chas = has;
-      if constexpr (kPipe) {
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-          cv[j] = v[j];
-          csc[j] = sc[j];
-        }
-        if (i + 1 < nt) issue(i + 1);
-      }
-      // this tile's chunks: the copy (pipelined) or the loads themselves
-      auto chunk = [&](int j) -> const uint4 & { if constexpr (kPipe) return cv[j]; else return v[j]; };
-      auto scale = [&](int j) -> uint32_t { if constexpr (kPipe) return csc[j]; else return sc[j]; };
+      const uint32_t chas = has;
+      auto chunk = [&](int j) -> const uint4 & { return v[j]; };
+      auto scale = [&](int j) -> uint32_t { return sc[j]; };
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
         const int c = gl + 128 * j;
@@ -561,7 +551,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         o[0] = o[1] = ol[0] = ol[1] = make_uint4(0u, 0u, 0u, 0u);
         if (hv) {
           if (FMT == kFmtUniform)
-            deq16_e4m3_hilo(chunk(j), __uint_as_float(scale(j)), o, ol, bad);
+            deq16_e4m3_kx_v(chunk(j), __uint_as_float(scale(j)), o, ol, bad);
           else
             deq16_e4m3_pow2(chunk(j), scale(j), o[0], o[1], bad);
         }
@@ -570,15 +560,19 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         *reinterpret_cast<uint4 *>(rowp + ((s0 ^ ph) << 4)) = o[0];
         *reinterpret_cast<uint4 *>(rowp + (((s0 + 1) ^ ph) << 4)) = o[1];
         if (FMT == kFmtUniform) {
-          unsigned char *lowp = rowp + kKBlocks * kKBlockBytes;
-          *reinterpret_cast<uint4 *>(lowp + ((s0 ^ ph) << 4)) = ol[0];
-          *reinterpret_cast<uint4 *>(lowp + (((s0 + 1) ^ ph) << 4)) = ol[1];
+          unsigned char *vp = rowp + kKBlocks * kKBlockBytes;   // the scaled V plane
+          *reinterpret_cast<uint4 *>(vp + ((s0 ^ ph) << 4)) = ol[0];
+          *reinterpret_cast<uint4 *>(vp + (((s0 + 1) ^ ph) << 4)) = ol[1];
+          // the row's group scale (0 for a masked row: its S terms are masked anyway)
+          if ((cc & 3) == 0)
+            reinterpret_cast<float *>(smem + L.gsc)[(st * 8 + (cc >> 2)) * 32 + r] =
+                hv ? __uint_as_float(scale(j)) : 0.f;
         }
       }
       if (i + kPrefetchTiles < nt) prefetch_row(i + kPrefetchTiles);
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&kfull[st]);
-      if (!kPipe && i + 1 < nt) issue(i + 1);
+      if (i + 1 < nt) issue(i + 1);
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.err_flag, DSA_DEVERR_FP16_RANGE);
     __syncwarp();
@@ -595,7 +589,10 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         const int st = i % NS;              // K stage
         const int sb = i & 1;               // S buffer in TMEM
         if (!tc::mbar_wait(&kfull[st], (i / NS) & 1, abort_flag)) break;
-        if (!tc::mbar_wait(&sempty[sb], ((i >> 1) & 1) ^ 1, abort_flag)) break;
+        // one S buffer for the per-group accumulators (uniform pool), else two
+        if (!tc::mbar_wait(&sempty[F::kGroupS ? 0 : sb],
+                           ((F::kGroupS ? i : (i >> 1)) & 1) ^ 1, abort_flag))
+          break;
         tc::fence_after_sync();
         // descriptors: the start-address field is the byte address / 16, so
         // a K-block of Q (8192 B) adds 512, one of the tile kKBlockBytes / 16,
@@ -605,18 +602,19 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
 #pragma unroll
         for (int kb = 0; kb < kKBlocks; ++kb) {
           if ((kb & 1) != sh) continue;
-#pragma unroll
-          for (int ko = 0; ko < 4; ++ko)   // 32 bytes (16 values) of K per instruction
-            tc::mma_f16(dcol, adq + kb * 512 + 2 * ko, bdk + kb * (kKBlockBytes >> 4) + 2 * ko, idesc_s,
-                        (kb > sh || ko > 0) ? 1u : 0u);
-          if (F::kLoBlocks > 0) {          // the low plane of the same K-block
+          if constexpr (F::kGroupS) {      // K-block kb into its own accumulator
 #pragma unroll
             for (int ko = 0; ko < 4; ++ko)
-              tc::mma_f16(dcol, adq + kb * 512 + 2 * ko,
-                          bdk + (kKBlocks + kb) * (kKBlockBytes >> 4) + 2 * ko, idesc_s, 1u);
+              tc::mma_f16(tmem + kSCol + kb * R, adq + kb * 512 + 2 * ko,
+                          bdk + kb * (kKBlockBytes >> 4) + 2 * ko, idesc_s, ko > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int ko = 0; ko < 4; ++ko)   // 32 bytes (16 values) of K per instruction
+              tc::mma_f16(dcol, adq + kb * 512 + 2 * ko, bdk + kb * (kKBlockBytes >> 4) + 2 * ko,
+                          idesc_s, (kb > sh || ko > 0) ? 1u : 0u);
           }
         }
-        tc::mma_commit(&sfull[sb]);
+        tc::mma_commit(&sfull[F::kGroupS ? 0 : sb]);
       }
       if (nt > 0) {
         // this warp's MMAs retired before TMEM is released
@@ -642,7 +640,8 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         // A = V^T: dv block j is K-blocks 2j, 2j+1 (+2 kKBlockBytes / 16 in the
         // descriptor), 16 kv rows = 2048 B (+128); B = P (or P_lo, bf16: the
         // RoPE block), 16 kv = 32 B (+2)
-        const uint64_t adv = tc::sdesc_sw128(k_addr, kKBlockBytes, 1024);
+        const uint64_t adv =
+            tc::sdesc_sw128(k_addr + (F::kGroupS ? kKBlocks * kKBlockBytes : 0), kKBlockBytes, 1024);
         const uint64_t bdp = tc::sdesc_sw128(p_addr, 16, 1024);
         const uint64_t bdl = tc::sdesc_sw128(k_addr + 8 * kKBlockBytes, 16, 1024);
 #pragma unroll
@@ -702,10 +701,31 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       const bool v_hi = R > 32 && e + 32 < je && entry_slot(a, t, e + 32, quad == 0) >= 0;
       const uint32_t vm_lo = __ballot_sync(0xffffffffu, v_lo);
       const uint32_t vm_hi = __ballot_sync(0xffffffffu, v_hi);
-      if (!tc::mbar_wait(&sfull[b], (i >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!tc::mbar_wait(&sfull[F::kGroupS ? 0 : b], (F::kGroupS ? i : (i >> 1)) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
       tc::fence_after_sync();
       float x[RH];                          // this lane's half of its head's R scores
-      {
+      if constexpr (F::kGroupS) {
+        // S = sum over groups g of scale[row, g] * S_g (rows RH half .. + RH - 1)
+        const float *gs = reinterpret_cast<const float *>(smem + L.gsc) + (i % NS) * 8 * 32 + RH * half;
+#pragma unroll
+        for (int j = 0; j < RH; ++j) x[j] = 0.f;
+#pragma unroll
+        for (int g = 0; g < kKBlocks; ++g) {
+          float sg[RH];
+          tc::tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kSCol + g * R, sg);
+#pragma unroll
+          for (int j = 0; j < RH; j += 4) {
+            const float4 sc4 = *reinterpret_cast<const float4 *>(gs + g * 32 + j);
+            x[j] = fmaf(sg[j], sc4.x, x[j]);
+            x[j + 1] = fmaf(sg[j + 1], sc4.y, x[j + 1]);
+            x[j + 2] = fmaf(sg[j + 2], sc4.z, x[j + 2]);
+            x[j + 3] = fmaf(sg[j + 3], sc4.w, x[j + 3]);
+          }
+        }
+      } else {
         float xb[RH];                       // S = S_a + S_b (even and odd K-blocks)
         if constexpr (R == 64) {
           tc::tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kSCol + b * 64, x);
@@ -719,7 +739,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sempty[b]);
+      if (lane == 0) tc::mbar_arrive(&sempty[F::kGroupS ? 0 : b]);
       // this lane's entries: kv RH * half + j
       const uint32_t vm = R == 64 ? (half ? vm_hi : vm_lo) : (vm_lo >> (RH * half));
       float tmax = -INFINITY;
