@@ -237,49 +237,55 @@ sparse_mla_simt_kernel(MlaArgs a) {
   }
 }
 
-// Merge split partials: one warp per (token, head) record (Dv <= 512: four
-// float4 columns a lane), the splits folded in batches whose loads -- lse
-// values and partial rows alike -- are all in flight together, so a call with
-// at most kCombineBatch splits waits for one round of L2 latency.
+// Merge split partials.  A warp per (token, head) record, or, for a call with
+// few records (a single-token decode: 64 records), a warp per quarter of a
+// record, so that such a call still has a few hundred warps.  Lane l holds
+// the float4 columns l + 32 c of its part.  The splits are folded in batches
+// whose loads -- lse values and partial columns alike -- are all issued
+// before any is used, into a running maximum and sum; a call with at most
+// one batch of splits (4 a record-warp, 16 a quarter-warp, whose lanes hold
+// one column each) waits for one round of L2 latency.
 constexpr int kMaxSplits = 256;
 
-constexpr int kCombineWarps = 8;     // records per 256-thread CTA, one per warp
-constexpr int kCombineBatch = 4;     // splits whose loads are in flight together
+constexpr int kCombineWarps = 8;     // warps per 256-thread CTA
+constexpr int kFewRecords = 512;     // at most this many records: four warps a record
 
+template <int QPR>   // warps per record: 1 or 4
 __global__ void __launch_bounds__(32 * kCombineWarps)
 mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse, int T,
                    int H, int Dv, int n_splits, __nv_bfloat16 *__restrict__ out,
                    float *__restrict__ lse, const float *__restrict__ sinks, int lse_log2) {
+  constexpr int CPL = 4 / QPR;                   // float4 columns a lane holds
+  constexpr int kCombineBatch = QPR == 4 ? 16 : 4;   // splits whose loads are in flight together
   pdl_wait();      // the partials come from the previous kernel
-  // one warp per record (t, h); lane l holds the float4 columns l + 32 q
-  const int64_t r = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
-  if (r >= (int64_t)T * H) return;
+  const int64_t w = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (w >= (int64_t)T * H * QPR) return;
   const int lane = threadIdx.x & 31;
+  const int64_t r = w / QPR;                     // record (t, h)
+  const int part = (int)(w - r * QPR);
   const int64_t t = r / H, h = r - t * H;
   const int nf = Dv >> 2;                        // float4 columns of a record
-  // the splits in batches: every load of a batch (its lse values and its
-  // partial rows) is issued before any is used, and the batch folds into a
-  // running maximum and sum
+  const int f0 = 32 * CPL * part + lane;         // this lane's columns: f0 + 32 c
   float mx = -INFINITY, tot = 0.f;
-  float4 acc[4];
+  float4 acc[CPL];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < CPL; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int i0 = 0; i0 < n_splits; i0 += kCombineBatch) {
     float li[kCombineBatch];
-    float4 v[kCombineBatch][4];
+    float4 v[kCombineBatch][CPL];
 #pragma unroll
     for (int b = 0; b < kCombineBatch; ++b) {
       const int i = i0 + b;
       li[b] = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) v[b][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < CPL; ++c) v[b][c] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (i < n_splits) {
         const int64_t rec = (t * n_splits + i) * H + h;
         li[b] = __ldcg(part_lse + rec);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int f = lane + 32 * q;
-          if (f < nf) v[b][q] = __ldcg(reinterpret_cast<const float4 *>(part_o + rec * Dv) + f);
+        for (int c = 0; c < CPL; ++c) {
+          const int f = f0 + 32 * c;
+          if (f < nf) v[b][c] = __ldcg(reinterpret_cast<const float4 *>(part_o + rec * Dv) + f);
         }
       }
     }
@@ -290,8 +296,8 @@ mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ p
     const float sc = mx == -INFINITY ? 0.f : __expf(mx - bm);
     tot *= sc;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      acc[q].x *= sc; acc[q].y *= sc; acc[q].z *= sc; acc[q].w *= sc;
+    for (int c = 0; c < CPL; ++c) {
+      acc[c].x *= sc; acc[c].y *= sc; acc[c].z *= sc; acc[c].w *= sc;
     }
 #pragma unroll
     for (int b = 0; b < kCombineBatch; ++b) {
@@ -299,11 +305,11 @@ mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ p
       const float wgt = li[b] == -INFINITY ? 0.f : __expf(li[b] - bm);
       tot += wgt;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[q].x = fmaf(wgt, v[b][q].x, acc[q].x);
-        acc[q].y = fmaf(wgt, v[b][q].y, acc[q].y);
-        acc[q].z = fmaf(wgt, v[b][q].z, acc[q].z);
-        acc[q].w = fmaf(wgt, v[b][q].w, acc[q].w);
+      for (int c = 0; c < CPL; ++c) {
+        acc[c].x = fmaf(wgt, v[b][c].x, acc[c].x);
+        acc[c].y = fmaf(wgt, v[b][c].y, acc[c].y);
+        acc[c].z = fmaf(wgt, v[b][c].z, acc[c].z);
+        acc[c].w = fmaf(wgt, v[b][c].w, acc[c].w);
       }
     }
     mx = bm;
@@ -317,24 +323,24 @@ mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ p
       const float sc = mx == -INFINITY ? 0.f : __expf(mx - M);
       tot = tot * sc + __expf(sg - M);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[q].x *= sc; acc[q].y *= sc; acc[q].z *= sc; acc[q].w *= sc;
+      for (int c = 0; c < CPL; ++c) {
+        acc[c].x *= sc; acc[c].y *= sc; acc[c].z *= sc; acc[c].w *= sc;
       }
       mx = M;
     }
   }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int f = lane + 32 * q;
+  for (int c = 0; c < CPL; ++c) {
+    const int f = f0 + 32 * c;
     if (f < nf) {
       uint2 pk;
-      pk.x = pack_bf16x2(acc[q].x * inv, acc[q].y * inv);
-      pk.y = pack_bf16x2(acc[q].z * inv, acc[q].w * inv);
+      pk.x = pack_bf16x2(acc[c].x * inv, acc[c].y * inv);
+      pk.y = pack_bf16x2(acc[c].z * inv, acc[c].w * inv);
       *reinterpret_cast<uint2 *>(out + r * Dv + 4 * f) = pk;
     }
   }
-  if (lane == 0) lse[r] = lse_report(tot > 0.f ? mx + logf(tot) : -INFINITY, lse_log2);
+  if (part == 0 && lane == 0) lse[r] = lse_report(tot > 0.f ? mx + logf(tot) : -INFINITY, lse_log2);
 }
 
 }  // namespace
@@ -390,8 +396,10 @@ cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_splits == 1) return e;
   const int64_t recs = (int64_t)a.T * a.H;
-  return launch_pdl(mla_combine_kernel,
-                    dim3((unsigned)((recs + kCombineWarps - 1) / kCombineWarps)),
+  const bool few = recs <= kFewRecords;
+  const int64_t warps = recs * (few ? 4 : 1);
+  return launch_pdl(few ? mla_combine_kernel<4> : mla_combine_kernel<1>,
+                    dim3((unsigned)((warps + kCombineWarps - 1) / kCombineWarps)),
                     dim3(32 * kCombineWarps), 0, s, (const float *)a.part_o,
                     (const float *)a.part_lse, a.T, a.H, a.Dv, a.n_splits,
                     static_cast<__nv_bfloat16 *>(a.out), a.lse, a.sinks, a.lse_log2);
