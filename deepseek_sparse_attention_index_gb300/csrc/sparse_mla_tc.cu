@@ -712,7 +712,7 @@ sparse_mla_tc_kernel(MlaArgs a, const __grid_constant__ CUtensorMap qmap, int pe
         const float *gs = reinterpret_cast<const float *>(smem + L.gsc) + (i % NS) * 8 * 32 + RH * half;
 #pragma unroll
         for (int j = 0; j < RH; ++j) x[j] = 0.f;
-#pragma unroll
+#pragma unroll 1
         for (int g = 0; g < kKBlocks; ++g) {
           float sg[RH];
           tc::tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kSCol + g * R, sg);

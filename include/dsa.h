@@ -360,9 +360,13 @@ int dsa_decode_paged(const void *q_idx, int idx_dtype, const float *q_scale,
  * h_slot_base, h_q_idx, h_w, h_q_scale into the workspace, then the step,
  * then h_idx_out (optional), h_out and h_lse back.
  * Host pointers (h_*) are read and written by the copies when `stream` gets
- * there: they must stay valid until then, as with cudaMemcpyAsync.  Page-
- * locked (pinned) host memory lets the copies run asynchronously; pageable
- * memory is accepted and the CUDA runtime then stages the copies itself.
+ * there: they must stay valid until then, as with cudaMemcpyAsync.  When
+ * every given host buffer is page-locked (pinned, so the GPU reaches it at
+ * its device-mapped address) and 16-byte aligned, two kernels move the data
+ * (one gathers the inputs, one writes the outputs back), which avoids the
+ * fixed cost of ten copy-engine transfers.  Otherwise each buffer is copied
+ * with cudaMemcpyAsync; pageable memory is accepted and the CUDA runtime then
+ * stages those copies itself.  Both give the same results bit for bit.
  * Shapes, types and limits are those of dsa_decode.  err_flag, if given, is
  * a device pointer.  No host synchronisation: the outputs are in host memory
  * once `stream` has passed this call (e.g. after cudaStreamSynchronize).

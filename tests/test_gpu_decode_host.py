@@ -69,6 +69,23 @@ def test_decode_host_equals_device_call(name, make):
     _same(lse_h, lse_d)
 
 
+def test_decode_host_pageable_buffers_equal_pinned():
+    """Pinned host buffers are moved by copy kernels, pageable ones by the copy
+    engines: the same results either way (odd sizes leave byte tails)."""
+    case = I.decode_case("host_pageable", 3, [700, 5000, 20001], 64, 128, "fp8", 2048, 64,
+                         I.KV_BF16, device="cuda")
+    h = _host_inputs(case)
+    pageable = {k: (None if v is None else v.clone()) for k, v in h.items()}
+    assert all(v is None or not v.is_pinned() for v in pageable.values())
+    a = _run_host(case, h)
+    b = _run_host(case, pageable, idx_out=torch.empty((3, case.k), dtype=torch.int32),
+                  out=torch.empty((3, case.H, case.Dv), dtype=torch.bfloat16),
+                  lse=torch.empty((3, case.H), dtype=torch.float32))
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
 def test_decode_host_against_oracle():
     case = I.decode_case("host_oracle", 3, [129, 2500, 6000], 64, 128, "fp8", 2048, 64, I.KV_BF16,
                          device="cuda")
