@@ -15,7 +15,9 @@
 //
 // One CTA per (token, group of <= 64 heads) walks the token's list in tiles
 // of 32 gathered rows, twice.  Pass 1 sums delta; pass 2 forms dS and the
-// gradients.  Per tile (tcgen05, bf16 operands, fp32 accumulators in TMEM):
+// gradients.  Pass 1 alternates two tile buffers (the second is the region
+// that holds the dS / P operand planes in pass 2), so the next tile's gather
+// overlaps the current tile's products.  Per tile (tcgen05, bf16 operands, fp32 accumulators in TMEM):
 //   S   = Q  K^T     M = 64 heads, N = 32 rows, K = 576   (pass 1 and 2)
 //   dP  = dO V^T     M = 64 heads, N = 32 rows, K = 512   (pass 1 and 2)
 //   dQ^T += K^T dS^T M = 128 dims (64 for RoPE), N = 64 heads, K = 32 rows;
@@ -60,23 +62,36 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kColS = 0, kColDP = 32, kColDQ = 64, kColDK = 384, kColDKR = 0;
 
 struct BwdSmem {
-  uint32_t q, dout, k, ds_h, ds_t, p_t, lse, slot, bars, total;
+  uint32_t q, dout, k, k2, ds_h, ds_t, p_t, lse, slot, bars, total;
 };
 __host__ __device__ inline BwdSmem bwd_smem_layout() {
   BwdSmem L;
   L.q = 0;                              // bf16 [64 heads][576], 9 swizzled K-blocks
   L.dout = L.q + kKB * kHKB;            // bf16 [64 heads][512], 8 K-blocks
-  L.k = L.dout + kKBV * kHKB;           // bf16 [32 rows][576], 9 K-blocks of 4 KB
-  L.ds_h = L.k + kKB * kTileKB;         // dS [64 heads][32 rows], hi and lo (128-byte rows)
+  L.k = L.dout + kKBV * kHKB;           // stage A: bf16 [32 rows][576], 9 K-blocks of 4 KB
+  // region 2: pass 1 uses it as a second K stage (B); pass 2 as the dS / P
+  // operand planes
+  L.k2 = L.k + kKB * kTileKB;
+  L.ds_h = L.k2;                        // dS [64 heads][32 rows], hi and lo (128-byte rows)
   L.ds_t = L.ds_h + 2 * kHKB;           // dS^T [32 rows][64 heads], hi and lo
   L.p_t = L.ds_t + 2 * kTileKB;         // P^T  [32 rows][64 heads], hi and lo
-  L.lse = L.p_t + 2 * kTileKB;          // fp32 [64] (natural log, padded heads +inf)
-  L.slot = L.lse + 64 * 4;              // int [2][32] slots of the tile (-1: masked), by parity
-  L.bars = L.slot + 2 * kR * 4;         // mbarriers (8-byte aligned)
+  L.lse = L.k2 + kKB * kTileKB;         // fp32 [64] (natural log, padded heads +inf)
+  L.slot = L.lse + 64 * 4;              // int [4][32] slots of step g's tile (-1: masked) at g % 4
+  L.bars = L.slot + 4 * kR * 4;         // mbarriers (8-byte aligned)
   L.total = L.bars + 16 * 8;
   return L;
 }
 
+// Step g (pass 1: g < nt, pass 2 after) uses K stage st and is that stage's
+// u-th use: pass 1 alternates stages A and B, pass 2 uses A only.
+struct StageUse {
+  int st;
+  int u;
+};
+__device__ __forceinline__ StageUse stage_use(int g, int nt) {
+  if (g < nt) return StageUse{g & 1, g >> 1};
+  return StageUse{0, ((nt + 1) >> 1) + (g - nt)};
+}
 // 16-bit element (row r, column c) of a 128-byte-swizzled operand buffer
 __device__ __forceinline__ uint32_t sw_off(int r, int c) {
   return (uint32_t)(r * 128 + ((((c >> 3) ^ (r & 7))) << 4) + (c & 7) * 2);
@@ -90,14 +105,16 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
   unsigned char *q_s = smem + L.q;
   unsigned char *do_s = smem + L.dout;
   unsigned char *k_s = smem + L.k;
+  unsigned char *k2_s = smem + L.k2;
   unsigned char *dsh_s = smem + L.ds_h;
   unsigned char *dst_s = smem + L.ds_t;
   unsigned char *pt_s = smem + L.p_t;
   float *lse_s = reinterpret_cast<float *>(smem + L.lse);
   int *slot_s = reinterpret_cast<int *>(smem + L.slot);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
-  uint64_t *kfull = bars + 0;     // the tile landed (gather lanes)
-  uint64_t *kempty = bars + 1;    // the tile's readers retired (S / dQ issuer, dP issuer)
+  uint64_t *kfull = bars + 14;    // [2] by K stage: the tile landed (gather lanes)
+  uint64_t *kempty = bars + 0;    // [2] by K stage: the tile's readers retired (S / dQ issuer,
+                                  //     dP issuer); the second at bars + 1
   uint64_t *sfull = bars + 2;     // S and dP in TMEM (both issuers)
   uint64_t *tfree = bars + 3;     // TMEM [0, 64) free again (math warps; pass 2: drain warps)
   uint64_t *pfull = bars + 4;     // dS / P planes written (math warps)
@@ -119,8 +136,10 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
     return;
   }
   if (threadIdx.x == 0) {
-    tc::mbar_init(kfull, 32 * 4);
-    tc::mbar_init(kempty, 2);
+    for (int st = 0; st < 2; ++st) {
+      tc::mbar_init(&kfull[st], 32 * 4);
+      tc::mbar_init(&kempty[st], 2);
+    }
     tc::mbar_init(sfull, 2);
     tc::mbar_init(tfree, 4);
     tc::mbar_init(pfull, 4);
@@ -172,8 +191,9 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
     const int gl = threadIdx.x - 7 * 32;   // 0..127
     for (int g = 0; g < steps; ++g) {
       const int i = g % nt;
-      if (!tc::mbar_wait(kempty, (g & 1) ^ 1, abort_flag)) break;
-      int *sl = slot_s + (g & 1) * kR;
+      const StageUse su = stage_use(g, nt);
+      if (!tc::mbar_wait(&kempty[su.st], (su.u & 1) ^ 1, abort_flag)) break;
+      int *sl = slot_s + (g & 3) * kR;
       if (gl < kR) {
         const int e = i * kR + gl;
         int s = -1;
@@ -185,7 +205,7 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
         sl[gl] = s;
       }
       tc::named_bar_sync(2, 128);
-      const uint32_t kb0 = tc::smem_u32(k_s);
+      const uint32_t kb0 = tc::smem_u32(su.st ? k2_s : k_s);
 #pragma unroll 6
       for (int j = 0; j < 18; ++j) {
         const int c = gl + 128 * j;
@@ -201,7 +221,7 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
       asm volatile("cp.async.commit_group;" ::: "memory");
       asm volatile("cp.async.wait_group 0;" ::: "memory");
       tc::fence_proxy_async_smem();
-      tc::mbar_arrive(kfull);
+      tc::mbar_arrive(&kfull[su.st]);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncwarp();
@@ -221,14 +241,15 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
       constexpr uint32_t idesc_q = tc::idesc_f32acc(1, 1, 1, 0, 64, 128);
       constexpr uint32_t idesc_qr = tc::idesc_f32acc(1, 1, 1, 0, 64, 64);
       const uint64_t adq = tc::sdesc_sw128(tc::smem_u32(q_s), 16, 1024);
-      const uint64_t bdk = tc::sdesc_sw128(tc::smem_u32(k_s), 16, 1024);
-      const uint64_t akt = tc::sdesc_sw128(tc::smem_u32(k_s), kTileKB, 1024);
       const uint64_t bds = tc::sdesc_sw128(tc::smem_u32(dsh_s), 16, 1024);
       bool ok = nt == 0 || tc::mbar_wait(qfull, 0, abort_flag);
       for (int g = 0; g < steps && ok; ++g) {
-        if (!tc::mbar_wait(kfull, g & 1, abort_flag)) break;
+        const StageUse su = stage_use(g, nt);
+        if (!tc::mbar_wait(&kfull[su.st], su.u & 1, abort_flag)) break;
         if (g > 0 && !tc::mbar_wait(tfree, (g - 1) & 1, abort_flag)) break;
         tc::fence_after_sync();
+        const uint32_t kst = tc::smem_u32(su.st ? k2_s : k_s);
+        const uint64_t bdk = tc::sdesc_sw128(kst, 16, 1024);
 #pragma unroll 1
         for (int kb = 0; kb < kKB; ++kb)
 #pragma unroll
@@ -240,6 +261,7 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
           const int g2 = g - nt;
           if (!tc::mbar_wait(pfull, g2 & 1, abort_flag)) break;
           tc::fence_after_sync();
+          const uint64_t akt = tc::sdesc_sw128(kst, kTileKB, 1024);
           // dims 0..511: four M = 128 blocks (K-blocks 2j, 2j+1); RoPE: M = 64
 #pragma unroll 1
           for (int j = 0; j < 5; ++j) {
@@ -253,7 +275,7 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
           }
           tc::mma_commit(dkfull);
         }
-        tc::mma_commit(kempty);
+        tc::mma_commit(&kempty[su.st]);
       }
       tc::mma_commit(&bars[9]);
       tc::mbar_wait_drain(&bars[9], 0);
@@ -270,7 +292,6 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
       constexpr uint32_t idesc_k = tc::idesc_f32acc(1, 1, 1, 0, kR, 128);
       constexpr uint32_t idesc_kr = tc::idesc_f32acc(1, 1, 1, 0, kR, 64);
       const uint64_t ado = tc::sdesc_sw128(tc::smem_u32(do_s), 16, 1024);
-      const uint64_t bdk = tc::sdesc_sw128(tc::smem_u32(k_s), 16, 1024);
       const uint64_t aqt = tc::sdesc_sw128(tc::smem_u32(q_s), kHKB, 1024);
       const uint64_t adot = tc::sdesc_sw128(tc::smem_u32(do_s), kHKB, 1024);
       const uint64_t bdst = tc::sdesc_sw128(tc::smem_u32(dst_s), 16, 1024);
@@ -278,9 +299,11 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
       bool ok = nt == 0 || tc::mbar_wait(qfull, 0, abort_flag);
       for (int g = 0; g < steps && ok; ++g) {
         if (w5) {
-          if (!tc::mbar_wait(kfull, g & 1, abort_flag)) break;
+          const StageUse su = stage_use(g, nt);
+          if (!tc::mbar_wait(&kfull[su.st], su.u & 1, abort_flag)) break;
           if (g > 0 && !tc::mbar_wait(tfree, (g - 1) & 1, abort_flag)) break;
           tc::fence_after_sync();
+          const uint64_t bdk = tc::sdesc_sw128(tc::smem_u32(su.st ? k2_s : k_s), 16, 1024);
 #pragma unroll 1
           for (int kb = 0; kb < kKBV; ++kb)
 #pragma unroll
@@ -288,7 +311,7 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
               tc::mma_f16(tmem + kColDP, ado + kb * 512 + 2 * ko,
                           bdk + kb * (kTileKB >> 4) + 2 * ko, idesc_p, (kb > 0 || ko > 0) ? 1u : 0u);
           tc::mma_commit(sfull);
-          tc::mma_commit(kempty);
+          tc::mma_commit(&kempty[su.st]);
         }
         if (g < nt) continue;
         const int g2 = g - nt;
@@ -337,7 +360,7 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
       tc::fence_after_sync();
       // this tile's slots, before the columns are released: the gather may
       // rewrite the slot table once the next tile is under way
-      const int *sl = slot_s + (g & 1) * kR;
+      const int *sl = slot_s + (g & 3) * kR;
       int slots[kR];
 #pragma unroll
       for (int r = 0; r < kR; ++r) slots[r] = sl[r];
@@ -391,7 +414,7 @@ sparse_mla_bwd_tc_kernel(MlaBwdArgs a, const __grid_constant__ CUtensorMap qmap,
       float s[16], dp[16];
       tc::tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColS, s);
       tc::tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColDP, dp);
-      const int *sl = slot_s + (g & 1) * kR;
+      const int *sl = slot_s + (g & 3) * kR;
       float p[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
