@@ -538,7 +538,13 @@ int dsa_decode_host(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
   // overlapping the index score was measured slower: the wait for it cost the
   // top-k its early launch), then the step, then the outputs.  Pinned,
   // aligned host buffers are moved by two copy kernels (see SegBuilder),
-  // any other by the copy engines.
+  // any other by the copy engines.  Pinned, aligned out and lse buffers are
+  // written by the step itself through their device addresses (the last
+  // kernel's stores cross to host memory), so only the selection is copied
+  // back.
+  void *d_out = const_cast<void *>(mapped_host(h_out));
+  float *d_lse = static_cast<float *>(const_cast<void *>(mapped_host(h_lse)));
+  const bool direct_out = d_out && d_lse;
   SegBuilder in, out;
   in.add(h_q, S.q, (size_t)B * H * D * 2, true);
   if (k_swa > 0) in.add(h_idx_swa, S.idx_swa, (size_t)B * k_swa * 4, true);
@@ -548,8 +554,10 @@ int dsa_decode_host(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
   in.add(h_w, S.w, (size_t)B * H_I * 4, true);
   if (h_q_scale) in.add(h_q_scale, S.q_scale, (size_t)B * H_I * 4, true);
   if (h_idx_out) out.add(h_idx_out, S.idx_out, (size_t)B * k * 4, false);
-  out.add(h_out, S.out, (size_t)B * H * Dv * 2, false);
-  out.add(h_lse, S.lse, (size_t)B * H * 4, false);
+  if (!direct_out) {
+    out.add(h_out, S.out, (size_t)B * H * Dv * 2, false);
+    out.add(h_lse, S.lse, (size_t)B * H * 4, false);
+  }
   const bool kernels_io = in.ok && out.ok;
   bool ok = kernels_io ? in.launch(s) == cudaSuccess :
             cudaMemcpyAsync(S.q, h_q, (size_t)B * H * D * 2, cudaMemcpyHostToDevice, s) == cudaSuccess &&
@@ -565,13 +573,15 @@ int dsa_decode_host(const void *h_q_idx, int idx_dtype, const float *h_q_scale,
   st = decode_enqueue(S.q_idx, idx_dtype, h_q_scale ? S.q_scale : nullptr, k_idx, k_scale,
                       k_rows, S.w, H_I, d_idx, B, S.seq_lens, S.slot_base, max_seq_len, k, S.q,
                       H, D, Dv, softmax_scale, kv, kv_swa, k_swa > 0 ? S.idx_swa : nullptr, k_swa,
-                      S.idx_out, S.out, S.lse, S.dec_ws, err_flag, s);
+                      S.idx_out, direct_out ? d_out : S.out, direct_out ? d_lse : S.lse, S.dec_ws,
+                      err_flag, s);
   if (st != DSA_OK) return st;
   if (kernels_io) return status_of(out.launch(s));
   ok = (!h_idx_out || cudaMemcpyAsync(h_idx_out, S.idx_out, (size_t)B * k * 4,
                                       cudaMemcpyDeviceToHost, s) == cudaSuccess) &&
-       cudaMemcpyAsync(h_out, S.out, (size_t)B * H * Dv * 2, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
-       cudaMemcpyAsync(h_lse, S.lse, (size_t)B * H * 4, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+       (direct_out ||
+        (cudaMemcpyAsync(h_out, S.out, (size_t)B * H * Dv * 2, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+         cudaMemcpyAsync(h_lse, S.lse, (size_t)B * H * 4, cudaMemcpyDeviceToHost, s) == cudaSuccess));
   return ok ? DSA_OK : DSA_ERR_CUDA;
 }
 

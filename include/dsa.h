@@ -363,10 +363,13 @@ int dsa_decode_paged(const void *q_idx, int idx_dtype, const float *q_scale,
  * there: they must stay valid until then, as with cudaMemcpyAsync.  When
  * every given host buffer is page-locked (pinned, so the GPU reaches it at
  * its device-mapped address) and 16-byte aligned, two kernels move the data
- * (one gathers the inputs, one writes the outputs back), which avoids the
- * fixed cost of ten copy-engine transfers.  Otherwise each buffer is copied
- * with cudaMemcpyAsync; pageable memory is accepted and the CUDA runtime then
- * stages those copies itself.  Both give the same results bit for bit.
+ * (one gathers the inputs, one writes the selection back), which avoids the
+ * fixed cost of ten copy-engine transfers.  Whenever h_out and h_lse are
+ * pinned and 16-byte aligned, the step's last kernel writes them itself at
+ * their device-mapped addresses (no copy back for those two).  Otherwise
+ * each buffer is copied with cudaMemcpyAsync; pageable memory is accepted
+ * and the CUDA runtime then stages those copies itself.  All give the same
+ * results bit for bit.
  * Shapes, types and limits are those of dsa_decode.  err_flag, if given, is
  * a device pointer.  No host synchronisation: the outputs are in host memory
  * once `stream` has passed this call (e.g. after cudaStreamSynchronize).
