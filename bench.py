@@ -12,8 +12,11 @@ launching stream; between timed steps a 256 MiB buffer is written and a
 second 256 MiB buffer is read, so the L2 holds neither step inputs nor dirty
 lines whose write-back would be charged to the next step (the flush is
 outside the events).  A GPU-side sleep ahead of each timed loop lets the host
-queue its launches first, so host launch latency stays out of the events.  Multi-GPU runs (torchrun) are
-independent replicas: the path does not shard across GPUs.
+queue its launches first, so host launch latency stays out of the events.
+Beside these cold steps the line reports the same step warm (back to back,
+no flush: `warm_us`) and captured once into a CUDA graph (`graph_us`, cold).
+Multi-GPU runs (torchrun) are independent replicas: the path does not shard
+across GPUs.
 
 Prints one JSON line.  `--impl reference` times the CPU oracle instead (the
 reference arm), on a bounded sample of the same workload.
@@ -189,6 +192,26 @@ def run_ours(args, rank, world):
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     us_per_step = total_ms * 1000.0 / args.steps
 
+    # ---- beside the cold steps (the timed region above): the same fused step
+    # back to back without the L2 flush (warm), and the step captured once
+    # into a CUDA graph, each replay between events after an L2 flush
+    warm_us = statistics.median(_timed(step, args.steps, 1, lambda i: None))
+    graph_dev_us = None
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        gdev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gdev):
+            step()
+        graph_dev_us = statistics.median(_timed(gdev.replay, args.steps, 2, l2_flush))
+        del gdev
+    except RuntimeError as exc:    # reported, not fatal
+        graph_dev_us = "capture failed: %s" % str(exc).splitlines()[0][:120]
+
     # ---- staged pass: the three stages as separate entry points, events around each
     rs = case.slot_base
     re = (case.slot_base + case.seq_lens).contiguous()
@@ -329,6 +352,8 @@ def run_ours(args, rank, world):
         "step_roofline": {"achieved_gbs": round(step_gbs, 1), "frac": round(step_gbs / hbm_gbs, 4),
                           "algorithmic_bytes_per_step": step_bytes},
         "stages_us": {s: round(v, 2) for s, v in stage_us.items()},
+        "warm_us": round(warm_us, 3),
+        "graph_us": round(graph_dev_us, 3) if isinstance(graph_dev_us, float) else graph_dev_us,
         # e2e: the step through the library's public API from pinned host
         # buffers -- the captured step (dsa_decode_graph, one launch a step,
         # the way a decode loop runs it) and, beside it, the direct call
