@@ -491,20 +491,26 @@ def run_workload(args):
         Bq, Q, N = args.batch, 2, args.context
         case = I.multi_token_decode(Bq, Q, N, device=dev)
         ws = ops.workspace(ops.dsa_decode_workspace_size(case.B, N, case.k, case.H, case.Dv), dev)
-        fn = lambda: ops.decode_case(case, ws=ws)
+        # the step as a request's rows paired (rows_per_request = 2: one read of
+        # the request's keys for both rows), and beside it every row on its own
+        fn = lambda: ops.decode_case(case, ws=ws, rows_per_request=2)
+        fn1 = lambda: ops.decode_case(case, ws=ws)
         clocks.start()
         us = _timed(fn, args.steps, args.warmup, l2_flush)
         clk = clocks.stop()
         v = statistics.median(us)
+        v1 = statistics.median(_timed(fn1, args.steps, args.warmup, l2_flush))
         # unique bytes: each request's keys and scales once, the selected rows of
-        # every token, q/out/lse of every row; each row's index score reads its
-        # own key range, so the kernel moves Q times the key bytes
+        # every token, q/out/lse of every row (the paired step reads a request's
+        # keys once; one row at a time, Q times)
         nbytes = Bq * N * (128 + 4) + case.B * N * 4 + case.B * 2048 * 1152 + \
             case.B * case.H * (576 * 2 + 512 * 2 + 4)
         res.update({"value": round(v, 3), "ms_per_step": round(v / 1000, 6),
                     "dtype": "fp8_e4m3 indexer + bf16 attention (fp32 accumulate)",
                     "config": {"workload": case.name, "requests": Bq, "tokens_per_request": Q,
-                               "context": N, "topk": case.k, "heads": case.H},
+                               "context": N, "topk": case.k, "heads": case.H,
+                               "rows_per_request": 2},
+                    "single_rows_us": round(v1, 3),
                     "step_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": nbytes,
                                       "achieved_gbs": round(nbytes / (v * 1e-6) / 1e9, 1),
                                       "frac": round(nbytes / (v * 1e-6) / 1e9 / hbm_gbs, 4),

@@ -141,6 +141,7 @@ int decode_enqueue(const void *q_idx, int idx_dtype, const float *q_scale, const
   ia.scores = L.scores; ia.ld_scores = ld; ia.hist = L.topk.hist; ia.topk_k = k;
   ia.inputs_ready = 1;   // the inputs precede the whole call; only the zeroing precedes us
   ia.err_flag = err_flag;
+  ia.rows_per_unit = opts && opts->rows_per_request == 2 && !pages.table ? 2 : 1;
   e = index_score_launch(ia, s);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   e = topk_select(L.scores, ld, seq_lens, B, max_seq_len, k, pages.table ? nullptr : slot_base,
@@ -381,7 +382,7 @@ int dsa_sparse_mla_fwd_ex(const void *q, int T, int H, int D, int Dv, float soft
                           const dsa_kv_pool *kv_extra, const int32_t *idx_extra, int k2,
                           void *out, float *lse, void *ws, size_t ws_bytes, int32_t *err_flag,
                           const dsa_attn_opts *opts, dsa_stream_t stream) {
-  if (opts && opts->reserved != 0) return DSA_ERR_INVALID_ARG;
+  if (opts && opts->rows_per_request != 0) return DSA_ERR_INVALID_ARG;
   int st = check_mla_shape(q, T, H, D, Dv, softmax_scale, kv, idx, k, kv_extra, idx_extra, k2, out, lse);
   if (st != DSA_OK) return st;
   if (T == 0) return DSA_OK;
@@ -403,7 +404,7 @@ int dsa_sparse_mla_bwd(const void *q, int T, int H, int D, int Dv, float softmax
                        const dsa_kv_pool *kv, const int32_t *idx, int k, const float *lse,
                        const void *dout, const dsa_attn_opts *opts, float *dq, float *dkv,
                        float *dsinks, int32_t *err_flag, dsa_stream_t stream) {
-  if (opts && opts->reserved != 0) return DSA_ERR_INVALID_ARG;
+  if (opts && opts->rows_per_request != 0) return DSA_ERR_INVALID_ARG;
   if (T < 0 || k < 1) return DSA_ERR_INVALID_ARG;
   if (H < 1 || H > DSA_MAX_HEADS) return DSA_ERR_UNSUPPORTED;
   if (D != 576 || Dv != 512 || !kv || kv->format != DSA_KV_BF16) return DSA_ERR_UNSUPPORTED;
@@ -447,8 +448,16 @@ int dsa_decode_ex(const void *q_idx, int idx_dtype, const float *q_scale, const 
                   const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa, int32_t *idx_out,
                   void *out, float *lse, void *ws, size_t ws_bytes, int32_t *err_flag,
                   const dsa_attn_opts *opts, dsa_stream_t stream) {
-  if (opts && opts->reserved != 0) return DSA_ERR_INVALID_ARG;
+  const int rpr = opts ? opts->rows_per_request : 0;
+  if (rpr < 0 || rpr > 2) return DSA_ERR_UNSUPPORTED;
   if (B < 0 || max_seq_len < 0) return DSA_ERR_INVALID_ARG;
+  if (rpr == 2) {
+    // the paired index score: two rows of 64 heads at most, one 128-byte K-block
+    if (B % 2 != 0) return DSA_ERR_INVALID_ARG;
+    if (H_I > 64 || !((idx_dtype == DSA_IDX_FP8_E4M3 && d_idx == 128) ||
+                      (idx_dtype == DSA_IDX_BF16 && d_idx == 64)))
+      return DSA_ERR_UNSUPPORTED;
+  }
   if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
   int st = check_indexer(q_idx, idx_dtype, q_scale, k_idx, k_scale, k_rows, w, B, H_I, d_idx);
   if (st != DSA_OK) return st;
@@ -474,7 +483,7 @@ int dsa_decode_paged(const void *q_idx, int idx_dtype, const float *q_scale, con
                      const dsa_kv_pool *kv_swa, const int32_t *idx_swa, int k_swa,
                      int32_t *idx_out, void *out, float *lse, void *ws, size_t ws_bytes,
                      int32_t *err_flag, const dsa_attn_opts *opts, dsa_stream_t stream) {
-  if (opts && opts->reserved != 0) return DSA_ERR_INVALID_ARG;
+  if (opts && opts->rows_per_request != 0) return DSA_ERR_INVALID_ARG;
   if (B < 0 || max_seq_len < 0 || max_pages < 0) return DSA_ERR_INVALID_ARG;
   if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
   if (page_size < 64 || page_size % 64 != 0) return DSA_ERR_UNSUPPORTED;

@@ -68,6 +68,10 @@ struct IndexScoreArgs {
   const int32_t *block_table;  // or NULL
   int max_pages;
   int page_size;               // a multiple of 64
+  // 2: rows 2g and 2g + 1 share their keys (a request's two new tokens in a
+  // multi-token decode) and are scored together, each key tile read once;
+  // 0 or 1: every row on its own
+  int rows_per_unit;
 };
 cudaError_t index_score_launch(const IndexScoreArgs &a, cudaStream_t s);
 // The prefill form (row ranges, no histogram): groups of four consecutive

@@ -392,21 +392,21 @@ def decode_sweep(B: int, N: int, device="cpu", seed=0) -> DecodeCase:
 
 
 def multi_token_decode(B: int, Q: int, N: int, device="cpu", seed=0, k=2048, H=64,
-                       idx_kind="fp8") -> DecodeCase:
+                       idx_kind="fp8", d_idx=128) -> DecodeCase:
     """Decode with Q query tokens per request (speculative verification):
     request b's context has N positions, the last Q of them the new tokens.
     Query row b*Q + i is new token i: it sees positions [0, N - Q + 1 + i) of
     its request (causal among the new tokens) at the request's slots.  The
     rows share their request's slot base, so the fused decode serves them as
     B*Q rows.  Indexer 64 x 128 (fp8, or the bf16 integer grid), sparse MLA
-    H heads over bf16 576-wide rows."""
+    H heads over bf16 576-wide rows; d_idx the indexer's head width."""
     assert 1 <= Q <= N
     T = B * Q
     S_total = B * N
     if idx_kind == "fp8":
-        ind = indexer_fp8(T, S_total, 64, 128, seed, device)
+        ind = indexer_fp8(T, S_total, 64, d_idx, seed, device)
     else:
-        ind = indexer_grid_bf16(T, S_total, 64, 128, seed, device)
+        ind = indexer_grid_bf16(T, S_total, 64, d_idx, seed, device)
     kv = kv_bf16_pool(S_total, seed, 5, device)
     gq = _gen(seed, 4, device)
     q = to_bf16(torch.randn((T, H, 576), generator=gq, device=device)).contiguous()
@@ -414,7 +414,7 @@ def multi_token_decode(B: int, Q: int, N: int, device="cpu", seed=0, k=2048, H=6
     base = [b * N for b in range(B) for i in range(Q)]
     return DecodeCase("multi_token_b%d_q%d_n%d" % (B, Q, N), T,
                       torch.tensor(lens, dtype=torch.int32, device=device),
-                      torch.tensor(base, dtype=torch.int32, device=device), N, 64, 128, ind,
+                      torch.tensor(base, dtype=torch.int32, device=device), N, 64, d_idx, ind,
                       k, H, 576, 512, 1.0 / math.sqrt(192.0), q, kv,
                       meta={"requests": B, "tokens_per_request": Q})
 

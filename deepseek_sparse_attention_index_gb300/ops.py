@@ -40,7 +40,7 @@ class DsaKvPool(ctypes.Structure):
 
 
 class DsaAttnOpts(ctypes.Structure):
-    _fields_ = [("sinks", c_p), ("lse_log2", c_i32), ("reserved", c_i32)]
+    _fields_ = [("sinks", c_p), ("lse_log2", c_i32), ("rows_per_request", c_i32)]
 
 
 _SIGS = {
@@ -240,15 +240,16 @@ def dsa_sparse_mla_workspace_size(T, H, Dv, k, k2=0) -> int:
     return int(load().dsa_sparse_mla_workspace_size(T, H, Dv, k, k2))
 
 
-def _opts(sinks, lse_log2):
-    """Attention options: per-head sink logits (a CUDA fp32 [H] tensor) and the
-    lse in log2 units; None when neither is asked for."""
-    if sinks is None and not lse_log2:
+def _opts(sinks, lse_log2, rows_per_request=0):
+    """Attention and step options: per-head sink logits (a CUDA fp32 [H]
+    tensor), the lse in log2 units, and (dsa_decode_ex) the rows a request
+    contributes; None when none is asked for."""
+    if sinks is None and not lse_log2 and not rows_per_request:
         return None
     o = DsaAttnOpts()
     o.sinks = None if sinks is None else _ptr(sinks).value
     o.lse_log2 = 1 if lse_log2 else 0
-    o.reserved = 0
+    o.rows_per_request = int(rows_per_request)
     return o
 
 
@@ -313,9 +314,9 @@ def dsa_decode_workspace_size(B, max_seq_len, k, H, Dv, k_swa=0) -> int:
 def dsa_decode(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, slot_base,
                max_seq_len: int, k: int, q, softmax_scale: float, kv: _inp.KVPool,
                kv_swa=None, idx_swa=None, idx_out=None, out=None, lse=None, ws=None,
-               err_flag=None, sinks=None, lse_log2=False):
-    """One fused decode step (see dsa_decode; sinks and lse_log2 as
-    dsa_attn_opts).  Returns (idx_out, out, lse)."""
+               err_flag=None, sinks=None, lse_log2=False, rows_per_request=0):
+    """One fused decode step (see dsa_decode; sinks, lse_log2 and
+    rows_per_request as dsa_attn_opts).  Returns (idx_out, out, lse)."""
     B, H_I, d_idx = q_idx.shape
     _, H, D = q.shape
     Dv = kv.d_nope if kv.format != _inp.KV_BF16 else 512
@@ -335,7 +336,7 @@ def dsa_decode(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, slot_base
             _ptr(w), H_I, d_idx, B, _ptr(seq_lens), _ptr(slot_base), int(max_seq_len), k, _ptr(q),
             H, D, Dv, float(softmax_scale), _ref(s1), _ref(s2), _ptr(idx_swa), k_swa,
             _ptr(idx_out), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _ptr(err_flag))
-    o = _opts(sinks, lse_log2)
+    o = _opts(sinks, lse_log2, rows_per_request)
     if o is None:
         st = load().dsa_decode(*args, _stream())
     else:
@@ -476,7 +477,8 @@ def dsa_decode_paged(q_idx, idx_dtype, q_scale, k_idx, k_scale, w, seq_lens, blo
     return idx_out, out, lse
 
 
-def decode_case(case: _inp.DecodeCase, ws=None, err_flag=None, idx_out=None, out=None, lse=None):
+def decode_case(case: _inp.DecodeCase, ws=None, err_flag=None, idx_out=None, out=None, lse=None,
+                rows_per_request=0):
     """dsa_decode on a generated DecodeCase."""
     ind = case.indexer
     if case.meta.get("block_table") is not None:
@@ -488,7 +490,8 @@ def decode_case(case: _inp.DecodeCase, ws=None, err_flag=None, idx_out=None, out
     return dsa_decode(ind["q_idx"], ind["idx_dtype"], ind["q_scale"], ind["k_idx"], ind["k_scale"],
                       ind["w"], case.seq_lens, case.slot_base, case.max_seq_len, case.k, case.q,
                       case.softmax_scale, case.kv, case.kv_swa, case.idx_swa, idx_out=idx_out,
-                      out=out, lse=lse, ws=ws, err_flag=err_flag)
+                      out=out, lse=lse, ws=ws, err_flag=err_flag,
+                      rows_per_request=rows_per_request)
 
 
 def selftest_wait_timeout():

@@ -235,7 +235,8 @@ int dsa_sparse_mla_fwd(const void *q, int T, int H, int D, int Dv, float softmax
                        int32_t *err_flag, dsa_stream_t stream);
 
 /*
- * Attention options (dsa_sparse_mla_fwd_ex, dsa_decode_ex; NULL: none).
+ * Attention and step options (dsa_sparse_mla_fwd_ex, dsa_sparse_mla_bwd,
+ * dsa_decode_ex, dsa_decode_paged; NULL: none).
  *   sinks     device fp32 [H] or NULL: per-head sink logits.  A sink is one
  *             more logit in every softmax denominator of its head, in the
  *             units of the scores s_j = softmax_scale * q . K_j, with no
@@ -245,12 +246,23 @@ int dsa_sparse_mla_fwd(const void *q, int T, int H, int D, int Dv, float softmax
  *             no valid entry then gets out = 0 and lse = sink.
  *   lse_log2  nonzero: lse is reported in log2 units (the natural-log lse
  *             divided by ln 2), the form those notes hand to the backward.
- *   reserved  0 (else DSA_ERR_INVALID_ARG).
+ *   rows_per_request  dsa_decode_ex only (0 elsewhere, else
+ *             DSA_ERR_INVALID_ARG).  0 or 1: every row is its own request.
+ *             2: rows 2r and 2r+1 are two new tokens of one request (a
+ *             multi-token decode: speculative verification), so they share
+ *             their context start (slot_base[2r] == slot_base[2r+1]) and
+ *             their index scores are computed together, each key tile read
+ *             once for both rows.  Results are the same bit for bit as
+ *             with 0.  Needs an even B, H_I <= 64 and an fp8 indexer with
+ *             d_idx = 128 or a bf16 one with d_idx = 64 (else
+ *             DSA_ERR_UNSUPPORTED); a pair whose starts differ is reported
+ *             (DSA_DEVERR_INDEX_RANGE) and its scores are not computed.
+ *             Other values: DSA_ERR_UNSUPPORTED.
  */
 typedef struct dsa_attn_opts {
   const float *sinks;
   int32_t lse_log2;
-  int32_t reserved;
+  int32_t rows_per_request;
 } dsa_attn_opts;
 
 /* dsa_sparse_mla_fwd with attention options (opts may be NULL). */

@@ -118,19 +118,33 @@ def test_workspace_sizes_grow_with_the_problem(lib):
     assert b >= 32 * (1 << 17) * 4   # the score rows live in the workspace
 
 
-def _opts(reserved=0, lse_log2=0):
+def _opts(rows_per_request=0, lse_log2=0):
     o = ops.DsaAttnOpts()
     o.sinks = None
     o.lse_log2 = lse_log2
-    o.reserved = reserved
+    o.rows_per_request = rows_per_request
     return o
 
 
-def test_attention_options_reserved_field_must_be_zero(lib):
+def test_rows_per_request_is_a_decode_option_only(lib):
     st = lib.dsa_sparse_mla_fwd_ex(FAKE, 2, 8, 576, 512, 0.1, ctypes.byref(_pool(0, d_nope=512)),
                                    FAKE, 4, None, None, 0, FAKE, FAKE, FAKE, 1 << 30, None,
-                                   ctypes.byref(_opts(reserved=1)), None)
+                                   ctypes.byref(_opts(rows_per_request=2)), None)
     assert st == 1
+
+
+def test_decode_rows_per_request_checks(lib):
+    def call(rpr, B=4, idx_dtype=1, H_I=64, d=128):
+        return lib.dsa_decode_ex(FAKE, idx_dtype, FAKE, FAKE, FAKE, 1 << 20, FAKE, H_I, d, B,
+                                 FAKE, FAKE, 1000, 64, FAKE, 8, 576, 512, 0.1,
+                                 ctypes.byref(_pool(0, rows=1 << 20, d_nope=512)), None, None, 0,
+                                 None, FAKE, FAKE, FAKE, 1 << 34, None,
+                                 ctypes.byref(_opts(rows_per_request=rpr)), None)
+    assert call(3) == 2                  # pairs only
+    assert call(-1) == 2
+    assert call(2, B=3) == 1             # rows come in pairs
+    assert call(2, H_I=128) == 2         # two rows of at most 64 heads
+    assert call(2, idx_dtype=0, d=128) == 2   # bf16 indexer: d = 64 only
 
 
 def test_decode_paged_rejects_bad_arguments(lib):
@@ -145,7 +159,7 @@ def test_decode_paged_rejects_bad_arguments(lib):
     assert call(max_pages=3) == 1       # 3 x 64 < max_seq_len
     assert call(bt=None) == 1           # no block table
     assert call(k=0) == 2
-    assert call(opts=_opts(reserved=7)) == 1
+    assert call(opts=_opts(rows_per_request=2)) == 1
 
 
 def test_sparse_mla_backward_rejects_bad_arguments(lib):

@@ -535,6 +535,38 @@ def test_multi_token_decode_grid_bit_exact():
     _check_decode(case, idx, out, lse, range(case.B), bit_exact=True)
 
 
+def _pairs_equal_single_rows(case, check_rows=(), bit_exact=False):
+    """The paired index score (rows_per_request = 2) against the one-row path:
+    the same selection, output and lse bit for bit; then the oracle."""
+    flag = _flag()
+    idx1, out1, lse1 = ops.decode_case(case, err_flag=flag)
+    idx2, out2, lse2 = ops.decode_case(case, err_flag=flag, rows_per_request=2)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    assert torch.equal(idx1, idx2)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1.view(torch.int32), lse2.view(torch.int32))
+    if check_rows:
+        _check_decode(case, idx2, out2, lse2, check_rows, bit_exact=bit_exact)
+
+
+def test_multi_token_decode_pairs_equal_single_rows():
+    case = I.multi_token_decode(5, 2, 20000, device="cuda", seed=3)
+    _pairs_equal_single_rows(case, range(case.B))
+
+
+def test_multi_token_decode_pairs_grid_bit_exact():
+    # bf16 indexer of 64-wide heads (the pair path's other layout), integer grid
+    case = I.multi_token_decode(3, 2, 5000, device="cuda", idx_kind="bf16_grid", d_idx=64)
+    _pairs_equal_single_rows(case, range(case.B), bit_exact=True)
+
+
+def test_multi_token_decode_pairs_full_size():
+    """32 requests x 2 new tokens at 131072 positions (the mtp bench workload)."""
+    case = I.multi_token_decode(32, 2, 131072, device="cuda")
+    _pairs_equal_single_rows(case, [0, 1, 63])
+
+
 def test_decode_sweep_full_size_sampled():
     """Batch 32 x 128k context, the bench workload; three requests checked."""
     case = I.decode_sweep(32, 131072, device="cuda")
