@@ -273,8 +273,6 @@ struct ResolveSmem {
   uint32_t sh[kHistBins];
   uint32_t run_pre[kThreads];    // ordered start of each run of a group of chunks
   uint32_t run_at[kThreads];     // where that run sits in the list
-  uint32_t ph_at[kThreads];      // the runs sorted by where they sit in the list:
-  uint32_t ph_pre[kThreads];     //   list start and ordered (position-order) start
   uint32_t warp_sums[32];
   int s_bin;
   uint32_t s_before;
@@ -401,28 +399,17 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
   uint2 run0 = make_uint2(0u, 0u);
   if (!src.from_row && (int)threadIdx.x < min(nch, kThreads)) run0 = __ldcg(rt + threadIdx.x);
   // With the list copied and at most kThreads chunks, the copy is made in
-  // position order: run c (chunk c) starts at the ordered offset pre(c), and
-  // a list slot i finds its run by a binary search over the runs sorted by
-  // list start (an empty run sorts last and is never found).
+  // position order: run c (chunk c) goes to the ordered offsets [pre(c),
+  // pre(c + 1)), pre by a block scan in chunk order (so already sorted), and
+  // ordered slot o takes the entry at its run's list start plus o - pre(c),
+  // its run found by a binary search over pre (an empty run shares its pre
+  // with the next run and is never the last one at or before o).
   const bool ordered = to_cache && nch <= kThreads;
-  int n_runs = 0;
   if (ordered) {
     uint32_t tot_runs;
     const uint32_t pre = block_excl_scan(run0.y, S.warp_sums, &tot_runs);
-    const uint32_t at = ((int)threadIdx.x < nch && run0.y > 0) ? run0.x : 0xffffffffu;
-    S.run_at[threadIdx.x] = at;
+    S.run_at[threadIdx.x] = run0.x;
     S.run_pre[threadIdx.x] = pre;
-    __syncthreads();
-    if ((int)threadIdx.x < nch) {
-      int rank = 0;   // position of this run among the runs sorted by (list start, chunk)
-      for (int c2 = 0; c2 < nch; ++c2) {
-        const uint32_t a2 = S.run_at[c2];
-        rank += (a2 < at || (a2 == at && c2 < (int)threadIdx.x)) ? 1 : 0;
-      }
-      S.ph_at[rank] = at;
-      S.ph_pre[rank] = pre;
-    }
-    for (int c2 = 0; c2 < nch; ++c2) n_runs += S.run_at[c2] != 0xffffffffu ? 1 : 0;
     __syncthreads();
   }
 
@@ -434,26 +421,27 @@ __device__ __noinline__ void resolve_row(int t, ResolveSmem &S, uint2 *lc, uint3
     int32_t pos[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      const int64_t i = i0 + (int64_t)j * kThreads + threadIdx.x;
+      const int64_t i = i0 + (int64_t)j * kThreads + threadIdx.x;   // ordered slot, if ordered
       key[j] = 0;
       pos[j] = -1;                       // -1: past the end
-      if (i < src.n) src.get(i, key[j], pos[j]);
+      if (i < src.n) {
+        if (ordered) {
+          int lo = 0, hi = nch;          // the last run c with pre(c) <= i
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (S.run_pre[mid] <= (uint32_t)i) lo = mid; else hi = mid;
+          }
+          src.get(S.run_at[lo] + ((uint32_t)i - S.run_pre[lo]), key[j], pos[j]);
+        } else {
+          src.get(i, key[j], pos[j]);
+        }
+      }
     }
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int64_t i = i0 + (int64_t)j * kThreads + threadIdx.x;
       if (pos[j] >= 0) {
-        if (ordered) {
-          // the run holding list slot i: the last one starting at or before i
-          int lo = 0, hi = n_runs;
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (S.ph_at[mid] <= (uint32_t)i) lo = mid; else hi = mid;
-          }
-          lc[S.ph_pre[lo] + ((uint32_t)i - S.ph_at[lo])] = make_uint2(key[j], (uint32_t)pos[j]);
-        } else if (to_cache) {
-          lc[i] = make_uint2(key[j], (uint32_t)pos[j]);
-        }
+        if (to_cache) lc[i] = make_uint2(key[j], (uint32_t)pos[j]);
         if ((key[j] >> 20) == b1) atomicAdd(&sh[(key[j] >> 8) & 0xFFFu], 1u);
       }
     }
