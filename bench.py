@@ -454,7 +454,7 @@ def run_workload(args):
         # 2.5 times the forward's 2 * H * 1088 flops per (token, row)
         flop = 2.5 * 2.0 * H * 1088 * rows
         res.update({"value": round(v, 3), "ms_per_step": round(v / 1000, 6),
-                    "dtype": "bf16 inputs, fp32 arithmetic (SIMT)",
+                    "dtype": "bf16 operands on the tensor cores (P and dS as bf16 hi + lo terms), fp32 accumulate",
                     "config": {"workload": "sparse_mla_bwd_T%d_H%d" % (T, H), "tokens": T,
                                "heads": H, "topk": case.k},
                     "roofline": {"bound": "tensor", "unit": "TFLOP/s",

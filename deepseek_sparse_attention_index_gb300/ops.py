@@ -25,6 +25,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "dsa.h")
 DSA_OK = 0
 DEVERR_INDEX_RANGE = 1
 DEVERR_TIMEOUT = 2
+DEVERR_FP16_RANGE = 4
 MAX_TOPK = 2048
 
 c_p = ctypes.c_void_p

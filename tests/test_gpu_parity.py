@@ -403,6 +403,35 @@ def test_sparse_mla_masks_and_flags_out_of_range_entries():
     check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "masked")
 
 
+
+def test_sparse_mla_uniform_extreme_scales_and_fp16_range():
+    # Group scales far outside the workload's 2^[-4, 4] (2^-17, 2^-10,
+    # 2^-6.9, 143, 200: products from fp16 subnormals to near its largest
+    # values) still agree with the oracle; a scale that carries x s past
+    # fp16's range is reported.
+    pool, idx, q, D = _mla_case(I.KV_FP8_UNIFORM, 3, 64, 300, all_neg_row=False)
+    sel = torch.unique(idx[idx >= 0])
+    sc = pool.scales
+    sc[sel[0::3], 2] = 2.0 ** -17
+    sc[sel[1::5], 5] = 200.0
+    sc[sel[2::7], 0] = 2.0 ** -10
+    sc[sel[3::7], 3] = 2.0 ** -6.9
+    sc[sel[4::9], 6] = 143.0
+    scale = 1 / math.sqrt(512.0)
+    flag = _flag()
+    out, lse = ops.dsa_sparse_mla_fwd(q, scale, pool, idx, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(pool), raw(idx), scale,
+                                    out.shape[2])
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "scales")
+    sc[sel[4], 1] = 2.0 ** 17     # any |x| > 0.5 in that group leaves fp16's range
+    flag = _flag()
+    ops.dsa_sparse_mla_fwd(q, scale, pool, idx, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() & ops.DEVERR_FP16_RANGE
+
+
 # ---------------------------------------------------------------- fused decode
 
 def _check_decode(case, idx_gpu, out_gpu, lse_gpu, requests, bit_exact=False):
