@@ -259,6 +259,53 @@ def test_sparse_mla_sinks(fmt, H, k, T):
     assert torch.equal(lse[1].cpu(), sinks.cpu())
 
 
+
+def _vmax(pool, idx, Dv):
+    """[T, 1, Dv]: the largest |V[d]| over each token's valid selected rows."""
+    pnp, ix = pool_np(pool), raw(idx)
+    vm = np.zeros((ix.shape[0], 1, Dv))
+    for t in range(ix.shape[0]):
+        sl = ix[t][ix[t] >= 0].astype(np.int64)
+        if sl.size:
+            vm[t, 0] = np.abs(O.kv_rows(pnp, sl)[:, :Dv]).max(axis=0)
+    return vm
+
+
+@pytest.mark.parametrize("fmt,T,H,k", [(I.KV_BF16, 32, 64, 2048),      # 4 pieces a token
+                                       (I.KV_BF16, 40, 64, 600),       # 3 pieces
+                                       (I.KV_BF16, 64, 32, 300),       # 2 pieces, 32 heads
+                                       (I.KV_FP8_UNIFORM, 32, 64, 1152),
+                                       (I.KV_FP8_DS_MLA, 40, 16, 700)])
+def test_sparse_mla_few_pieces_a_token(fmt, T, H, k):
+    # Batches of 32-76 tokens split each list into 2-4 pieces (one wave of
+    # CTAs), whose partials the combine merges: with sinks and log2 lse, and
+    # a token whose list is all -1 (its pieces are empty: no value, lse = the
+    # sink).  The packed pool is held to its logit-error bound
+    # (tests/parity.py): at these batch sizes some of its small output
+    # elements exceed the unit-scale one.
+    pool, idx, q, D = _mla_case(fmt, T, H, k)
+    scale = 1 / math.sqrt(192.0) if D == 576 else 1 / math.sqrt(512.0)
+    Dv = 512 if D == 576 else 448
+    # the pieces a token, read off the partials' workspace (T x pieces x H records)
+    pieces = round(ops.dsa_sparse_mla_workspace_size(T, H, Dv, k) / (T * H * (Dv + 1) * 4))
+    assert 2 <= pieces <= 4, pieces
+    ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(pool), raw(idx), scale, Dv)
+    vmax = _vmax(pool, idx, Dv) if fmt == I.KV_FP8_DS_MLA else None
+    flag = _flag()
+    out, lse = ops.dsa_sparse_mla_fwd(q, scale, pool, idx, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, "pieces",
+                  lse_tol=lse_tol(fmt), vmax=vmax)
+    sinks = _sinks(H)
+    out, lse = ops.dsa_sparse_mla_fwd(q, scale, pool, idx, sinks=sinks, lse_log2=True)
+    ref_out, ref_lse = O.sparse_mla(O.decode_bf16(raw(q)), pool_np(pool), raw(idx), scale,
+                                    out.shape[2], sinks=sinks.double().cpu().numpy())
+    check_out_lse(out.float().cpu().numpy(), lse.cpu().numpy() * math.log(2.0), ref_out, ref_lse,
+                  "pieces+sinks", lse_tol=lse_tol(fmt), vmax=vmax)
+    assert (out[1] == 0).all()
+    assert torch.allclose(lse[1].cpu() * math.log(2.0), sinks.cpu(), rtol=1e-6, atol=1e-6)
+
 def test_sparse_mla_lse_log2():
     pool, idx, q, D = _mla_case(I.KV_BF16, 3, 64, 700)
     scale = 1 / math.sqrt(192.0)
