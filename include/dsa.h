@@ -47,7 +47,7 @@ typedef struct CUstream_st *dsa_stream_t; /* a cudaStream_t */
 enum {
   DSA_OK = 0,
   DSA_ERR_INVALID_ARG = 1,         /* null pointer, bad size or range   */
-  DSA_ERR_UNSUPPORTED = 2,         /* shape / format this build lacks   */
+  DSA_ERR_UNSUPPORTED = 2,         /* shape / format not supported       */
   DSA_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes below *_workspace_size() */
   DSA_ERR_CUDA = 4                 /* a launch or driver call failed    */
 };
@@ -81,7 +81,7 @@ enum {
                              exponents + 1 pad; NoPE x = fp8 * 2^(e - 127)   */
 };
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define DSA_MAX_TOPK 2048     /* k of dsa_topk / dsa_decode                 */
 #define DSA_MAX_INDEX_HEADS 64
 #define DSA_MAX_HEADS 128     /* H of dsa_sparse_mla_fwd                    */
