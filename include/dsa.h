@@ -47,7 +47,7 @@ typedef struct CUstream_st *dsa_stream_t; /* a cudaStream_t */
 enum {
   DSA_OK = 0,
   DSA_ERR_INVALID_ARG = 1,         /* null pointer, bad size or range   */
-  DSA_ERR_UNSUPPORTED = 2,         /* shape / format not supported       */
+  DSA_ERR_UNSUPPORTED = 2,         /* shape / format not supported      */
   DSA_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes below *_workspace_size() */
   DSA_ERR_CUDA = 4                 /* a launch or driver call failed    */
 };
