@@ -238,39 +238,58 @@ sparse_mla_simt_kernel(MlaArgs a) {
 }
 
 // Merge split partials.  A warp per (token, head) record, or, for a call with
-// few records (a single-token decode: 64 records), a warp per quarter of a
-// record, so that such a call still has a few hundred warps.  Lane l holds
-// the float4 columns l + 32 c of its part.  The splits are folded in batches
-// whose loads -- lse values and partial columns alike -- are all issued
-// before any is used, into a running maximum and sum; a call with at most
-// one batch of splits (4 a record-warp, 16 a quarter-warp, whose lanes hold
-// one column each) waits for one round of L2 latency.
+// few records (a single-token decode: 64 records), a CTA of eight warps per
+// record: a warp per quarter of the columns and half of the splits, the two
+// halves then merged through shared memory, so that such a call still has a
+// few hundred warps and up to 32 splits wait for one round of L2 latency.
+// Lane l holds the float4 columns l + 32 c of its part.  The splits are
+// folded in batches whose loads -- lse values and partial columns alike --
+// are all issued before any is used, into a running maximum and sum; a call
+// with at most one batch of splits (4 a record-warp, 16 a quarter-warp, whose
+// lanes hold one column each) waits for one round of L2 latency.
 constexpr int kMaxSplits = 256;
 
 constexpr int kCombineWarps = 8;     // warps per 256-thread CTA
 constexpr int kFewRecords = 512;     // at most this many records: four warps a record
 
-template <int QPR>   // warps per record: 1 or 4
+template <int QPR>   // column parts per record: 1 (a warp a record) or 4 (a CTA a record)
 __global__ void __launch_bounds__(32 * kCombineWarps)
 mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse, int T,
                    int H, int Dv, int n_splits, __nv_bfloat16 *__restrict__ out,
                    float *__restrict__ lse, const float *__restrict__ sinks, int lse_log2) {
   constexpr int CPL = 4 / QPR;                   // float4 columns a lane holds
   constexpr int kCombineBatch = QPR == 4 ? 16 : 4;   // splits whose loads are in flight together
+  constexpr int SH = QPR == 4 ? kCombineWarps / QPR : 1;   // split halves (QPR 4: a CTA a record)
+  static_assert(QPR == 1 || SH == 2, "a few-record CTA holds four parts x two halves");
+  __shared__ float4 x_acc[QPR == 4 ? QPR * 32 : 1];   // the second half's sums, by part and lane
+  __shared__ float x_m[QPR], x_t[QPR];
   pdl_wait();      // the partials come from the previous kernel
-  const int64_t w = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
-  if (w >= (int64_t)T * H * QPR) return;
   const int lane = threadIdx.x & 31;
-  const int64_t r = w / QPR;                     // record (t, h)
-  const int part = (int)(w - r * QPR);
+  int64_t r;                                     // record (t, h)
+  int part, half;
+  if (QPR == 4) {
+    r = blockIdx.x;                              // one CTA a record, warps = parts x halves
+    if (r >= (int64_t)T * H) return;             // whole CTA
+    part = (threadIdx.x >> 5) & 3;
+    half = (threadIdx.x >> 5) >> 2;
+  } else {
+    const int64_t w = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    if (w >= (int64_t)T * H) return;
+    r = w;
+    part = 0;
+    half = 0;
+  }
   const int64_t t = r / H, h = r - t * H;
   const int nf = Dv >> 2;                        // float4 columns of a record
   const int f0 = 32 * CPL * part + lane;         // this lane's columns: f0 + 32 c
+  // this warp's splits: [s0, s1)
+  const int hs = (n_splits + SH - 1) / SH;
+  const int s0 = min(n_splits, half * hs), s1 = min(n_splits, s0 + hs);
   float mx = -INFINITY, tot = 0.f;
   float4 acc[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i0 = 0; i0 < n_splits; i0 += kCombineBatch) {
+  for (int i0 = s0; i0 < s1; i0 += kCombineBatch) {
     float li[kCombineBatch];
     float4 v[kCombineBatch][CPL];
 #pragma unroll
@@ -279,7 +298,7 @@ mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ p
       li[b] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < CPL; ++c) v[b][c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < n_splits) {
+      if (i < s1) {
         const int64_t rec = (t * n_splits + i) * H + h;
         li[b] = __ldcg(part_lse + rec);
 #pragma unroll
@@ -313,6 +332,31 @@ mla_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ p
       }
     }
     mx = bm;
+  }
+  if (QPR == 4) {
+    // the second half hands its (max, sum, columns) to the first
+    if (half == 1) {
+      x_acc[part * 32 + lane] = acc[0];
+      if (lane == 0) {
+        x_m[part] = mx;
+        x_t[part] = tot;
+      }
+    }
+    __syncthreads();
+    if (half == 1) return;
+    const float m1 = x_m[part], t1 = x_t[part];
+    const float4 a1 = x_acc[part * 32 + lane];
+    const float M = fmaxf(mx, m1);
+    if (M != -INFINITY) {
+      const float sc0 = mx == -INFINITY ? 0.f : __expf(mx - M);
+      const float sc1 = m1 == -INFINITY ? 0.f : __expf(m1 - M);
+      tot = tot * sc0 + t1 * sc1;
+      acc[0].x = fmaf(acc[0].x, sc0, a1.x * sc1);
+      acc[0].y = fmaf(acc[0].y, sc0, a1.y * sc1);
+      acc[0].z = fmaf(acc[0].z, sc0, a1.z * sc1);
+      acc[0].w = fmaf(acc[0].w, sc0, a1.w * sc1);
+      mx = M;
+    }
   }
   if (sinks) {
     // the head's sink joins the denominator (no value): rescale to a maximum
@@ -397,7 +441,8 @@ cudaError_t sparse_mla_launch(const MlaArgs &a, cudaStream_t s) {
   if (e != cudaSuccess || a.n_splits == 1) return e;
   const int64_t recs = (int64_t)a.T * a.H;
   const bool few = recs <= kFewRecords;
-  const int64_t warps = recs * (few ? 4 : 1);
+  // few records: a CTA of kCombineWarps warps each (see mla_combine_kernel)
+  const int64_t warps = recs * (few ? kCombineWarps : 1);
   return launch_pdl(few ? mla_combine_kernel<4> : mla_combine_kernel<1>,
                     dim3((unsigned)((warps + kCombineWarps - 1) / kCombineWarps)),
                     dim3(32 * kCombineWarps), 0, s, (const float *)a.part_o,
